@@ -1,0 +1,404 @@
+"""Benchmark of the sparse-weight direct convolution forward on GB300.
+
+One step = one forward of one seeded synthetic layer (default: the ResNet-style
+3x3 layer, N=1, C=M=256, 14x14, 90 % unstructured sparsity) through the C ABI
+(spconv_forward), inputs resident in HBM.  The packing (spconv_pack) runs once
+per weight set before timing, as in deployment, and is reported separately.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
+device synchronize; each step flushes L2 (a 256 MiB write, outside the timed
+events) and is timed with CUDA events on the launching stream.  Rank 0 prints
+one JSON line.  --impl reference times the CPU oracle (the only other
+implementation of this path) on the host cores on the same layer.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+from sparse_weight_direct_gb300 import roofline  # noqa: E402
+
+METRIC = "µs/layer and dense-equivalent TFLOP/s at 90–99% sparsity; % of roofline"
+UNIT = "µs/layer"
+FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
+SM_COUNT_NOMINAL = 152
+FP32_LANES_PER_SM = 128
+KERNEL_SOURCE = os.path.join(ROOT, "sparse_weight_direct_gb300", "csrc", "spconv_fwd.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def fp32_peak_flops(sm_count: int, sm_mhz: float) -> float:
+    """CUDA-core fp32 peak: SMs x 128 FMA lanes x 2 FLOP x clock."""
+    return sm_count * FP32_LANES_PER_SM * 2.0 * sm_mhz * 1e6
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for p in (KERNEL_SOURCE,):
+        with open(p, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(config: str):
+    """DRAM bytes per launch from an ncu capture of this exact kernel source,
+    or None (no capture, or the kernel changed since)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    sha = kernel_sha()
+    with open(TRAFFIC_FILE) as fh:
+        for line in fh:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == config \
+                    and parts[1] == sha:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def layer_numbers(L, nnz: int):
+    E, F = L.E, L.F
+    return {
+        "useful_flop": roofline.useful_flops(nnz, L.N, E, F),
+        "dense_flop": roofline.dense_equiv_flops(L.N, E, F, L.M, L.C, L.R, L.S),
+        "alg_bytes": roofline.algorithmic_bytes(L.N, L.C, L.H, L.W, L.M, E, F, nnz),
+    }
+
+
+def describe(L):
+    return {"workload": L.name, "N": L.N, "C": L.C, "H": L.H, "W": L.W, "M": L.M,
+            "R": L.R, "S": L.S, "stride": L.stride, "pad": L.pad,
+            "sparsity": round(1 - L.density, 4), "rows": L.rows,
+            "l2": "flushed between timed steps (256 MiB write)"}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline leg)
+# --------------------------------------------------------------------------
+
+def time_oracle(L, rowptr, colidx, value, x, budget_s: float, steps: int = 1):
+    """Time oracle.csr on a bounded sample of the layer: the first n images and
+    first m output channels, sized so `steps` repeats fit in budget_s.
+    Returns (us_per_layer, threads, sample_description, per-step seconds)."""
+    import oracle
+    # calibrate on one image and a slice of channels
+    m_cal = max(1, min(L.M, 16))
+    t0 = time.perf_counter()
+    _, _, threads = oracle.csr(x[:1], rowptr[:m_cal + 1], colidx[:rowptr[m_cal]],
+                               value[:rowptr[m_cal]], m_cal, L.R, L.S, L.stride, L.pad,
+                               return_threads=True)
+    t_cal = max(time.perf_counter() - t0, 1e-6)
+    nnz_cal = max(int(rowptr[m_cal]), 1)
+    per_nnz_img = t_cal / nnz_cal
+    full = per_nnz_img * int(rowptr[-1]) * L.N
+    target = max(budget_s / max(steps, 1), 1e-4)
+    if full <= target:
+        n_s, m_s = L.N, L.M
+    else:
+        n_s = max(1, min(L.N, int(target / (per_nnz_img * int(rowptr[-1])))))
+        if n_s > 1 or per_nnz_img * int(rowptr[-1]) <= target:
+            m_s = L.M
+        else:
+            frac = target / (per_nnz_img * int(rowptr[-1]))
+            m_s = max(1, min(L.M, int(L.M * frac)))
+    nnz_s = int(rowptr[m_s])
+    xs = x[:n_s]
+    args = (rowptr[:m_s + 1], colidx[:nnz_s], value[:nnz_s], m_s, L.R, L.S, L.stride, L.pad)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.csr(xs, *args)
+        times.append(time.perf_counter() - t0)
+    t_step = statistics.mean(times)
+    scale = (int(rowptr[-1]) * L.N) / max(nnz_s * n_s, 1)
+    us_layer = t_step * scale * 1e6
+    sample = (f"oracle_csr (fp64) on images [0,{n_s}) x output channels [0,{m_s}) of "
+              f"{L.name} ({nnz_s * n_s} of {int(rowptr[-1]) * L.N} nonzero-image pairs), "
+              f"scaled to one layer; {steps} timed repeat(s)")
+    return us_layer, threads, sample, times
+
+
+def run_reference(args, L):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    rowptr, colidx, value = workloads.make_weights(L)
+    x = workloads.make_input(L)
+    budget = min(120.0, max(5.0, 0.02 * (args.steps + args.warmup)))
+    # warm-up repeats are untimed
+    if args.warmup:
+        time_oracle(L, rowptr, colidx, value, x, budget * args.warmup /
+                    max(args.steps + args.warmup, 1), steps=1)
+    us, threads, sample, times = time_oracle(L, rowptr, colidx, value, x, budget,
+                                             steps=args.steps)
+    nnz = int(rowptr[-1])
+    num = layer_numbers(L, nnz)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": describe(L),
+        "dense_equiv_tflops": num["dense_flop"] / (us * 1e-6) / 1e12,
+        "useful_gflops": num["useful_flop"] / (us * 1e-6) / 1e9,
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
+# The CUDA path
+# --------------------------------------------------------------------------
+
+def run_ours(args, L):
+    import torch
+    import torch.distributed as dist
+    import sparse_weight_direct_gb300 as swd
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    rowptr, colidx, value = workloads.make_weights(L)
+    x_host = workloads.make_input(L)
+    nnz = int(rowptr[-1])
+    stream = torch.cuda.Stream(device=dev)
+
+    t0 = time.perf_counter()
+    w = swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
+                 stride=L.stride, pad=L.pad, stream=stream)
+    pack_ms = (time.perf_counter() - t0) * 1e3
+    info = w.info()
+
+    x = torch.from_numpy(x_host).to(dev)
+    y = torch.empty((L.N, L.M, L.E, L.F), device=dev, dtype=torch.float32)
+    flush = torch.empty(FLUSH_BYTES // 4, device=dev, dtype=torch.float32)
+    x_pin = torch.from_numpy(x_host).pin_memory()
+    y_pin = torch.empty(tuple(y.shape), dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            swd.forward(x, w, out=y, stream=stream)
+        torch.cuda.synchronize(dev)
+
+        # ---- device-timed region: inputs resident in HBM ----
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        clocks = ClockSampler(local)
+        clocks.start()
+        time.sleep(0.25)
+        barrier()
+        torch.cuda.synchronize(dev)
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            swd.forward(x, w, out=y, stream=stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        wall = time.perf_counter() - wall0
+        clk = clocks.stop()
+        per = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
+        total_ms = sum(per)
+
+        # ---- end to end through the public API with host buffers ----
+        e2e_steps = max(3, min(args.steps, 200))
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+        for i in range(e2e_steps + 2):
+            flush.zero_()
+            if i >= 2:
+                es[i - 2].record(stream)
+            x.copy_(x_pin, non_blocking=True)
+            swd.forward(x, w, out=y, stream=stream)
+            y_pin.copy_(y, non_blocking=True)
+            if i >= 2:
+                ee[i - 2].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e2e_steps
+
+    # max over ranks
+    t_rank = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_rank, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = float(t_rank[0]), float(t_rank[1])
+
+    ms_step = total_ms / args.steps
+    us_layer = total_ms * 1e3 / (args.steps * world)        # whole-job µs per layer
+    us_kernel = ms_step * 1e3                                 # one launch on one GPU
+    num = layer_numbers(L, nnz)
+    peaks, peak_kind = measured_peaks()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    p_fp32 = fp32_peak_flops(sm_count, float(peaks.get("sm_max_mhz", 2070.0)))
+    bw = float(peaks["hbm_gbs"]) * 1e9
+    t_comp = num["useful_flop"] / p_fp32
+    t_comm = num["alg_bytes"] / bw
+    if t_comp >= t_comm:
+        achieved = num["useful_flop"] / (us_kernel * 1e-6) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": p_fp32 / 1e12, "unit": "TFLOP/s",
+                "frac": achieved / (p_fp32 / 1e12),
+                "peak_source": f"{sm_count} SMs x 128 fp32 lanes x 2 x "
+                               f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz ({peak_kind} clock)"}
+    else:
+        achieved = num["alg_bytes"] / (us_kernel * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": bw / 1e9, "unit": "GB/s",
+                "frac": achieved / (bw / 1e9), "peak_source": f"hbm_gbs ({peak_kind})"}
+    traffic = recorded_traffic(L.name)
+    roof["traffic"] = traffic
+    roof["algorithmic"] = num["alg_bytes"]
+    roof["kernel"] = "spconv_fwd_kernel"
+    roof["roofline_us"] = max(t_comp, t_comm) * 1e6
+
+    line = {
+        "metric": METRIC, "value": us_layer, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic", "config": describe(L),
+        "dense_equiv_tflops": num["dense_flop"] / (us_kernel * 1e-6) / 1e12,
+        "useful_gflops": num["useful_flop"] / (us_kernel * 1e-6) / 1e9,
+        "alg_gbs": num["alg_bytes"] / (us_kernel * 1e-6) / 1e9,
+        "us_per_launch": {"median": statistics.median(per) * 1e3,
+                          "mean": ms_step * 1e3,
+                          "sem": (statistics.stdev(per) / len(per) ** 0.5 * 1e3)
+                          if len(per) > 1 else 0.0},
+        "nnz": nnz, "pack_ms": pack_ms,
+        "tiling": {k: info[k] for k in ("tile_rows", "tiles_y", "tiles_x", "chunk",
+                                         "num_chunks", "slots_per_warp", "groups",
+                                         "smem_bytes")},
+        "roofline": roof,
+        "e2e": {"value": e2e_ms * 1e3 / world, "unit": UNIT,
+                "h2d_bytes_per_step": int(x_host.nbytes),
+                "d2h_bytes_per_step": int(y.numel() * 4)},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        us_cpu, threads, sample, _ = time_oracle(L, rowptr, colidx, value, x_host,
+                                                 budget_s=args.cpu_budget, steps=3)
+        line["cpu_baseline"] = {"value": us_cpu, "unit": UNIT, "cores": threads,
+                                "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    w.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default=workloads.BENCH_DEFAULT, choices=sorted(workloads.LAYERS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline leg")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    L = workloads.LAYERS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, L)
+    return run_ours(args, L)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

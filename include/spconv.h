@@ -1,0 +1,162 @@
+/*
+ * spconv.h -- C ABI of libspconv: forward 2-D convolution of a dense NCHW fp32
+ * activation tensor with unstructured-sparse (pruned) weights, computed
+ * directly on the GPU (GB300, sm_103a) without materialising an im2col matrix.
+ *
+ * Operation (Tuteja et al., "Theoretical and Empirical Analysis of Sparse
+ * Convolution", Sec. 3 Eq.(1)-(3); Escoin, arXiv 1802.10280, "Sparse
+ * convolution", Algorithm 2):
+ *
+ *   Y[n,m,e,f] = sum over nonzeros j of row m of value[j] *
+ *                X[n, c_j, e*stride + r_j - pad, f*stride + s_j - pad]
+ *
+ * with X taken as zero outside [0,H) x [0,W) (symmetric zero padding, no
+ * kernel flip), E = floor((H + 2*pad - R)/stride) + 1 and likewise F (Eq.(2)).
+ * The weights are the M x (C*R*S) lowered filter matrix (Escoin Fig. 3) held
+ * in CSR (Escoin, "Sparse weights": rowptr[M+1], colidx[nnz], value[nnz]);
+ * colidx = (c*R + r)*S + s.
+ *
+ * Conventions shared by every call:
+ *  - Return value: SPCONV_OK (0) or a negative spconv_status.  No call aborts,
+ *    throws or prints; spconv_status_string() names a status.
+ *  - Tensors are contiguous row-major: X is N x C x H x W, Y is N x M x E x F,
+ *    both float32 in device memory of the device that was current when the
+ *    handle was packed.
+ *  - "stream" is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - All shape arguments are int; sizes are validated before any device work.
+ */
+#ifndef SPCONV_H
+#define SPCONV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum spconv_status {
+    SPCONV_OK = 0,
+    SPCONV_ERR_INVALID_ARG = -1, /* bad shape, NULL pointer, misaligned buffer     */
+    SPCONV_ERR_BAD_CSR = -2,     /* rowptr not monotone / colidx out of range / dup */
+    SPCONV_ERR_UNSUPPORTED = -3, /* shape beyond what the kernels were built for     */
+    SPCONV_ERR_ALLOC = -4,       /* host or device allocation failed                 */
+    SPCONV_ERR_CUDA = -5,        /* a CUDA runtime call or kernel launch failed      */
+    SPCONV_ERR_MISMATCH = -6     /* forward shape/device differs from the packed one */
+} spconv_status;
+
+/* Opaque handle of a packed weight set.  Owned by the library from
+ * spconv_pack / spconv_pack_host until spconv_packed_free. */
+typedef struct spconv_packed spconv_packed;
+
+/*
+ * spconv_pack -- CSR -> packed device layout (once per weight set).
+ *
+ * Follows Escoin's "weight stretching" (the column index of every nonzero is
+ * rewritten once, ahead of time, into an offset into the input array, relying
+ * on the layout function f(c, y+r, x+s) = f(c,y,x) + f(0,r,s)) and the per
+ * output channel offset array of Tuteja et al. Sec. 5.3.  Here each nonzero
+ * becomes an 8-byte entry (fp32 value, int32 offset into the shared-memory
+ * input tile the kernel stages), entries are grouped per output channel and
+ * input-channel chunk, and output channels are binned by nonzero count onto
+ * warps (longest-first onto the least-loaded warp).
+ *
+ * Inputs (host memory, caller-owned, only read during the call):
+ *   C, H, W      input channels and spatial size of the layer (>= 1)
+ *   M            output channels (rows of the CSR matrix, >= 1)
+ *   R, S         kernel height and width (>= 1); stride >= 1; pad >= 0;
+ *                the output extent E, F must be >= 1
+ *   rowptr[M+1]  rowptr[0] == 0, non-decreasing; nnz = rowptr[M] < 2^31
+ *   colidx[nnz]  column in [0, C*R*S); any order within a row; no duplicates
+ *   value[nnz]   fp32 weights (explicit zeros are allowed)
+ *   stream       stream for the upload; the call waits for it before returning
+ * Output: *out receives a new handle (device buffers on the current device).
+ * Errors: INVALID_ARG, BAD_CSR, UNSUPPORTED, ALLOC, CUDA; *out is untouched.
+ */
+int spconv_pack(int C, int H, int W, int M, int R, int S, int stride, int pad,
+                const int32_t *rowptr, const int32_t *colidx, const float *value,
+                void *stream, spconv_packed **out);
+
+/*
+ * spconv_forward -- Y = conv(X, packed weights); the hot path.
+ *
+ * Launches the sparse direct convolution kernel on `stream` and returns
+ * without synchronising.  Y is overwritten (no accumulation, no bias).
+ * An output channel whose CSR row is empty is written as zeros.
+ *   N                 batch size (>= 0; N == 0 is a no-op)
+ *   C,H,W,M,R,S,stride,pad   must equal the values given to spconv_pack
+ *   input   device pointer, N*C*H*W floats, 16-byte aligned
+ *   packed  handle from spconv_pack (read-only; may be shared by concurrent
+ *           forwards on different streams)
+ *   output  device pointer, N*M*E*F floats, 4-byte aligned, not overlapping input
+ * Errors: INVALID_ARG (NULL/misaligned/negative N), MISMATCH (shape or current
+ * device differs from the handle's), UNSUPPORTED, CUDA (launch failure).
+ * Inputs are expected to be finite.
+ */
+int spconv_forward(int N, int C, int H, int W, int M, int R, int S, int stride, int pad,
+                   const float *input, const spconv_packed *packed, float *output,
+                   void *stream);
+
+/* Frees the handle and its device buffers.  NULL-safe.  The caller must make
+ * sure no forward that uses the handle is still running. */
+void spconv_packed_free(spconv_packed *p);
+
+/* Static, never-NULL description of a status code. */
+const char *spconv_status_string(int status);
+
+/*
+ * spconv_pack_host -- the same packing as spconv_pack, kept in host memory
+ * only (no device work, no GPU needed).  The handle can be inspected with
+ * spconv_packed_info / spconv_packed_copy_array; spconv_forward rejects it
+ * with SPCONV_ERR_MISMATCH.  Same arguments and errors as spconv_pack.
+ */
+int spconv_pack_host(int C, int H, int W, int M, int R, int S, int stride, int pad,
+                     const int32_t *rowptr, const int32_t *colidx, const float *value,
+                     spconv_packed **out);
+
+/* Geometry and sizes of a packed handle (all counts are plain integers). */
+typedef struct spconv_packed_info {
+    int32_t C, H, W, M, R, S, stride, pad, E, F;
+    int64_t nnz;            /* nonzeros of the CSR input                        */
+    int64_t entries;        /* packed (value, offset) entries (== nnz)          */
+    int32_t tile_rows;      /* output rows per tile (per lane)                  */
+    int32_t tile_cols;      /* output columns per tile (one per lane: 32)       */
+    int32_t tiles_y, tiles_x;
+    int32_t in_rows;        /* staged input rows per channel (with halo)        */
+    int32_t in_cols;        /* staged input columns per channel (with halo)     */
+    int32_t phase_pitch;    /* words per stride-phase sub-row                   */
+    int32_t row_pitch;      /* words per staged input row (= stride*phase_pitch)*/
+    int32_t plane;          /* words per staged channel                         */
+    int32_t chunk;          /* input channels staged at once                    */
+    int32_t num_chunks;
+    int32_t slots_per_warp; /* output channels a warp carries at once           */
+    int32_t warps;          /* warps per block                                  */
+    int32_t groups;         /* output-channel groups (blocks along grid y)      */
+    int32_t num_slots;      /* groups * warps * slots_per_warp                  */
+    int32_t on_device;      /* 1 if device buffers exist (spconv_pack)          */
+    int64_t device_bytes;   /* bytes of device memory held by the handle        */
+    int64_t smem_bytes;     /* dynamic shared memory per block of the forward   */
+    int64_t max_warp_nnz;   /* heaviest warp's total entries (balance metric)   */
+    int64_t mean_warp_nnz;  /* mean over non-empty warps, rounded down          */
+} spconv_packed_info;
+
+int spconv_packed_info_get(const spconv_packed *p, spconv_packed_info *info);
+
+/* Which host-side array spconv_packed_copy_array copies. */
+typedef enum spconv_array {
+    SPCONV_ARRAY_ENTRIES = 0, /* entries x {float value, int32 offset}, 8 B each    */
+    SPCONV_ARRAY_SEGPTR = 1,  /* int32 [num_slots * (num_chunks + 1)]: entry index  */
+                              /* where slot s's chunk k starts ([.., k+1] ends it)  */
+    SPCONV_ARRAY_SLOT_OC = 2  /* int32 [num_slots]: output channel of a slot or -1  */
+} spconv_array;
+
+/* Copies one packed array into dst (host, dst_bytes long).  *needed (if not
+ * NULL) receives the array's size in bytes.  INVALID_ARG if dst_bytes is too
+ * small (dst may be NULL to query the size). */
+int spconv_packed_copy_array(const spconv_packed *p, int which, void *dst, int64_t dst_bytes,
+                             int64_t *needed);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPCONV_H */

@@ -1,3 +1,155 @@
-"""sparse_weight_direct_gb300: direct 2-D convolution with unstructured-sparse
-weights on GB300 (sm_103a).  The compute path lives in ``libspconv.so``; this
-package is a thin ctypes binding plus host-side accounting helpers."""
+"""sparse_weight_direct_gb300 -- direct 2-D convolution with unstructured-sparse
+weights on GB300 (sm_103a).
+
+The whole computation runs in ``libspconv.so`` (hand-written CUDA behind the C
+ABI of ``include/spconv.h``).  This package only marshals arguments: it passes
+raw pointers, sizes and a stream to the library.  PyTorch provides device
+memory and streams; no step of the convolution runs in Python or PyTorch, and
+there is no CPU fallback -- if the library is missing, every call raises.
+
+    from sparse_weight_direct_gb300 import pack, forward
+    w = pack(rowptr, colidx, value, C=..., H=..., W=..., M=..., R=3, S=3,
+             stride=1, pad=1)
+    y = forward(x_cuda, w)            # x: (N, C, H, W) float32 on the GPU
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import _lib
+from ._lib import SpconvError, status_string
+
+__all__ = ["pack", "pack_host", "forward", "PackedWeights", "SpconvError", "status_string",
+           "out_extent", "library_path"]
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def out_extent(size: int, k: int, stride: int, pad: int) -> int:
+    """Output extent, floor((size + 2*pad - k) / stride) + 1."""
+    return (size + 2 * pad - k) // stride + 1
+
+
+class PackedWeights:
+    """Owner of a ``spconv_packed`` handle (freed on close / garbage collection)."""
+
+    def __init__(self, handle: ctypes.c_void_p, shape: dict):
+        self._h = handle
+        self.shape = shape  # C, H, W, M, R, S, stride, pad
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if not self._h:
+            raise SpconvError(_lib.SPCONV_ERR_INVALID_ARG, "packed weights already freed")
+        return self._h
+
+    def info(self) -> dict:
+        info = _lib.PackedInfo()
+        _lib.check(_lib.lib().spconv_packed_info_get(self.handle, ctypes.byref(info)),
+                   "spconv_packed_info_get")
+        return {name: getattr(info, name) for name, _ in _lib.PackedInfo._fields_}
+
+    def array(self, which: str) -> np.ndarray:
+        """Copy of a packed host array: 'entries' (structured value/off),
+        'segptr' or 'slot_oc'."""
+        code = {"entries": 0, "segptr": 1, "slot_oc": 2}[which]
+        need = ctypes.c_int64(0)
+        L = _lib.lib()
+        _lib.check(L.spconv_packed_copy_array(self.handle, code, None, 0, ctypes.byref(need)),
+                   "spconv_packed_copy_array")
+        if which == "entries":
+            out = np.zeros(need.value // 8, dtype=[("value", "<f4"), ("off", "<i4")])
+        else:
+            out = np.zeros(need.value // 4, dtype=np.int32)
+        _lib.check(L.spconv_packed_copy_array(self.handle, code, out.ctypes.data_as(ctypes.c_void_p),
+                                              out.nbytes, None), "spconv_packed_copy_array")
+        return out
+
+    def close(self) -> None:
+        if self._h:
+            _lib.lib().spconv_packed_free(self._h)
+            self._h = None
+
+    def __del__(self):  # pragma: no cover - best effort
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _csr_arrays(rowptr, colidx, value):
+    rowptr = np.ascontiguousarray(np.asarray(rowptr, dtype=np.int32))
+    colidx = np.ascontiguousarray(np.asarray(colidx, dtype=np.int32))
+    value = np.ascontiguousarray(np.asarray(value, dtype=np.float32))
+    return rowptr, colidx, value
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def pack(rowptr, colidx, value, *, C: int, H: int, W: int, M: int, R: int, S: int,
+         stride: int = 1, pad: int = 0, stream=None) -> PackedWeights:
+    """CSR (host arrays) -> packed device layout on the current CUDA device."""
+    rowptr, colidx, value = _csr_arrays(rowptr, colidx, value)
+    if rowptr.size != M + 1:
+        raise SpconvError(_lib.SPCONV_ERR_INVALID_ARG, "rowptr must have M + 1 entries")
+    h = ctypes.c_void_p()
+    _lib.check(_lib.lib().spconv_pack(C, H, W, M, R, S, stride, pad, _ptr(rowptr), _ptr(colidx),
+                                      _ptr(value), _stream_ptr(stream), ctypes.byref(h)),
+               "spconv_pack")
+    return PackedWeights(h, dict(C=C, H=H, W=W, M=M, R=R, S=S, stride=stride, pad=pad))
+
+
+def pack_host(rowptr, colidx, value, *, C: int, H: int, W: int, M: int, R: int, S: int,
+              stride: int = 1, pad: int = 0) -> PackedWeights:
+    """The same packing kept in host memory only (inspection; needs no GPU)."""
+    rowptr, colidx, value = _csr_arrays(rowptr, colidx, value)
+    if rowptr.size != M + 1:
+        raise SpconvError(_lib.SPCONV_ERR_INVALID_ARG, "rowptr must have M + 1 entries")
+    h = ctypes.c_void_p()
+    _lib.check(_lib.lib().spconv_pack_host(C, H, W, M, R, S, stride, pad, _ptr(rowptr),
+                                           _ptr(colidx), _ptr(value), ctypes.byref(h)),
+               "spconv_pack_host")
+    return PackedWeights(h, dict(C=C, H=H, W=W, M=M, R=R, S=S, stride=stride, pad=pad))
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        if not torch.cuda.is_available():
+            return None
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def forward(x, packed: PackedWeights, out=None, stream=None):
+    """Y = conv(x, packed) on the GPU.  x: (N, C, H, W) contiguous float32
+    CUDA tensor; out (optional): (N, M, E, F) float32 CUDA tensor, overwritten.
+    Asynchronous on ``stream`` (default: the current torch stream)."""
+    import torch
+    sh = packed.shape
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32
+            and x.dim() == 4 and x.is_contiguous()):
+        raise SpconvError(_lib.SPCONV_ERR_INVALID_ARG,
+                          "x must be a contiguous 4-D float32 CUDA tensor")
+    N = x.shape[0]
+    E = out_extent(sh["H"], sh["R"], sh["stride"], sh["pad"])
+    F = out_extent(sh["W"], sh["S"], sh["stride"], sh["pad"])
+    if out is None:
+        out = torch.empty((N, sh["M"], E, F), device=x.device, dtype=torch.float32)
+    elif not (out.is_cuda and out.dtype == torch.float32 and out.is_contiguous()
+              and tuple(out.shape) == (N, sh["M"], E, F)):
+        raise SpconvError(_lib.SPCONV_ERR_INVALID_ARG, "out has the wrong shape/dtype/layout")
+    rc = _lib.lib().spconv_forward(N, x.shape[1], x.shape[2], x.shape[3], sh["M"], sh["R"],
+                                   sh["S"], sh["stride"], sh["pad"],
+                                   ctypes.c_void_p(x.data_ptr()), packed.handle,
+                                   ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream))
+    _lib.check(rc, "spconv_forward")
+    return out

@@ -1,0 +1,91 @@
+"""ctypes loader for libspconv.so (argument marshalling only).
+
+The library is built in-tree by ``sparse_weight_direct_gb300/build.py`` (the
+repository's ``__graft_entry__.build()`` calls it).  If it is missing, loading
+raises: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libspconv.so")
+
+SPCONV_OK = 0
+SPCONV_ERR_INVALID_ARG = -1
+SPCONV_ERR_BAD_CSR = -2
+SPCONV_ERR_UNSUPPORTED = -3
+SPCONV_ERR_ALLOC = -4
+SPCONV_ERR_CUDA = -5
+SPCONV_ERR_MISMATCH = -6
+
+# Every symbol include/spconv.h declares.
+EXPORTS = ("spconv_pack", "spconv_forward", "spconv_packed_free", "spconv_status_string",
+           "spconv_pack_host", "spconv_packed_info_get", "spconv_packed_copy_array")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpconvError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})" if what
+                         else f"{status_string(status)} (status {status})")
+
+
+class PackedInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("C", "H", "W", "M", "R", "S", "stride", "pad", "E", "F")] + [
+        ("nnz", ctypes.c_int64), ("entries", ctypes.c_int64)] + [
+        (n, ctypes.c_int32) for n in
+        ("tile_rows", "tile_cols", "tiles_y", "tiles_x", "in_rows", "in_cols", "phase_pitch",
+         "row_pitch", "plane", "chunk", "num_chunks", "slots_per_warp", "warps", "groups",
+         "num_slots", "on_device")] + [
+        (n, ctypes.c_int64) for n in
+        ("device_bytes", "smem_bytes", "max_warp_nnz", "mean_warp_nnz")]
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; "
+                f"g.build()'` (or python sparse_weight_direct_gb300/build.py); "
+                "there is no CPU fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        i, p = ctypes.c_int, ctypes.c_void_p
+        L.spconv_pack.argtypes = [i] * 8 + [p, p, p, p, ctypes.POINTER(ctypes.c_void_p)]
+        L.spconv_pack.restype = i
+        L.spconv_pack_host.argtypes = [i] * 8 + [p, p, p, ctypes.POINTER(ctypes.c_void_p)]
+        L.spconv_pack_host.restype = i
+        L.spconv_forward.argtypes = [i] * 9 + [p, p, p, p]
+        L.spconv_forward.restype = i
+        L.spconv_packed_free.argtypes = [p]
+        L.spconv_packed_free.restype = None
+        L.spconv_status_string.argtypes = [i]
+        L.spconv_status_string.restype = ctypes.c_char_p
+        L.spconv_packed_info_get.argtypes = [p, ctypes.POINTER(PackedInfo)]
+        L.spconv_packed_info_get.restype = i
+        L.spconv_packed_copy_array.argtypes = [p, i, p, ctypes.c_int64,
+                                               ctypes.POINTER(ctypes.c_int64)]
+        L.spconv_packed_copy_array.restype = i
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().spconv_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def check(rc: int, what: str) -> None:
+    if rc != SPCONV_OK:
+        raise SpconvError(rc, what)

@@ -25,3 +25,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built_library():
+    """Build libspconv.so (and the oracle) in-tree if missing or stale; the
+    library itself never falls back to anything when it is absent."""
+    from sparse_weight_direct_gb300 import build as b
+    b.build()
+    yield

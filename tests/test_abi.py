@@ -1,0 +1,180 @@
+"""Host-side tests of the C ABI (no GPU): the library loads and exports every
+symbol include/spconv.h declares, argument validation, and the packed layout
+(weight stretching + output-channel binning) decodes back to the CSR input."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads
+import sparse_weight_direct_gb300 as swd
+from sparse_weight_direct_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "spconv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spconv_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert set(names) == set(_lib.EXPORTS)
+    L = _lib.lib()
+    for n in names:
+        assert getattr(L, n) is not None
+    # nothing else is exported
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", swd.library_path()],
+                         capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert {e for e in exported if e.startswith("spconv")} == set(names)
+
+
+def test_status_strings():
+    for code in range(-6, 1):
+        s = swd.status_string(code)
+        assert s and "unknown" not in s
+    assert "unknown" in swd.status_string(-99)
+
+
+def _pack_host(L, rowptr, colidx, value):
+    return swd.pack_host(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
+                         stride=L.stride, pad=L.pad)
+
+
+def decode_layout(w):
+    """Rebuild {m: sorted [(colidx, value)]} from the packed arrays."""
+    info = w.info()
+    ent = w.array("entries")
+    seg = w.array("segptr").reshape(info["num_slots"], info["num_chunks"] + 1)
+    slot_oc = w.array("slot_oc")
+    st, R, S = info["stride"], info["R"], info["S"]
+    rows = {}
+    for slot, m in enumerate(slot_oc):
+        if m < 0:
+            assert seg[slot, 0] == seg[slot, -1]
+            continue
+        assert np.all(np.diff(seg[slot]) >= 0)
+        items = []
+        for k in range(info["num_chunks"]):
+            for e in ent[seg[slot, k]:seg[slot, k + 1]]:
+                off = int(e["off"])
+                cl, rem = divmod(off, info["plane"])
+                r, rem = divmod(rem, info["row_pitch"])
+                phase, q = divmod(rem, info["phase_pitch"])
+                s = q * st + phase
+                assert 0 <= cl < info["chunk"] and r < R and s < S and phase < st
+                c = k * info["chunk"] + cl
+                assert c < info["C"]
+                items.append(((c * R + r) * S + s, float(e["value"])))
+        rows[int(m)] = sorted(items)
+    return info, rows, slot_oc
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_int", "resnet3x3", "vgg3x3", "sweep90",
+                                  "sweep99", "alex11x11", "conv5x5"])
+def test_packed_layout_decodes_to_csr(name):
+    L = workloads.LAYERS[name]
+    rowptr, colidx, value = workloads.make_weights(L)
+    w = _pack_host(L, rowptr, colidx, value)
+    info, rows, slot_oc = decode_layout(w)
+    assert info["on_device"] == 0 and info["nnz"] == colidx.size == info["entries"]
+    assert info["E"] == L.E and info["F"] == L.F
+    assert info["num_slots"] == info["groups"] * info["warps"] * info["slots_per_warp"]
+    # every output channel sits in exactly one slot
+    used = slot_oc[slot_oc >= 0]
+    assert sorted(used.tolist()) == list(range(L.M))
+    for m in range(L.M):
+        lo, hi = rowptr[m], rowptr[m + 1]
+        want = sorted(zip(colidx[lo:hi].tolist(), value[lo:hi].astype(np.float64).tolist()))
+        assert rows[m] == want
+    # staged input tile covers every tap of every output of a tile
+    assert info["in_rows"] == (info["tile_rows"] - 1) * L.stride + L.R
+    assert info["in_cols"] == (info["tile_cols"] - 1) * L.stride + L.S
+    assert info["tiles_y"] * info["tile_rows"] >= L.E
+    assert info["tiles_x"] * info["tile_cols"] >= L.F
+    assert info["smem_bytes"] <= 200 * 1024
+    w.close()
+
+
+def test_binning_balances_warps():
+    # lognormal rows: longest-first onto the least-loaded warp keeps the
+    # heaviest warp within one row of the mean
+    L = workloads.LAYERS["sweep90"]
+    rowptr, colidx, value = workloads.make_weights(L)
+    w = _pack_host(L, rowptr, colidx, value)
+    info = w.info()
+    longest = int(np.diff(rowptr).max())
+    assert info["max_warp_nnz"] <= info["mean_warp_nnz"] + longest
+    w.close()
+
+
+def test_unsorted_columns_pack_like_sorted():
+    rng = np.random.default_rng(0)
+    M, C, R = 12, 5, 3
+    rowptr, colidx, value = workloads.random_csr(M, C * R * R, 0.3, rng)
+    perm_cols = colidx.copy()
+    perm_vals = value.copy()
+    for m in range(M):
+        lo, hi = rowptr[m], rowptr[m + 1]
+        p = rng.permutation(hi - lo)
+        perm_cols[lo:hi] = colidx[lo:hi][p]
+        perm_vals[lo:hi] = value[lo:hi][p]
+    kw = dict(C=C, H=9, W=9, M=M, R=R, S=R, stride=1, pad=1)
+    a = swd.pack_host(rowptr, colidx, value, **kw)
+    b = swd.pack_host(rowptr, perm_cols, perm_vals, **kw)
+    for k in ("entries", "segptr", "slot_oc"):
+        np.testing.assert_array_equal(a.array(k), b.array(k))
+
+
+def _status_of(**kw):
+    base = dict(rowptr=np.array([0, 1], np.int32), colidx=np.array([0], np.int32),
+                value=np.array([1.0], np.float32), C=1, H=5, W=5, M=1, R=3, S=3, stride=1,
+                pad=1)
+    base.update(kw)
+    try:
+        swd.pack_host(base.pop("rowptr"), base.pop("colidx"), base.pop("value"), **base).close()
+        return 0
+    except swd.SpconvError as e:
+        return e.status
+
+
+def test_pack_validation():
+    assert _status_of() == 0
+    assert _status_of(rowptr=np.array([1, 1], np.int32)) == _lib.SPCONV_ERR_BAD_CSR
+    assert _status_of(rowptr=np.array([0, 2, 1], np.int32), M=2) == _lib.SPCONV_ERR_BAD_CSR
+    assert _status_of(colidx=np.array([9], np.int32)) == _lib.SPCONV_ERR_BAD_CSR
+    assert _status_of(colidx=np.array([-1], np.int32)) == _lib.SPCONV_ERR_BAD_CSR
+    assert _status_of(rowptr=np.array([0, 2], np.int32), colidx=np.array([4, 4], np.int32),
+                      value=np.array([1, 2], np.float32)) == _lib.SPCONV_ERR_BAD_CSR
+    assert _status_of(C=0) == _lib.SPCONV_ERR_INVALID_ARG
+    assert _status_of(stride=0) == _lib.SPCONV_ERR_INVALID_ARG
+    assert _status_of(pad=-1) == _lib.SPCONV_ERR_INVALID_ARG
+    assert _status_of(H=1, pad=0) == _lib.SPCONV_ERR_INVALID_ARG  # E < 1
+    assert _status_of(stride=1000) == _lib.SPCONV_ERR_UNSUPPORTED
+    # explicit zero weights and empty rows are fine
+    assert _status_of(value=np.array([0.0], np.float32)) == 0
+    assert _status_of(rowptr=np.array([0, 0], np.int32), colidx=np.zeros(0, np.int32),
+                      value=np.zeros(0, np.float32)) == 0
+
+
+def test_forward_rejects_host_only_handle_and_null():
+    L = _lib.lib()
+    rowptr = np.array([0, 1], np.int32)
+    w = swd.pack_host(rowptr, np.array([4], np.int32), np.array([1.0], np.float32),
+                      C=1, H=5, W=5, M=1, R=3, S=3, stride=1, pad=1)
+    rc = L.spconv_forward(1, 1, 5, 5, 1, 3, 3, 1, 1, None, w.handle, None, None)
+    assert rc == _lib.SPCONV_ERR_MISMATCH
+    rc = L.spconv_forward(1, 1, 5, 5, 2, 3, 3, 1, 1, None, w.handle, None, None)
+    assert rc == _lib.SPCONV_ERR_MISMATCH
+    rc = L.spconv_forward(1, 1, 5, 5, 1, 3, 3, 1, 1, None, None, None, None)
+    assert rc == _lib.SPCONV_ERR_INVALID_ARG
+    L.spconv_packed_free(None)
+    info = _lib.PackedInfo()
+    assert L.spconv_packed_info_get(None, ctypes.byref(info)) == _lib.SPCONV_ERR_INVALID_ARG
+    w.close()

@@ -1,0 +1,188 @@
+"""GPU parity: spconv_forward (CUDA, through the C ABI) against the CPU oracle,
+element by element, on the seeded layers and on edge cases.
+
+Rule (fp32 layers): |gpu - oracle| <= 1e-5 * sum|w*x| + 1e-7 per output, the
+oracle in fp64.  Integer-valued layers: bit-exact (every fp32 partial sum is
+an exact integer below 2^24, so any summation order gives the same result).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+import sparse_weight_direct_gb300 as swd
+
+torch = pytest.importorskip("torch")
+
+RTOL = 1e-5
+ATOL = 1e-7
+
+
+def run_gpu(x, rowptr, colidx, value, C, H, W, M, R, S, stride, pad, stream=None,
+            prefill=float("nan")):
+    w = swd.pack(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=R, S=S, stride=stride, pad=pad)
+    xd = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    E = swd.out_extent(H, R, stride, pad)
+    F = swd.out_extent(W, S, stride, pad)
+    out = torch.full((x.shape[0], M, E, F), prefill, device="cuda", dtype=torch.float32)
+    swd.forward(xd, w, out=out, stream=stream)
+    torch.cuda.synchronize()
+    w.close()
+    return out.cpu().numpy().astype(np.float64)
+
+
+def check(got, ref, mag, exact=False, what=""):
+    assert got.shape == ref.shape, what
+    if exact:
+        bad = got != ref
+    else:
+        bad = ~(np.abs(got - ref) <= RTOL * mag + ATOL)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outputs off; first at "
+                             f"{tuple(i)}: gpu={got[tuple(i)]!r} oracle={ref[tuple(i)]!r} "
+                             f"abs_sum={mag[tuple(i)]!r}")
+
+
+def layer_case(L, N=None):
+    rowptr, colidx, value = workloads.make_weights(L)
+    x = workloads.make_input(L, N)
+    got = run_gpu(x, rowptr, colidx, value, L.C, L.H, L.W, L.M, L.R, L.S, L.stride, L.pad)
+    ref, mag = oracle.csr(x, rowptr, colidx, value, L.M, L.R, L.S, L.stride, L.pad)
+    check(got, ref, mag, exact=L.integer, what=L.name)
+    return got, ref, mag
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", list(workloads.LAYERS))
+def test_layer_full_size(name):
+    """Every seeded layer at its full size (the benchmark's launch shape)."""
+    layer_case(workloads.LAYERS[name])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["resnet3x3", "vgg3x3", "sweep90", "alex11x11", "conv5x5"])
+def test_integer_variant_bit_exact(name):
+    """The same shapes with integer weights in {-3..3}\\{0} and inputs in
+    {0..7}: the GPU result must equal the oracle exactly."""
+    import dataclasses
+    L = dataclasses.replace(workloads.LAYERS[name], integer=True, name=name + "_int")
+    layer_case(L, N=min(workloads.LAYERS[name].N, 4))
+
+
+EDGE = [
+    # (N, C, H, W, M, R, S, stride, pad, density)
+    (2, 3, 5, 37, 7, 3, 3, 1, 1, 0.3),       # F > 32: two column tiles, ragged
+    (1, 1, 1, 1, 1, 1, 1, 1, 0, 1.0),        # 1x1 everything
+    (3, 4, 9, 9, 5, 1, 1, 1, 0, 0.5),        # 1x1 conv
+    (2, 5, 11, 13, 6, 2, 2, 1, 0, 0.4),      # even kernel
+    (2, 4, 17, 19, 9, 7, 7, 2, 3, 0.2),      # generic 7x7 stride 2
+    (2, 6, 15, 15, 8, 3, 3, 2, 1, 0.3),      # 3x3 stride 2
+    (1, 3, 12, 40, 4, 1, 3, 1, 0, 0.5),      # 1x3
+    (1, 3, 40, 12, 4, 3, 1, 1, 1, 0.5),      # 3x1 with pad
+    (2, 600, 6, 6, 40, 3, 3, 1, 1, 0.05),    # many input channels: several chunks
+    (1, 8, 10, 10, 300, 3, 3, 1, 1, 0.2),    # M not a multiple of the group size
+    (1, 2, 30, 30, 3, 5, 5, 3, 2, 0.5),      # 5x5 stride 3
+    (2, 3, 23, 23, 4, 11, 11, 4, 1, 0.3),    # 11x11/4 with padding
+    (1, 16, 16, 16, 32, 3, 3, 1, 2, 0.1),    # pad larger than needed (E > H)
+    (5, 4, 8, 8, 6, 3, 3, 1, 1, 1.0),        # fully dense rows
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", EDGE, ids=[str(c) for c in EDGE])
+@pytest.mark.parametrize("integer", [False, True])
+def test_edge_shapes(case, integer):
+    N, C, H, W, M, R, S, st, pad, d = case
+    rng = np.random.default_rng(abs(hash(case)) % (2 ** 32))
+    rowptr, colidx, value = workloads.random_csr(M, C * R * S, d, rng, integer=integer)
+    x = workloads.random_input((N, C, H, W), rng, integer=integer)
+    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, R, S, st, pad)
+    ref, mag = oracle.csr(x, rowptr, colidx, value, M, R, S, st, pad)
+    check(got, ref, mag, exact=integer, what=str(case))
+
+
+@pytest.mark.gpu
+def test_empty_rows_and_empty_matrix():
+    rng = np.random.default_rng(1)
+    N, C, H, W, M = 2, 4, 9, 9, 10
+    rowptr, colidx, value = workloads.random_csr(M, C * 9, 0.3, rng)
+    # empty out rows 0, 3, 9
+    keep = np.ones(colidx.size, bool)
+    for m in (0, 3, 9):
+        keep[rowptr[m]:rowptr[m + 1]] = False
+    counts = np.array([keep[rowptr[m]:rowptr[m + 1]].sum() for m in range(M)])
+    rowptr2 = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = workloads.random_input((N, C, H, W), rng)
+    got = run_gpu(x, rowptr2, colidx[keep], value[keep], C, H, W, M, 3, 3, 1, 1)
+    ref, mag = oracle.csr(x, rowptr2, colidx[keep], value[keep], M, 3, 3, 1, 1)
+    check(got, ref, mag)
+    assert not got[:, [0, 3, 9]].any()
+    # no nonzeros at all: all outputs written as zero
+    z = run_gpu(x, np.zeros(M + 1, np.int32), np.zeros(0, np.int32), np.zeros(0, np.float32),
+                C, H, W, M, 3, 3, 1, 1)
+    assert np.all(z == 0)
+
+
+@pytest.mark.gpu
+def test_batch_zero_is_noop():
+    L = workloads.LAYERS["tiny"]
+    rowptr, colidx, value = workloads.make_weights(L)
+    w = swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
+                 stride=L.stride, pad=L.pad)
+    x = torch.zeros((0, L.C, L.H, L.W), device="cuda")
+    y = swd.forward(x, w)
+    assert y.shape == (0, L.M, L.E, L.F)
+    w.close()
+
+
+@pytest.mark.gpu
+def test_streams_and_shared_handle():
+    """One handle, two forwards on two non-default streams at once."""
+    L = workloads.LAYERS["vgg3x3"]
+    rowptr, colidx, value = workloads.make_weights(L)
+    x = workloads.make_input(L, N=4)
+    w = swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
+                 stride=L.stride, pad=L.pad)
+    xd = torch.from_numpy(x).cuda()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s1):
+        y1 = swd.forward(xd, w, stream=s1)
+    with torch.cuda.stream(s2):
+        y2 = swd.forward(xd[2:], w, stream=s2)
+    torch.cuda.synchronize()
+    ref, mag = oracle.csr(x, rowptr, colidx, value, L.M, L.R, L.S, L.stride, L.pad)
+    check(y1.cpu().numpy().astype(np.float64), ref, mag, what="stream 1")
+    check(y2.cpu().numpy().astype(np.float64), ref[2:], mag[2:], what="stream 2")
+    w.close()
+
+
+@pytest.mark.gpu
+def test_forward_argument_errors():
+    L = workloads.LAYERS["tiny"]
+    rowptr, colidx, value = workloads.make_weights(L)
+    w = swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
+                 stride=L.stride, pad=L.pad)
+    lib = swd._lib.lib()
+    x = torch.zeros((1, L.C, L.H, L.W), device="cuda")
+    y = torch.zeros((1, L.M, L.E, L.F), device="cuda")
+    args = (1, L.C, L.H, L.W, L.M, L.R, L.S, L.stride, L.pad)
+    import ctypes
+    P = ctypes.c_void_p
+    ok = lib.spconv_forward(*args, P(x.data_ptr()), w.handle, P(y.data_ptr()), None)
+    assert ok == 0
+    # misaligned input (not 16-byte aligned)
+    assert lib.spconv_forward(*args, P(x.data_ptr() + 4), w.handle, P(y.data_ptr()), None) == -1
+    # null output
+    assert lib.spconv_forward(*args, P(x.data_ptr()), w.handle, None, None) == -1
+    # shape differs from the packed handle
+    bad = (1, L.C, L.H + 1, L.W, L.M, L.R, L.S, L.stride, L.pad)
+    assert lib.spconv_forward(*bad, P(x.data_ptr()), w.handle, P(y.data_ptr()), None) == -6
+    # negative batch
+    neg = (-1,) + args[1:]
+    assert lib.spconv_forward(*neg, P(x.data_ptr()), w.handle, P(y.data_ptr()), None) == -1
+    # overlapping input and output
+    assert lib.spconv_forward(*args, P(x.data_ptr()), w.handle, P(x.data_ptr()), None) == -1
+    torch.cuda.synchronize()
+    w.close()
