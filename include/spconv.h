@@ -41,7 +41,8 @@ typedef enum spconv_status {
     SPCONV_ERR_UNSUPPORTED = -3, /* shape beyond what the kernels were built for     */
     SPCONV_ERR_ALLOC = -4,       /* host or device allocation failed                 */
     SPCONV_ERR_CUDA = -5,        /* a CUDA runtime call or kernel launch failed      */
-    SPCONV_ERR_MISMATCH = -6     /* forward shape/device differs from the packed one */
+    SPCONV_ERR_MISMATCH = -6,    /* forward shape/device differs from the packed one */
+    SPCONV_ERR_DEVICE = -7       /* a kernel reported a failure (see spconv_device_status) */
 } spconv_status;
 
 /* Opaque handle of a packed weight set.  Owned by the library from
@@ -113,18 +114,29 @@ int spconv_pack_host(int C, int H, int W, int M, int R, int S, int stride, int p
                      const int32_t *rowptr, const int32_t *colidx, const float *value,
                      spconv_packed **out);
 
+/*
+ * spconv_device_status -- failures that kernels using this handle recorded on
+ * the device.  Synchronises `stream`, reads and clears the handle's device
+ * error word and returns SPCONV_OK if it was clear, SPCONV_ERR_DEVICE if not
+ * (then *flags, if not NULL, receives the bits: 1 = a pipeline wait in the
+ * forward kernel ran out its time limit and the kernel returned without
+ * writing its outputs).  Errors: INVALID_ARG (NULL or host-only handle), CUDA.
+ */
+int spconv_device_status(const spconv_packed *p, void *stream, int32_t *flags);
+
 /* Geometry and sizes of a packed handle (all counts are plain integers). */
 typedef struct spconv_packed_info {
     int32_t C, H, W, M, R, S, stride, pad, E, F;
     int64_t nnz;            /* nonzeros of the CSR input                        */
     int64_t entries;        /* packed (value, offset) entries (== nnz)          */
     int32_t tile_rows;      /* output rows per tile (per lane)                  */
+    int32_t shift;          /* staged column of a tile's first input column     */
     int32_t tile_cols;      /* output columns per tile (one per lane: 32)       */
     int32_t tiles_y, tiles_x;
     int32_t in_rows;        /* staged input rows per channel (with halo)        */
     int32_t in_cols;        /* staged input columns per channel (with halo)     */
     int32_t phase_pitch;    /* words per stride-phase sub-row                   */
-    int32_t row_pitch;      /* words per staged input row (= stride*phase_pitch)*/
+    int32_t row_pitch;      /* words per staged input row                       */
     int32_t plane;          /* words per staged channel                         */
     int32_t chunk;          /* input channels staged at once                    */
     int32_t num_chunks;
@@ -137,16 +149,23 @@ typedef struct spconv_packed_info {
     int64_t smem_bytes;     /* dynamic shared memory per block of the forward   */
     int64_t max_warp_nnz;   /* heaviest warp's total entries (balance metric)   */
     int64_t mean_warp_nnz;  /* mean over non-empty warps, rounded down          */
+    int32_t hdr_words;      /* 32-bit words of a weight blob's header           */
+    int32_t blob_stage_bytes; /* largest weight blob (bytes, rounded to 128)    */
+    int32_t in_stage_bytes;   /* staged input of one chunk (bytes, to 128)      */
+    int32_t reserved;
 } spconv_packed_info;
 
 int spconv_packed_info_get(const spconv_packed *p, spconv_packed_info *info);
 
 /* Which host-side array spconv_packed_copy_array copies. */
 typedef enum spconv_array {
-    SPCONV_ARRAY_ENTRIES = 0, /* entries x {float value, int32 offset}, 8 B each    */
-    SPCONV_ARRAY_SEGPTR = 1,  /* int32 [num_slots * (num_chunks + 1)]: entry index  */
-                              /* where slot s's chunk k starts ([.., k+1] ends it)  */
-    SPCONV_ARRAY_SLOT_OC = 2  /* int32 [num_slots]: output channel of a slot or -1  */
+    SPCONV_ARRAY_BLOBS = 0,    /* the weight blobs, one per (group, chunk), each    */
+                               /* 16-byte aligned: hdr_words uint32 entry indices  */
+                               /* (slot w*Q+q spans [hdr[w*Q+q], hdr[w*Q+q+1])),   */
+                               /* then entries of {float value, int32 offset}      */
+    SPCONV_ARRAY_BLOB_OFF = 1, /* uint32 [groups * num_chunks + 1]: blob starts in  */
+                               /* 16-byte units                                     */
+    SPCONV_ARRAY_SLOT_OC = 2   /* int32 [num_slots]: output channel of a slot or -1 */
 } spconv_array;
 
 /* Copies one packed array into dst (host, dst_bytes long).  *needed (if not

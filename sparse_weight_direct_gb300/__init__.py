@@ -54,20 +54,31 @@ class PackedWeights:
         return {name: getattr(info, name) for name, _ in _lib.PackedInfo._fields_}
 
     def array(self, which: str) -> np.ndarray:
-        """Copy of a packed host array: 'entries' (structured value/off),
-        'segptr' or 'slot_oc'."""
-        code = {"entries": 0, "segptr": 1, "slot_oc": 2}[which]
+        """Copy of a packed host array: 'blobs' (raw bytes), 'blob_off'
+        (uint32, 16-byte units) or 'slot_oc' (int32)."""
+        code = {"blobs": 0, "blob_off": 1, "slot_oc": 2}[which]
         need = ctypes.c_int64(0)
         L = _lib.lib()
         _lib.check(L.spconv_packed_copy_array(self.handle, code, None, 0, ctypes.byref(need)),
                    "spconv_packed_copy_array")
-        if which == "entries":
-            out = np.zeros(need.value // 8, dtype=[("value", "<f4"), ("off", "<i4")])
+        if which == "blobs":
+            out = np.zeros(need.value, dtype=np.uint8)
+        elif which == "blob_off":
+            out = np.zeros(need.value // 4, dtype=np.uint32)
         else:
             out = np.zeros(need.value // 4, dtype=np.int32)
         _lib.check(L.spconv_packed_copy_array(self.handle, code, out.ctypes.data_as(ctypes.c_void_p),
                                               out.nbytes, None), "spconv_packed_copy_array")
         return out
+
+    def device_status(self, stream=None) -> int:
+        """Synchronise the stream and read/clear the device error flags
+        (0 = clean; bit 0 = a pipeline wait of the forward kernel timed out)."""
+        flags = ctypes.c_int32(0)
+        rc = _lib.lib().spconv_device_status(self.handle, _stream_ptr(stream), ctypes.byref(flags))
+        if rc not in (_lib.SPCONV_OK, _lib.SPCONV_ERR_DEVICE):
+            _lib.check(rc, "spconv_device_status")
+        return int(flags.value)
 
     def close(self) -> None:
         if self._h:

@@ -20,10 +20,12 @@ SPCONV_ERR_UNSUPPORTED = -3
 SPCONV_ERR_ALLOC = -4
 SPCONV_ERR_CUDA = -5
 SPCONV_ERR_MISMATCH = -6
+SPCONV_ERR_DEVICE = -7
 
 # Every symbol include/spconv.h declares.
 EXPORTS = ("spconv_pack", "spconv_forward", "spconv_packed_free", "spconv_status_string",
-           "spconv_pack_host", "spconv_packed_info_get", "spconv_packed_copy_array")
+           "spconv_pack_host", "spconv_device_status", "spconv_packed_info_get",
+           "spconv_packed_copy_array")
 
 _lock = threading.Lock()
 _lib = None
@@ -41,11 +43,13 @@ class PackedInfo(ctypes.Structure):
                 ("C", "H", "W", "M", "R", "S", "stride", "pad", "E", "F")] + [
         ("nnz", ctypes.c_int64), ("entries", ctypes.c_int64)] + [
         (n, ctypes.c_int32) for n in
-        ("tile_rows", "tile_cols", "tiles_y", "tiles_x", "in_rows", "in_cols", "phase_pitch",
-         "row_pitch", "plane", "chunk", "num_chunks", "slots_per_warp", "warps", "groups",
-         "num_slots", "on_device")] + [
+        ("tile_rows", "shift", "tile_cols", "tiles_y", "tiles_x", "in_rows", "in_cols",
+         "phase_pitch", "row_pitch", "plane", "chunk", "num_chunks", "slots_per_warp", "warps",
+         "groups", "num_slots", "on_device")] + [
         (n, ctypes.c_int64) for n in
-        ("device_bytes", "smem_bytes", "max_warp_nnz", "mean_warp_nnz")]
+        ("device_bytes", "smem_bytes", "max_warp_nnz", "mean_warp_nnz")] + [
+        (n, ctypes.c_int32) for n in
+        ("hdr_words", "blob_stage_bytes", "in_stage_bytes", "reserved")]
 
 
 def lib() -> ctypes.CDLL:
@@ -75,6 +79,8 @@ def lib() -> ctypes.CDLL:
         L.spconv_packed_copy_array.argtypes = [p, i, p, ctypes.c_int64,
                                                ctypes.POINTER(ctypes.c_int64)]
         L.spconv_packed_copy_array.restype = i
+        L.spconv_device_status.argtypes = [p, p, ctypes.POINTER(ctypes.c_int32)]
+        L.spconv_device_status.restype = i
         _lib = L
         return L
 

@@ -5,79 +5,177 @@
 // nonzeros of its output channel, of value * input at the padding-shifted
 // position -- with stride (Escoin, arXiv 1802.10280, Algorithm 2).
 //
-// How (one block = one output tile of P rows x 32 columns of one image, for a
-// group of 8 * Q output channels):
-//   1. stage: the input tile plus halo of a chunk of input channels is copied
-//      into shared memory with cp.async (zero-filled outside the image, so the
-//      padding needs no branch in the hot loop), double-buffered across chunks
-//      (the shared-memory tiling of Sec. 5.1 of the first page);
-//   2. accumulate: every warp carries Q output channels; lanes own one output
-//      column each and P rows in registers.  A warp walks its channels'
-//      packed (value, offset) entries with warp-uniform 16-byte loads (two
-//      entries per load, broadcast to all lanes) and, per entry, does P FMAs
-//      reading smem[lane_base + offset + p * row_step] -- consecutive lanes read
-//      consecutive words, so the reads are bank-conflict free;
-//   3. write back: coalesced stores along the output row, predicated for
-//      partial tiles (Sec. 5.5 of the first page).
-// Offsets are precomputed on the host per nonzero (Escoin's weight stretching),
-// against the shared-memory tile layout, so the kernel never decodes (c, r, s).
+// Work decomposition.  A block owns one output tile (P rows x 32 columns of one
+// image) and one group of 8 * Q output channels; a thread-block cluster of
+// `split` blocks shares the tile and splits the input-channel chunks between
+// them.  Per chunk, a pipeline stage holds
+//   * the input tile plus halo of the chunk's channels (Sec. 5.1 of the first
+//     page: each input region is read once per block and reused by all of the
+//     block's output channels and rows), fetched by one TMA tensor copy with
+//     hardware zero fill for the padding, or by cp.async where the input row
+//     stride is not 16-byte aligned; and
+//   * the chunk's weight blob of the block's channel group (a header of per-warp
+//     entry ranges, then 8-byte (value, offset) entries), fetched by one bulk
+//     asynchronous copy.
+// Both complete on the stage's mbarrier; two stages overlap copy and compute.
+// Each warp carries Q output channels; each lane owns one output column and P
+// rows in registers.  A warp walks its entries with 16-byte shared-memory
+// broadcasts (two entries per load) and does P FMAs per entry, reading
+// smem[lane + offset + p * row_step]: consecutive lanes read consecutive words,
+// so the reads are conflict free.  Offsets were precomputed per nonzero on the
+// host against this tile layout (Escoin's weight stretching).  With split > 1
+// the blocks of a cluster add their partial sums through distributed shared
+// memory in a fixed rank order (deterministic), then write back; otherwise the
+// accumulators are written directly (coalesced along the row, predicated for
+// partial tiles: Sec. 5.5 of the first page).
+#include <cooperative_groups.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "spconv_internal.h"
 
+namespace cg = cooperative_groups;
+
 namespace spconv {
 namespace {
 
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
+
 struct KParams {
-    const float *__restrict__ x;
-    float *__restrict__ y;
-    const float2 *__restrict__ entries;
-    const int *__restrict__ segptr;
-    const int *__restrict__ slot_oc;
+    const float *x;
+    float *y;
+    const unsigned char *blobs;
+    const uint32_t *blob_off;
+    const int *slot_oc;
+    unsigned int *err;
     int N, C, H, W, M, E, F, stride, pad;
-    int tiles_y, tiles_x, in_rows, in_cols, phase_pitch, row_pitch, plane, chunk, num_chunks;
+    int tiles_y, tiles_x, in_rows, in_cols, shift, phase_pitch, row_pitch, plane;
+    int chunk, num_chunks, split, hdr_words;
+    int in_stage_bytes, stage_bytes, in_tma_bytes;
+    int use_tma;
 };
 
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+// Waits for the stage's phase with a time limit; false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tmap, int x, int y,
+                                            int c, int n, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(c), "r"(n),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];\n" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void cp_async_4(float *smem_dst, const float *gsrc, bool pred) {
-    const unsigned saddr = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
     const int src_size = pred ? 4 : 0;  // 0 -> the 4 destination bytes are zero-filled
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(saddr), "l"(gsrc),
-                 "r"(src_size)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(src_size)
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
-template <int K>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(K) : "memory");
+__device__ __forceinline__ void cp_async_wait_all_but_one() {
+    asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
 }
 
-// Stage channels [c0, c0 + cc) of image n, input rows iy0.., columns ix0..
-// into buf with the tile layout [channel][row][phase][col / stride].
+// ---------------------------------------------------------------- staging
+
+// cp.async staging of channels [c0, c0 + cc) of image n: staged element
+// (channel cl, row, col) holds input (c0 + cl, iy0 + row, ix0 + col), zero
+// outside the image.  All threads take part; indices advance incrementally.
 template <int ST_CT>
-__device__ __forceinline__ void stage_chunk(const KParams &p, float *buf, int n, int c0, int cc,
-                                            int iy0, int ix0) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+__device__ __forceinline__ void stage_input_cp_async(const KParams &p, float *buf, int n, int c0,
+                                                     int cc, int iy0, int ix0) {
     const int st = ST_CT ? ST_CT : p.stride;
-    const int rows = cc * p.in_rows;
-    for (int rr = warp; rr < rows; rr += nw) {
-        const int cl = rr / p.in_rows;
-        const int row = rr - cl * p.in_rows;
-        const int gy = iy0 + row;
-        const bool rowok = gy >= 0 && gy < p.H;
-        const float *src = p.x + (((size_t)n * p.C + (c0 + cl)) * p.H + (rowok ? gy : 0)) * p.W;
-        float *dst = buf + cl * p.plane + row * p.row_pitch;
-        for (int col = lane; col < p.in_cols; col += 32) {
-            const int gx = ix0 + col;
-            const bool ok = rowok && gx >= 0 && gx < p.W;
-            const int phys = (st == 1) ? col : (col % st) * p.phase_pitch + col / st;
-            cp_async_4(dst + phys, ok ? src + gx : p.x, ok);
+    const int in_cols = p.in_cols, in_rows = p.in_rows;
+    const int total = cc * in_rows * in_cols;
+    int e = threadIdx.x;
+    if (e >= total) return;
+    const int dcol = blockDim.x % in_cols, drow = blockDim.x / in_cols;
+    int col = e % in_cols;
+    int rr = e / in_cols;
+    int row = rr % in_rows;
+    int cl = rr / in_rows;
+    const float *xn = p.x + (size_t)n * p.C * p.H * p.W;
+    for (; e < total; e += blockDim.x) {
+        const int gy = iy0 + row, gx = ix0 + col;
+        const bool ok = (unsigned)gy < (unsigned)p.H && (unsigned)gx < (unsigned)p.W;
+        const float *src = ok ? xn + ((size_t)(c0 + cl) * p.H + gy) * p.W + gx : p.x;
+        const int phys = (st == 1) ? col + p.shift : (col % st) * p.phase_pitch + col / st;
+        cp_async_4(buf + cl * p.plane + row * p.row_pitch + phys, src, ok);
+        col += dcol;
+        row += drow;
+        if (col >= in_cols) {
+            col -= in_cols;
+            ++row;
+        }
+        while (row >= in_rows) {
+            row -= in_rows;
+            ++cl;
         }
     }
 }
+
+// ---------------------------------------------------------------- compute
 
 template <int P, int ROW_STEP>
 __device__ __forceinline__ void apply_entry(float (&acc)[P], const float *sb, float v, int off,
@@ -88,25 +186,83 @@ __device__ __forceinline__ void apply_entry(float (&acc)[P], const float *sb, fl
         acc[r] = fmaf(v, s[r * (ROW_STEP ? ROW_STEP : row_step)], acc[r]);
 }
 
+template <int P, int ROW_STEP>
+__device__ __forceinline__ void run_segment(float (&acc)[P], const float *sb, const float2 *ent,
+                                            int j, int j1, int row_step) {
+    if ((j & 1) && j < j1) {  // head: bring j to a 16-byte boundary
+        const float2 e = ent[j];
+        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
+        ++j;
+    }
+    for (; j + 1 < j1; j += 2) {
+        const float4 e = *reinterpret_cast<const float4 *>(ent + j);
+        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
+        apply_entry<P, ROW_STEP>(acc, sb, e.z, __float_as_int(e.w), row_step);
+    }
+    if (j < j1) {  // tail
+        const float2 e = ent[j];
+        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
+    }
+}
+
 // P: output rows per lane; Q: output channels per warp; S_CT/ST_CT: kernel
 // width and stride when known at compile time (0 = read from p).
 template <int P, int Q, int S_CT, int ST_CT>
-__global__ void __launch_bounds__(256, 2) spconv_fwd_kernel(const KParams p) {
-    extern __shared__ __align__(16) float smem[];
-    constexpr int ROW_STEP = S_CT ? ST_CT * ST_CT * phase_pitch_for(S_CT, ST_CT) : 0;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    int t = blockIdx.x;
-    const int tx = t % p.tiles_x;
-    t /= p.tiles_x;
-    const int ty = t % p.tiles_y;
-    const int n = t / p.tiles_y;
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    spconv_fwd_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bar[2];
+    // stage buffers start on a 128-byte boundary (TMA destination)
+    unsigned char *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    constexpr int ROW_STEP =
+        S_CT ? (ST_CT == 1 ? row_pitch_s1(S_CT) : ST_CT * ST_CT * phase_pitch_for(S_CT, ST_CT))
+             : 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int st = ST_CT ? ST_CT : p.stride;
     const int row_step = st * p.row_pitch;
-    const int slot0 = (blockIdx.y * nw + warp) * Q;
-    const int nch = p.num_chunks;
-    const int buf_words = p.chunk * p.plane;
+
+    const int split = p.split;
+    int b = blockIdx.x;
+    const int kr = b % split;  // rank inside the cluster (clusters run along x)
+    b /= split;
+    const int tx = b % p.tiles_x;
+    b /= p.tiles_x;
+    const int ty = b % p.tiles_y;
+    const int n = b / p.tiles_y;
+    const int group = blockIdx.y;
+    const int k_begin = kr * p.num_chunks / split;
+    const int k_end = (kr + 1) * p.num_chunks / split;
     const int iy0 = ty * P * st - p.pad;
     const int ix0 = tx * kTileCols * st - p.pad;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    }
+    __syncthreads();
+
+    // Enqueue chunk k into stage s: thread 0 issues the bulk copies, every
+    // thread its share of the cp.async input staging when there is no TMA.
+    auto issue = [&](int k, int s) {
+        unsigned char *base = smem + (size_t)s * p.stage_bytes;
+        const uint32_t o0 = p.blob_off[group * p.num_chunks + k];
+        const uint32_t o1 = p.blob_off[group * p.num_chunks + k + 1];
+        const uint32_t blob_bytes = (o1 - o0) * 16u;
+        const int c0 = k * p.chunk;
+        if (threadIdx.x == 0) {
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            mbar_expect_tx(&bar[s], blob_bytes + (p.use_tma ? (uint32_t)p.in_tma_bytes : 0u));
+            bulk_load(base + p.in_stage_bytes, p.blobs + (size_t)o0 * 16u, blob_bytes, &bar[s]);
+            if (p.use_tma) tma_load_4d(base, &tmap, ix0 - p.shift, iy0, c0, n, &bar[s]);
+        }
+        if (!p.use_tma) {
+            stage_input_cp_async<ST_CT>(p, reinterpret_cast<float *>(base), n, c0,
+                                        min(p.chunk, p.C - c0), iy0, ix0);
+            cp_async_commit();
+        }
+    };
 
     float acc[Q][P];
 #pragma unroll
@@ -114,59 +270,88 @@ __global__ void __launch_bounds__(256, 2) spconv_fwd_kernel(const KParams p) {
 #pragma unroll
         for (int r = 0; r < P; ++r) acc[q][r] = 0.f;
 
-    stage_chunk<ST_CT>(p, smem, n, 0, min(p.chunk, p.C), iy0, ix0);
-    cp_async_commit();
-    for (int k = 0; k < nch; ++k) {
-        if (k + 1 < nch) {
-            const int c1 = (k + 1) * p.chunk;
-            stage_chunk<ST_CT>(p, smem + ((k + 1) & 1) * buf_words, n, c1, min(p.chunk, p.C - c1),
-                               iy0, ix0);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+    const int nmine = k_end - k_begin;
+    bool failed = false;
+    if (nmine > 0) issue(k_begin, 0);
+    if (nmine > 1) issue(k_begin + 1, 1);
+    for (int it = 0; it < nmine && !failed; ++it) {
+        const int s = it & 1;
+        if (!p.use_tma) {
+            if (it + 1 < nmine)
+                cp_async_wait_all_but_one();
+            else
+                cp_async_wait_all();
         }
-        __syncthreads();
-        const float *sb = smem + (k & 1) * buf_words + lane;
+        const bool ok = mbar_wait_bounded(&bar[s], (uint32_t)((it >> 1) & 1));
+        failed = __syncthreads_or(!ok) != 0;
+        if (failed) break;
+        const unsigned char *base = smem + (size_t)s * p.stage_bytes;
+        const float *sb = reinterpret_cast<const float *>(base) + lane;
+        const uint32_t *hdr = reinterpret_cast<const uint32_t *>(base + p.in_stage_bytes);
+        const float2 *ent = reinterpret_cast<const float2 *>(hdr + p.hdr_words);
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
-            const int *sp = p.segptr + (size_t)(slot0 + q) * (nch + 1) + k;
-            int j = __ldg(sp);
-            const int j1 = __ldg(sp + 1);
-            if ((j & 1) && j < j1) {  // head: bring j to a 16-byte boundary
-                const float2 e = __ldg(p.entries + j);
-                apply_entry<P, ROW_STEP>(acc[q], sb, e.x, __float_as_int(e.y), row_step);
-                ++j;
-            }
-            for (; j + 1 < j1; j += 2) {
-                const float4 e = __ldg(reinterpret_cast<const float4 *>(p.entries + j));
-                apply_entry<P, ROW_STEP>(acc[q], sb, e.x, __float_as_int(e.y), row_step);
-                apply_entry<P, ROW_STEP>(acc[q], sb, e.z, __float_as_int(e.w), row_step);
-            }
-            if (j < j1) {  // tail
-                const float2 e = __ldg(p.entries + j);
-                apply_entry<P, ROW_STEP>(acc[q], sb, e.x, __float_as_int(e.y), row_step);
-            }
+            const int j0 = (int)hdr[warp * Q + q];
+            const int j1 = (int)hdr[warp * Q + q + 1];
+            run_segment<P, ROW_STEP>(acc[q], sb, ent, j0, j1, row_step);
         }
-        __syncthreads();  // buffer (k & 1) is restaged two chunks later
+        __syncthreads();  // stage s is free again
+        if (it + 2 < nmine) issue(k_begin + it + 2, s);
+    }
+    if (failed) {
+        if (!p.use_tma) cp_async_wait_all();
+        if (threadIdx.x == 0) atomicOr(p.err, 1u);
     }
 
+    const int slot0 = (group * kWarps + warp) * Q;
     const int ox = tx * kTileCols + lane;
-    if (ox >= p.F) return;
+    if (split == 1) {
+        if (failed || ox >= p.F) return;
 #pragma unroll
-    for (int q = 0; q < Q; ++q) {
-        const int m = __ldg(p.slot_oc + slot0 + q);
-        if (m < 0) continue;
-        float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
+        for (int q = 0; q < Q; ++q) {
+            const int m = p.slot_oc[slot0 + q];
+            if (m < 0) continue;
+            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
 #pragma unroll
-        for (int r = 0; r < P; ++r) {
-            const int oy = ty * P + r;
-            if (oy < p.E) yo[(size_t)oy * p.F] = acc[q][r];
+            for (int r = 0; r < P; ++r) {
+                const int oy = ty * P + r;
+                if (oy < p.E) yo[(size_t)oy * p.F] = acc[q][r];
+            }
+        }
+        return;
+    }
+
+    // ---- cluster reduction of the channel split through distributed smem
+    cg::cluster_group cluster = cg::this_cluster();
+    float *part = reinterpret_cast<float *>(smem);  // [warp * Q + q][P][32]
+    // every block of the cluster has left its pipeline before partials land
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+#pragma unroll
+        for (int r = 0; r < P; ++r) part[((warp * Q + q) * P + r) * 32 + lane] = acc[q][r];
+    cluster.sync();
+    const int nslot = kWarps * Q;
+    const int s_begin = kr * nslot / split, s_end = (kr + 1) * nslot / split;
+    if (!failed && ox < p.F) {
+        for (int sl = s_begin + warp; sl < s_end; sl += kWarps) {
+            const int m = p.slot_oc[group * nslot + sl];
+            if (m < 0) continue;
+            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
+            for (int r = 0; r < P; ++r) {
+                const int oy = ty * P + r;
+                float sum = 0.f;
+                for (int j = 0; j < split; ++j) {
+                    const float *rp = cluster.map_shared_rank(part, j);
+                    sum += rp[(sl * P + r) * 32 + lane];
+                }
+                if (oy < p.E) yo[(size_t)oy * p.F] = sum;
+            }
         }
     }
+    cluster.sync();  // partials stay readable until every block is done
 }
 
-using KernelFn = void (*)(const KParams);
+using KernelFn = void (*)(const KParams, const CUtensorMap);
 
 template <int P, int Q>
 KernelFn pick_sst(int S, int stride) {
@@ -195,36 +380,74 @@ KernelFn pick(int S, int stride, int P, int Q) {
     }
 }
 
+size_t stage_bytes(const Geometry &g) { return g.in_stage_bytes + g.blob_stage_bytes; }
+
 }  // namespace
 
 int forward_variant_supported(int S, int stride, int P, int Q) {
     return pick(S, stride, P, Q) ? 0 : -1;
 }
 
-cudaError_t launch_forward(const Geometry &g, int N, const float *x, float *y,
-                           const DeviceArrays &d, cudaStream_t stream) {
+size_t forward_smem_bytes(const Geometry &g, int split) {
+    const int per_block = (g.num_chunks + split - 1) / split;
+    size_t bytes = (size_t)(per_block > 1 ? 2 : 1) * stage_bytes(g);
+    if (split > 1) {
+        const size_t part = (size_t)g.warps * g.slots * g.tile_rows * 32 * sizeof(float);
+        if (part > bytes) bytes = part;
+    }
+    return bytes + 128;  // room to align the stage buffers to 128 bytes
+}
+
+cudaError_t launch_forward(const Geometry &g, int N, int split, const float *x, float *y,
+                           const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream) {
     KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots);
-    if (!fn) return cudaErrorInvalidConfiguration;
-    if (g.smem_bytes > 48 * 1024) {
+    if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks)
+        return cudaErrorInvalidConfiguration;
+    const size_t smem = forward_smem_bytes(g, split);
+    if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)g.smem_bytes);
+                                             (int)smem);
         if (e != cudaSuccess) return e;
     }
     KParams p;
     p.x = x;
     p.y = y;
-    p.entries = d.entries;
-    p.segptr = d.segptr;
+    p.blobs = d.blobs;
+    p.blob_off = d.blob_off;
     p.slot_oc = d.slot_oc;
+    p.err = d.err;
     p.N = N; p.C = g.C; p.H = g.H; p.W = g.W; p.M = g.M; p.E = g.E; p.F = g.F;
     p.stride = g.stride; p.pad = g.pad;
     p.tiles_y = g.tiles_y; p.tiles_x = g.tiles_x; p.in_rows = g.in_rows; p.in_cols = g.in_cols;
-    p.phase_pitch = g.phase_pitch; p.row_pitch = g.row_pitch; p.plane = g.plane;
-    p.chunk = g.chunk; p.num_chunks = g.num_chunks;
-    const dim3 grid((unsigned)((int64_t)N * g.tiles_y * g.tiles_x), (unsigned)g.groups, 1);
-    fn<<<grid, g.warps * 32, g.smem_bytes, stream>>>(p);
-    return cudaGetLastError();
+    p.shift = g.shift; p.phase_pitch = g.phase_pitch; p.row_pitch = g.row_pitch;
+    p.plane = g.plane; p.chunk = g.chunk; p.num_chunks = g.num_chunks; p.split = split;
+    p.hdr_words = g.hdr_words;
+    p.in_stage_bytes = (int)g.in_stage_bytes;
+    p.stage_bytes = (int)stage_bytes(g);
+    p.in_tma_bytes = g.chunk * g.plane * (int)sizeof(float);
+    p.use_tma = tmap ? 1 : 0;
+    CUtensorMap dummy;
+    if (!tmap) {
+        for (int i = 0; i < 16; ++i) dummy.opaque[i] = 0;
+        tmap = &dummy;
+    }
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((int64_t)N * g.tiles_y * g.tiles_x * split), (unsigned)g.groups, 1);
+    cfg.blockDim = dim3(kWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (split > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)split;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, fn, p, *tmap);
 }
 
 }  // namespace spconv

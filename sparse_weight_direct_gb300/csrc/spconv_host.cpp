@@ -1,6 +1,6 @@
 // Host side of libspconv: argument validation, the packing of CSR weights into
 // the kernel's layout (weight stretching + output-channel binning), device
-// upload, and the C ABI declared in include/spconv.h.
+// upload, tensor-map encoding, and the C ABI declared in include/spconv.h.
 //
 // Packing follows Escoin (arXiv 1802.10280), "Sparse convolution": dynamic
 // indexing with the layout function f(c, y, x) and its shift property
@@ -8,13 +8,16 @@
 // (c, r, s) is rewritten once ("weight stretching") into an offset that the
 // kernel adds to a per-output-pixel base.  Here f is the layout of the
 // shared-memory input tile the kernel stages (channel plane, row, stride
-// phase, column), not of the global array.  The per-output-channel ranges
-// play the role of the offset array of Tuteja et al., "Theoretical and
-// Empirical Analysis of Sparse Convolution", Sec. 5.3.
+// phase, column), not of the global array.  The per-slot entry ranges in each
+// blob header play the role of the offset array of Tuteja et al.,
+// "Theoretical and Empirical Analysis of Sparse Convolution", Sec. 5.3.
 #include "../../include/spconv.h"
+
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <numeric>
 #include <queue>
@@ -30,25 +33,36 @@ struct HostEntry {
 };
 static_assert(sizeof(HostEntry) == 8, "entry must be 8 bytes");
 
+struct TmapCacheEntry {
+    const void *x = nullptr;
+    int N = -1;
+    CUtensorMap map;
+};
+
 }  // namespace
 
 struct spconv_packed {
     spconv::Geometry g{};
     int64_t nnz = 0;
     int64_t max_warp_nnz = 0, mean_warp_nnz = 0;
-    std::vector<HostEntry> entries;
-    std::vector<int32_t> segptr;   // [num_slots][num_chunks + 1]
-    std::vector<int32_t> slot_oc;  // [num_slots]
+    std::vector<unsigned char> blobs;  // concatenated (group, chunk) blobs
+    std::vector<uint32_t> blob_off;    // [groups * num_chunks + 1], 16-byte units
+    std::vector<int32_t> slot_oc;      // [num_slots]
     int device = -1;
     void *dev_block = nullptr;
     size_t dev_bytes = 0;
     spconv::DeviceArrays d{};
+    mutable std::mutex tmap_lock;
+    mutable TmapCacheEntry tmap_cache[4];
+    mutable unsigned tmap_next = 0;
 };
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr size_t kStageBudget = 96 * 1024;  // bytes of staged input per block
+constexpr size_t kSmemBudget = 110 * 1024;  // two resident blocks per SM
+constexpr int kSMs = 152;                   // GB300 SM count, for the split heuristic
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int out_extent(int in, int k, int stride, int pad) {
     const long num = (long)in + 2L * pad - k;
@@ -64,6 +78,8 @@ int validate_shape(int C, int H, int W, int M, int R, int S, int stride, int pad
     // keep every index the host computes inside int32 / int64 comfortably
     if ((int64_t)C * R * S >= (int64_t)1 << 31) return SPCONV_ERR_UNSUPPORTED;
     if (pad > 4096 || stride > 64 || R > 64 || S > 64) return SPCONV_ERR_UNSUPPORTED;
+    if ((int64_t)H * W >= (int64_t)1 << 31 || (int64_t)M * C >= (int64_t)1 << 40)
+        return SPCONV_ERR_UNSUPPORTED;
     return SPCONV_OK;
 }
 
@@ -81,8 +97,9 @@ int validate_csr(int M, int64_t CRS, const int32_t *rowptr, const int32_t *colid
     return SPCONV_OK;
 }
 
-// Choose the tiling.  Returns SPCONV_OK or SPCONV_ERR_UNSUPPORTED.
-int plan(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, int stride, int pad) {
+// Tile shape and channel group size (everything but the chunking).
+int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, int stride,
+               int pad) {
     g.C = C; g.H = H; g.W = W; g.M = M; g.R = R; g.S = S; g.stride = stride; g.pad = pad;
     g.E = out_extent(H, R, stride, pad);
     g.F = out_extent(W, S, stride, pad);
@@ -97,41 +114,30 @@ int plan(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, int stri
     g.tiles_x = (g.F + spconv::kTileCols - 1) / spconv::kTileCols;
     g.in_rows = (best_p - 1) * stride + R;
     g.in_cols = (spconv::kTileCols - 1) * stride + S;
-    g.phase_pitch = spconv::phase_pitch_for(S, stride);
-    g.row_pitch = stride * g.phase_pitch;
-    g.plane = g.in_rows * g.row_pitch;
-    const size_t plane_bytes = (size_t)g.plane * sizeof(float);
-    if ((size_t)C * plane_bytes <= kStageBudget) {
-        g.chunk = C;
-        g.num_chunks = 1;
-        g.smem_bytes = (size_t)C * plane_bytes;
+    g.shift = spconv::align_shift_for(pad, stride);
+    if (stride == 1) {
+        g.phase_pitch = spconv::row_pitch_s1(S);
+        g.row_pitch = g.phase_pitch;
     } else {
-        g.chunk = (int)(kStageBudget / (2 * plane_bytes));
-        if (g.chunk < 1) return SPCONV_ERR_UNSUPPORTED;
-        // even out the chunks so the last is not a sliver
-        g.num_chunks = (C + g.chunk - 1) / g.chunk;
-        g.chunk = (C + g.num_chunks - 1) / g.num_chunks;
-        g.smem_bytes = 2 * (size_t)g.chunk * plane_bytes;
+        g.phase_pitch = spconv::phase_pitch_for(S, stride);
+        g.row_pitch = stride * g.phase_pitch;
     }
-    g.warps = kWarps;
+    g.plane = g.in_rows * g.row_pitch;
+    g.warps = spconv::kWarps;
     // output channels per warp: four when that still leaves >= 4 groups
-    g.slots = M >= 4 * kWarps * 4 ? 4 : (M >= 4 * kWarps * 2 ? 2 : 1);
-    g.groups = (M + kWarps * g.slots - 1) / (kWarps * g.slots);
-    g.num_slots = g.groups * kWarps * g.slots;
+    g.slots = M >= 4 * spconv::kWarps * 4 ? 4 : (M >= 4 * spconv::kWarps * 2 ? 2 : 1);
+    g.groups = (M + spconv::kWarps * g.slots - 1) / (spconv::kWarps * g.slots);
+    g.num_slots = g.groups * spconv::kWarps * g.slots;
+    g.hdr_words = (int)round_up((size_t)spconv::kWarps * g.slots + 1, 4);
     if (g.groups > 65535) return SPCONV_ERR_UNSUPPORTED;
     if (spconv::forward_variant_supported(S, stride, g.tile_rows, g.slots) != 0)
         return SPCONV_ERR_UNSUPPORTED;
-    if (g.smem_bytes > 200 * 1024) return SPCONV_ERR_UNSUPPORTED;
     return SPCONV_OK;
 }
 
-// Builds the host arrays of a handle.  Returns a status.
-int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
-                 const float *value) {
+// Longest row first onto the warp with the least work that has a free slot.
+void bin_channels(spconv_packed &P, const int32_t *rowptr) {
     const spconv::Geometry &g = P.g;
-    const int RS = g.R * g.S;
-    // --- bin output channels onto warps: longest row first onto the warp
-    //     with the least work that still has a free slot
     std::vector<int> order(g.M);
     std::iota(order.begin(), order.end(), 0);
     std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
@@ -145,7 +151,7 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
     std::vector<int64_t> load(nwarps, 0);
     P.slot_oc.assign(g.num_slots, -1);
     for (int m : order) {
-        Item it = heap.top();
+        const Item it = heap.top();
         heap.pop();
         const int w = it.second;
         P.slot_oc[(size_t)w * g.slots + fill[w]] = m;
@@ -160,49 +166,129 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
     }
     P.max_warp_nnz = mx;
     P.mean_warp_nnz = used ? sum / used : 0;
+}
 
-    // --- entries: per slot, per chunk, columns ascending ((c, r, s) order)
-    const int nch = g.num_chunks;
-    P.segptr.assign((size_t)g.num_slots * (nch + 1), 0);
-    P.entries.clear();
-    P.entries.reserve((size_t)P.nnz);
-    std::vector<int32_t> cols;
-    std::vector<int64_t> idx;
-    for (int slot = 0; slot < g.num_slots; ++slot) {
-        int32_t *sp = &P.segptr[(size_t)slot * (nch + 1)];
-        const int m = P.slot_oc[slot];
-        if (m < 0) {
-            for (int k = 0; k <= nch; ++k) sp[k] = (int32_t)P.entries.size();
-            continue;
+// Chunk size: the largest that keeps two pipeline stages (staged input plus
+// the largest weight blob) within the shared-memory budget, and small enough
+// that a one-image launch can split the chunks over a cluster to fill the GPU.
+int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
+    // gpre[(group) * (C + 1) + c]: entries of the group in channels [0, c)
+    const int C = g.C;
+    const int64_t base_blocks = (int64_t)g.tiles_y * g.tiles_x * g.groups;
+    int want_split = (int)std::min<int64_t>(spconv::kMaxSplit,
+                                            (kSMs + base_blocks - 1) / std::max<int64_t>(base_blocks, 1));
+    want_split = std::max(want_split, 1);
+    int cap = std::min(C, 256);  // TMA box extent limit
+    if (want_split > 1 && C / want_split >= 16)
+        cap = std::min(cap, (C + want_split - 1) / want_split);
+    const size_t hdr_bytes = (size_t)g.hdr_words * 4;
+    for (int chunk = cap; chunk >= 1; --chunk) {
+        const int nch = (C + chunk - 1) / chunk;
+        const size_t in_stage = round_up((size_t)chunk * g.plane * sizeof(float), 128);
+        size_t blob_max = 0;
+        for (int grp = 0; grp < g.groups; ++grp) {
+            const int64_t *pre = &gpre[(size_t)grp * (C + 1)];
+            for (int k = 0; k < nch; ++k) {
+                const int c0 = k * chunk, c1 = std::min(C, c0 + chunk);
+                const size_t bytes = hdr_bytes + round_up((size_t)(pre[c1] - pre[c0]) * 8, 16);
+                blob_max = std::max(blob_max, bytes);
+            }
         }
-        const int64_t lo = rowptr[m], hi = rowptr[m + 1];
-        idx.resize(hi - lo);
-        std::iota(idx.begin(), idx.end(), lo);
+        const size_t stage = in_stage + round_up(blob_max, 128);
+        const size_t total = (nch > 1 ? 2 : 1) * stage + 128;
+        if (total <= kSmemBudget || (chunk == 1 && total <= 200 * 1024)) {
+            g.chunk = chunk;
+            g.num_chunks = nch;
+            g.in_stage_bytes = in_stage;
+            g.blob_stage_bytes = round_up(blob_max, 128);
+            return SPCONV_OK;
+        }
+    }
+    return SPCONV_ERR_UNSUPPORTED;
+}
+
+// Builds the host arrays of a handle.  Returns a status.
+int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
+                 const float *value) {
+    spconv::Geometry &g = P.g;
+    const int RS = g.R * g.S;
+    bin_channels(P, rowptr);
+
+    // per-slot entries sorted by column ((c, r, s) order); duplicates rejected
+    std::vector<std::vector<int64_t>> order(g.num_slots);
+    std::vector<int64_t> gpre((size_t)g.groups * (g.C + 1), 0);
+    const int slots_per_group = g.warps * g.slots;
+    for (int slot = 0; slot < g.num_slots; ++slot) {
+        const int m = P.slot_oc[slot];
+        if (m < 0) continue;
+        std::vector<int64_t> &idx = order[slot];
+        idx.resize(rowptr[m + 1] - rowptr[m]);
+        std::iota(idx.begin(), idx.end(), (int64_t)rowptr[m]);
         std::sort(idx.begin(), idx.end(),
                   [&](int64_t a, int64_t b) { return colidx[a] < colidx[b]; });
         for (size_t t = 1; t < idx.size(); ++t)
             if (colidx[idx[t]] == colidx[idx[t - 1]]) return SPCONV_ERR_BAD_CSR;
-        size_t t = 0;
-        for (int k = 0; k < nch; ++k) {
-            sp[k] = (int32_t)P.entries.size();
-            const int c_end = std::min(g.C, (k + 1) * g.chunk);
-            for (; t < idx.size(); ++t) {
-                const int col = colidx[idx[t]];
-                const int c = col / RS;
-                if (c >= c_end) break;
-                const int r = (col / g.S) % g.R;
-                const int s = col % g.S;
-                const int cl = c - k * g.chunk;
-                HostEntry e;
-                e.value = value[idx[t]];
-                e.off = cl * g.plane + r * g.row_pitch + (s % g.stride) * g.phase_pitch +
-                        s / g.stride;
-                P.entries.push_back(e);
-            }
-        }
-        sp[nch] = (int32_t)P.entries.size();
+        int64_t *pre = &gpre[(size_t)(slot / slots_per_group) * (g.C + 1)];
+        for (int64_t j : idx) pre[colidx[j] / RS + 1] += 1;
     }
-    return (int64_t)P.entries.size() == P.nnz ? SPCONV_OK : SPCONV_ERR_BAD_CSR;
+    for (int grp = 0; grp < g.groups; ++grp) {
+        int64_t *pre = &gpre[(size_t)grp * (g.C + 1)];
+        for (int c = 0; c < g.C; ++c) pre[c + 1] += pre[c];
+    }
+    int st = plan_chunks(g, gpre);
+    if (st) return st;
+
+    // blobs, in (group, chunk) order
+    const int nch = g.num_chunks;
+    P.blob_off.assign((size_t)g.groups * nch + 1, 0);
+    size_t total = 0;
+    for (int grp = 0; grp < g.groups; ++grp) {
+        const int64_t *pre = &gpre[(size_t)grp * (g.C + 1)];
+        for (int k = 0; k < nch; ++k) {
+            const int c0 = k * g.chunk, c1 = std::min(g.C, c0 + g.chunk);
+            P.blob_off[(size_t)grp * nch + k] = (uint32_t)(total / 16);
+            total += (size_t)g.hdr_words * 4 + round_up((size_t)(pre[c1] - pre[c0]) * 8, 16);
+        }
+    }
+    P.blob_off[(size_t)g.groups * nch] = (uint32_t)(total / 16);
+    if (total / 16 >= ((size_t)1 << 32)) return SPCONV_ERR_UNSUPPORTED;
+    P.blobs.assign(total, 0);
+    std::vector<size_t> cursor(g.num_slots, 0);  // next sorted entry of each slot
+    for (int grp = 0; grp < g.groups; ++grp) {
+        for (int k = 0; k < nch; ++k) {
+            unsigned char *blob = P.blobs.data() + (size_t)P.blob_off[(size_t)grp * nch + k] * 16;
+            uint32_t *hdr = reinterpret_cast<uint32_t *>(blob);
+            HostEntry *ent = reinterpret_cast<HostEntry *>(blob + (size_t)g.hdr_words * 4);
+            const int c_end = std::min(g.C, (k + 1) * g.chunk);
+            uint32_t e = 0;
+            for (int ls = 0; ls < slots_per_group; ++ls) {
+                const int slot = grp * slots_per_group + ls;
+                hdr[ls] = e;
+                const std::vector<int64_t> &idx = order[slot];
+                size_t &t = cursor[slot];
+                for (; t < idx.size(); ++t) {
+                    const int col = colidx[idx[t]];
+                    const int c = col / RS;
+                    if (c >= c_end) break;
+                    const int r = (col / g.S) % g.R;
+                    const int s = col % g.S;
+                    const int cl = c - k * g.chunk;
+                    HostEntry h;
+                    h.value = value[idx[t]];
+                    if (g.stride == 1)
+                        h.off = cl * g.plane + r * g.row_pitch + s + g.shift;
+                    else
+                        h.off = cl * g.plane + r * g.row_pitch +
+                                (s % g.stride) * g.phase_pitch + s / g.stride;
+                    ent[e++] = h;
+                }
+            }
+            hdr[slots_per_group] = e;
+        }
+    }
+    for (int slot = 0; slot < g.num_slots; ++slot)
+        if (cursor[slot] != order[slot].size()) return SPCONV_ERR_BAD_CSR;
+    return SPCONV_OK;
 }
 
 int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
@@ -218,7 +304,7 @@ int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
     spconv_packed *P = new (std::nothrow) spconv_packed();
     if (!P) return SPCONV_ERR_ALLOC;
     P->nnz = nnz;
-    st = plan(P->g, C, H, W, M, R, S, stride, pad);
+    st = plan_tiles(P->g, C, H, W, M, R, S, stride, pad);
     if (!st) st = build_layout(*P, rowptr, colidx, value);
     if (st) {
         delete P;
@@ -228,14 +314,13 @@ int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
     return SPCONV_OK;
 }
 
-size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
-
 int upload(spconv_packed *P, cudaStream_t stream) {
     if (cudaGetDevice(&P->device) != cudaSuccess) return SPCONV_ERR_CUDA;
-    const size_t b_entries = align256(std::max<size_t>(P->entries.size(), 2) * sizeof(HostEntry));
-    const size_t b_segptr = align256(P->segptr.size() * sizeof(int32_t));
-    const size_t b_slot = align256(P->slot_oc.size() * sizeof(int32_t));
-    P->dev_bytes = b_entries + b_segptr + b_slot;
+    const size_t b_blobs = round_up(std::max<size_t>(P->blobs.size(), 16), 256);
+    const size_t b_off = round_up(P->blob_off.size() * sizeof(uint32_t), 256);
+    const size_t b_slot = round_up(P->slot_oc.size() * sizeof(int32_t), 256);
+    const size_t b_err = 256;
+    P->dev_bytes = b_blobs + b_off + b_slot + b_err;
     void *blk = nullptr;
     if (cudaMalloc(&blk, P->dev_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -243,14 +328,14 @@ int upload(spconv_packed *P, cudaStream_t stream) {
     }
     P->dev_block = blk;
     char *base = static_cast<char *>(blk);
-    bool ok = cudaMemsetAsync(base, 0, b_entries, stream) == cudaSuccess;
-    ok = ok && (P->entries.empty() ||
-                cudaMemcpyAsync(base, P->entries.data(), P->entries.size() * sizeof(HostEntry),
-                                cudaMemcpyHostToDevice, stream) == cudaSuccess);
-    ok = ok && cudaMemcpyAsync(base + b_entries, P->segptr.data(),
-                               P->segptr.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+    bool ok = cudaMemsetAsync(base, 0, P->dev_bytes, stream) == cudaSuccess;
+    ok = ok && (P->blobs.empty() ||
+                cudaMemcpyAsync(base, P->blobs.data(), P->blobs.size(), cudaMemcpyHostToDevice,
+                                stream) == cudaSuccess);
+    ok = ok && cudaMemcpyAsync(base + b_blobs, P->blob_off.data(),
+                               P->blob_off.size() * sizeof(uint32_t), cudaMemcpyHostToDevice,
                                stream) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(base + b_entries + b_segptr, P->slot_oc.data(),
+    ok = ok && cudaMemcpyAsync(base + b_blobs + b_off, P->slot_oc.data(),
                                P->slot_oc.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
                                stream) == cudaSuccess;
     ok = ok && cudaStreamSynchronize(stream) == cudaSuccess;
@@ -258,15 +343,78 @@ int upload(spconv_packed *P, cudaStream_t stream) {
         cudaGetLastError();
         return SPCONV_ERR_CUDA;
     }
-    P->d.entries = reinterpret_cast<const float2 *>(base);
-    P->d.segptr = reinterpret_cast<const int *>(base + b_entries);
-    P->d.slot_oc = reinterpret_cast<const int *>(base + b_entries + b_segptr);
+    P->d.blobs = reinterpret_cast<const unsigned char *>(base);
+    P->d.blob_off = reinterpret_cast<const uint32_t *>(base + b_blobs);
+    P->d.slot_oc = reinterpret_cast<const int *>(base + b_blobs + b_off);
+    P->d.err = reinterpret_cast<unsigned int *>(base + b_blobs + b_off + b_slot);
     return SPCONV_OK;
 }
 
 bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
     return pa < pb + nb && pb < pa + na;
+}
+
+// ---- TMA tensor map of the input (stride-1 layers with 16-byte row stride)
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+bool tma_eligible(const spconv::Geometry &g) {
+    return g.stride == 1 && (g.W * sizeof(float)) % 16 == 0 && g.row_pitch <= 256 &&
+           g.in_rows <= 256 && g.chunk <= 256;
+}
+
+// Returns a tensor map for (x, N), or nullptr if TMA staging is not possible.
+const CUtensorMap *input_tmap(const spconv_packed *P, const float *x, int N, CUtensorMap &tmp) {
+    const spconv::Geometry &g = P->g;
+    if (!tma_eligible(g)) return nullptr;
+    {
+        std::lock_guard<std::mutex> lk(P->tmap_lock);
+        for (const TmapCacheEntry &e : P->tmap_cache)
+            if (e.x == x && e.N == N) {
+                tmp = e.map;
+                return &tmp;
+            }
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return nullptr;
+    cuuint64_t dims[4] = {(cuuint64_t)g.W, (cuuint64_t)g.H, (cuuint64_t)g.C, (cuuint64_t)N};
+    cuuint64_t strides[3] = {(cuuint64_t)g.W * 4, (cuuint64_t)g.H * g.W * 4,
+                             (cuuint64_t)g.C * g.H * g.W * 4};
+    cuuint32_t box[4] = {(cuuint32_t)g.row_pitch, (cuuint32_t)g.in_rows, (cuuint32_t)g.chunk, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(&tmp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return nullptr;
+    std::lock_guard<std::mutex> lk(P->tmap_lock);
+    TmapCacheEntry &slot = P->tmap_cache[P->tmap_next++ % 4];
+    slot.x = x;
+    slot.N = N;
+    slot.map = tmp;
+    return &tmp;
+}
+
+// Blocks per cluster along the channel chunks: enough to fill the GPU once.
+int choose_split(const spconv::Geometry &g, int N) {
+    const int64_t blocks = (int64_t)N * g.tiles_y * g.tiles_x * g.groups;
+    if (blocks >= kSMs) return 1;
+    int s = (int)std::min<int64_t>(spconv::kMaxSplit, (kSMs + blocks - 1) / blocks);
+    return std::max(1, std::min(s, g.num_chunks));
 }
 
 }  // namespace
@@ -314,7 +462,7 @@ __attribute__((visibility("default"))) int spconv_forward(
     if (N == 0) return SPCONV_OK;
     if (!input || !output) return SPCONV_ERR_INVALID_ARG;
     if (((uintptr_t)input & 15) || ((uintptr_t)output & 3)) return SPCONV_ERR_INVALID_ARG;
-    const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x;
+    const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x * spconv::kMaxSplit;
     if (tiles > 0x7fffffffLL) return SPCONV_ERR_UNSUPPORTED;
     const size_t in_bytes = (size_t)N * C * H * W * sizeof(float);
     const size_t out_bytes = (size_t)N * M * g.E * g.F * sizeof(float);
@@ -322,13 +470,38 @@ __attribute__((visibility("default"))) int spconv_forward(
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return SPCONV_ERR_CUDA;
     if (dev != packed->device) return SPCONV_ERR_MISMATCH;
-    cudaError_t e = spconv::launch_forward(g, N, input, output, packed->d,
-                                           static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
+    try {
+        CUtensorMap tmp;
+        const CUtensorMap *tmap = input_tmap(packed, input, N, tmp);
+        const int split = choose_split(g, N);
+        cudaError_t e = spconv::launch_forward(g, N, split, input, output, packed->d, tmap,
+                                               static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return SPCONV_ERR_CUDA;
+        }
+    } catch (...) {
+        return SPCONV_ERR_ALLOC;
+    }
+    return SPCONV_OK;
+}
+
+__attribute__((visibility("default"))) int spconv_device_status(const spconv_packed *p,
+                                                                void *stream, int32_t *flags) {
+    if (!p || !p->dev_block) return SPCONV_ERR_INVALID_ARG;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return SPCONV_ERR_CUDA;
+    if (cur != p->device) return SPCONV_ERR_MISMATCH;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int word = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemcpy(&word, p->d.err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(p->d.err, 0, sizeof(word)) != cudaSuccess) {
         cudaGetLastError();
         return SPCONV_ERR_CUDA;
     }
-    return SPCONV_OK;
+    if (flags) *flags = (int32_t)word;
+    return word ? SPCONV_ERR_DEVICE : SPCONV_OK;
 }
 
 __attribute__((visibility("default"))) void spconv_packed_free(spconv_packed *p) {
@@ -352,6 +525,7 @@ __attribute__((visibility("default"))) const char *spconv_status_string(int stat
         case SPCONV_ERR_ALLOC: return "allocation failed";
         case SPCONV_ERR_CUDA: return "CUDA error";
         case SPCONV_ERR_MISMATCH: return "shape or device differs from the packed weights";
+        case SPCONV_ERR_DEVICE: return "a kernel reported a device-side failure";
         default: return "unknown status";
     }
 }
@@ -365,8 +539,9 @@ __attribute__((visibility("default"))) int spconv_packed_info_get(const spconv_p
     info->R = g.R; info->S = g.S; info->stride = g.stride; info->pad = g.pad;
     info->E = g.E; info->F = g.F;
     info->nnz = p->nnz;
-    info->entries = (int64_t)p->entries.size();
+    info->entries = p->nnz;
     info->tile_rows = g.tile_rows;
+    info->shift = g.shift;
     info->tile_cols = spconv::kTileCols;
     info->tiles_y = g.tiles_y;
     info->tiles_x = g.tiles_x;
@@ -383,9 +558,12 @@ __attribute__((visibility("default"))) int spconv_packed_info_get(const spconv_p
     info->num_slots = g.num_slots;
     info->on_device = p->dev_block ? 1 : 0;
     info->device_bytes = (int64_t)p->dev_bytes;
-    info->smem_bytes = (int64_t)g.smem_bytes;
+    info->smem_bytes = (int64_t)spconv::forward_smem_bytes(g, 1);
     info->max_warp_nnz = p->max_warp_nnz;
     info->mean_warp_nnz = p->mean_warp_nnz;
+    info->hdr_words = g.hdr_words;
+    info->blob_stage_bytes = (int32_t)g.blob_stage_bytes;
+    info->in_stage_bytes = (int32_t)g.in_stage_bytes;
     return SPCONV_OK;
 }
 
@@ -395,13 +573,13 @@ __attribute__((visibility("default"))) int spconv_packed_copy_array(
     const void *src = nullptr;
     int64_t n = 0;
     switch (which) {
-        case SPCONV_ARRAY_ENTRIES:
-            src = p->entries.data();
-            n = (int64_t)(p->entries.size() * sizeof(HostEntry));
+        case SPCONV_ARRAY_BLOBS:
+            src = p->blobs.data();
+            n = (int64_t)p->blobs.size();
             break;
-        case SPCONV_ARRAY_SEGPTR:
-            src = p->segptr.data();
-            n = (int64_t)(p->segptr.size() * sizeof(int32_t));
+        case SPCONV_ARRAY_BLOB_OFF:
+            src = p->blob_off.data();
+            n = (int64_t)(p->blob_off.size() * sizeof(uint32_t));
             break;
         case SPCONV_ARRAY_SLOT_OC:
             src = p->slot_oc.data();

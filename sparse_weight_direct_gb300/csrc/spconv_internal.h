@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #if defined(__CUDACC__)
@@ -15,7 +16,9 @@
 
 namespace spconv {
 
-constexpr int kTileCols = 32;  // one output column per lane
+constexpr int kTileCols = 32;   // output columns of a tile: one per lane
+constexpr int kWarps = 8;       // warps per block
+constexpr int kMaxSplit = 8;    // largest thread-block cluster of the channel split
 
 // Words of one stride-phase sub-row of a staged input row.  With stride st the
 // staged row is split into st sub-rows (column col goes to sub-row col % st at
@@ -33,6 +36,20 @@ SPCONV_HD constexpr int phase_pitch_for(int S, int stride) {
     return pp;
 }
 
+// Left shift that brings a stride-1 tile's first staged column down to a
+// multiple of 4 words (tile origins are multiples of 32 minus pad), so the
+// tile can be fetched by a TMA copy whose x coordinate is 16-byte aligned.
+SPCONV_HD constexpr int align_shift_for(int pad, int stride) {
+    return stride == 1 ? (4 - pad % 4) % 4 : 0;
+}
+
+// Words per staged input row for stride 1: the tile's columns plus room for
+// the largest alignment shift (3), rounded to 4 words (a TMA box row is a
+// multiple of 16 B).  Independent of pad so kernels can fix it at compile time.
+SPCONV_HD constexpr int row_pitch_s1(int S) {
+    return ((kTileCols - 1) + S + 3 + 3) / 4 * 4;
+}
+
 // Tiling of one layer, fixed at pack time.  The precomputed entry offsets
 // depend on it, so forward must use exactly this geometry.
 struct Geometry {
@@ -41,30 +58,39 @@ struct Geometry {
     int tiles_y, tiles_x;
     int in_rows;      // (P - 1) * stride + R
     int in_cols;      // (32 - 1) * stride + S
+    int shift;        // staged column of input column ix0 (stride 1), else 0
     int phase_pitch;  // words of one stride-phase sub-row
-    int row_pitch;    // stride * phase_pitch
-    int plane;        // words of one staged channel
+    int row_pitch;    // words of one staged row
+    int plane;        // words of one staged channel (in_rows * row_pitch)
     int chunk;        // channels staged per pipeline stage
     int num_chunks;
     int slots;        // Q: output channels a warp carries at once
     int warps;        // warps per block
     int groups;       // output-channel groups (grid y)
     int num_slots;    // groups * warps * slots
-    size_t smem_bytes;
+    int hdr_words;    // words of a weight blob header (warps * slots + 1, to 4)
+    size_t in_stage_bytes;    // staged input of one chunk, rounded to 128 B
+    size_t blob_stage_bytes;  // largest weight blob, rounded to 128 B
 };
 
 struct DeviceArrays {
-    const float2 *entries;  // {value, int offset bits}
-    const int *segptr;      // [num_slots][num_chunks + 1]
-    const int *slot_oc;     // [num_slots]
+    const unsigned char *blobs;  // weight blobs, each 16-byte aligned
+    const uint32_t *blob_off;    // [groups * num_chunks + 1] in 16-byte units
+    const int *slot_oc;          // [num_slots]
+    unsigned int *err;           // device error flags (bit 0: pipeline wait timed out)
 };
 
 // Kernel variants compiled for sm_103a.  Returns 0 if (S, stride, P, Q) has
 // an instance, else -1.
 int forward_variant_supported(int S, int stride, int P, int Q);
 
-// Enqueues the forward kernel.  Returns cudaSuccess or the launch error.
-cudaError_t launch_forward(const Geometry &g, int N, const float *x, float *y,
-                           const DeviceArrays &d, cudaStream_t stream);
+// Dynamic shared memory a launch needs with `split` blocks per cluster.
+size_t forward_smem_bytes(const Geometry &g, int split);
+
+// Enqueues the forward kernel.  tmap is a tiled tensor map of the input for
+// stride-1 layers whose row stride is a multiple of 16 bytes (nullptr:
+// stage with cp.async).  Returns cudaSuccess or the launch error.
+cudaError_t launch_forward(const Geometry &g, int N, int split, const float *x, float *y,
+                           const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream);
 
 }  // namespace spconv
