@@ -129,9 +129,9 @@ typedef struct spconv_packed_info {
     int32_t C, H, W, M, R, S, stride, pad, E, F;
     int64_t nnz;            /* nonzeros of the CSR input                        */
     int64_t entries;        /* packed (value, offset) entries (== nnz)          */
-    int32_t tile_rows;      /* output rows per tile (per lane)                  */
+    int32_t tile_rows;      /* output rows each lane carries                    */
     int32_t shift;          /* staged column of a tile's first input column     */
-    int32_t tile_cols;      /* output columns per tile (one per lane: 32)       */
+    int32_t tile_cols;      /* output columns per tile (lanes per lane row)     */
     int32_t tiles_y, tiles_x;
     int32_t in_rows;        /* staged input rows per channel (with halo)        */
     int32_t in_cols;        /* staged input columns per channel (with halo)     */
@@ -152,7 +152,8 @@ typedef struct spconv_packed_info {
     int32_t hdr_words;      /* 32-bit words of a weight blob's header           */
     int32_t blob_stage_bytes; /* largest weight blob (bytes, rounded to 128)    */
     int32_t in_stage_bytes;   /* staged input of one chunk (bytes, to 128)      */
-    int32_t reserved;
+    int32_t lane_rows;        /* lane rows of a warp (output rows per tile =    */
+                              /* lane_rows * tile_rows)                         */
 } spconv_packed_info;
 
 int spconv_packed_info_get(const spconv_packed *p, spconv_packed_info *info);

@@ -49,7 +49,7 @@ class PackedInfo(ctypes.Structure):
         (n, ctypes.c_int64) for n in
         ("device_bytes", "smem_bytes", "max_warp_nnz", "mean_warp_nnz")] + [
         (n, ctypes.c_int32) for n in
-        ("hdr_words", "blob_stage_bytes", "in_stage_bytes", "reserved")]
+        ("hdr_words", "blob_stage_bytes", "in_stage_bytes", "lane_rows")]
 
 
 def lib() -> ctypes.CDLL:

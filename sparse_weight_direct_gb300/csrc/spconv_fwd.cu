@@ -33,6 +33,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
+#include <utility>
 
 #include "spconv_internal.h"
 
@@ -42,6 +44,7 @@ namespace spconv {
 namespace {
 
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
+constexpr int kMaxDynamicSmem = 200 * 1024;                   // upper bound of any plan
 
 struct KParams {
     const float *x;
@@ -141,36 +144,38 @@ __device__ __forceinline__ void cp_async_wait_all() {
 
 // cp.async staging of channels [c0, c0 + cc) of image n: staged element
 // (channel cl, row, col) holds input (c0 + cl, iy0 + row, ix0 + col), zero
-// outside the image.  All threads take part; indices advance incrementally.
+// outside the image.  A thread owns fixed positions (row, col) of the staged
+// plane (its validity and both offsets do not depend on the channel) and walks
+// the chunk's channels for each, so the inner loop is two adds and a cp.async;
+// consecutive threads take consecutive columns (coalesced per channel).
 template <int ST_CT>
 __device__ __forceinline__ void stage_input_cp_async(const KParams &p, float *buf, int n, int c0,
                                                      int cc, int iy0, int ix0) {
     const int st = ST_CT ? ST_CT : p.stride;
-    const int in_cols = p.in_cols, in_rows = p.in_rows;
-    const int total = cc * in_rows * in_cols;
-    int e = threadIdx.x;
-    if (e >= total) return;
-    const int dcol = blockDim.x % in_cols, drow = blockDim.x / in_cols;
-    int col = e % in_cols;
-    int rr = e / in_cols;
-    int row = rr % in_rows;
-    int cl = rr / in_rows;
-    const float *xn = p.x + (size_t)n * p.C * p.H * p.W;
-    for (; e < total; e += blockDim.x) {
+    const int in_cols = p.in_cols;
+    const int plane_elems = p.in_rows * in_cols;
+    const size_t hw = (size_t)p.H * p.W;
+    const float *xc0 = p.x + ((size_t)n * p.C + c0) * hw;
+    const int T = blockDim.x;
+    int row = threadIdx.x / in_cols, col = threadIdx.x - row * in_cols;
+    const int drow = T / in_cols, dcol = T - drow * in_cols;
+    for (int e = threadIdx.x; e < plane_elems; e += T) {
         const int gy = iy0 + row, gx = ix0 + col;
         const bool ok = (unsigned)gy < (unsigned)p.H && (unsigned)gx < (unsigned)p.W;
-        const float *src = ok ? xn + ((size_t)(c0 + cl) * p.H + gy) * p.W + gx : p.x;
+        const float *src = ok ? xc0 + (size_t)gy * p.W + gx : p.x;
+        const size_t src_step = ok ? hw : 0;
         const int phys = (st == 1) ? col + p.shift : (col % st) * p.phase_pitch + col / st;
-        cp_async_4(buf + cl * p.plane + row * p.row_pitch + phys, src, ok);
-        col += dcol;
+        float *dst = buf + row * p.row_pitch + phys;
+        for (int cl = 0; cl < cc; ++cl) {
+            cp_async_4(dst, src, ok);
+            dst += p.plane;
+            src += src_step;
+        }
         row += drow;
+        col += dcol;
         if (col >= in_cols) {
             col -= in_cols;
             ++row;
-        }
-        while (row >= in_rows) {
-            row -= in_rows;
-            ++cl;
         }
     }
 }
@@ -205,21 +210,25 @@ __device__ __forceinline__ void run_segment(float (&acc)[P], const float *sb, co
     }
 }
 
-// P: output rows per lane; Q: output channels per warp; S_CT/ST_CT: kernel
-// width and stride when known at compile time (0 = read from p).
-template <int P, int Q, int S_CT, int ST_CT>
+// P: output rows per lane; Q: output channels per warp; LR: lane rows (1, or 2
+// interleaved half-warps of 16 lanes for outputs at most 16 wide); S_CT/ST_CT:
+// kernel width and stride when known at compile time (0 = read from p).
+template <int P, int Q, int S_CT, int ST_CT, int LR>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     spconv_fwd_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar[2];
     // stage buffers start on a 128-byte boundary (TMA destination)
     unsigned char *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    constexpr int LC = kLanes / LR;  // lanes per lane row = output columns of a tile
     constexpr int ROW_STEP =
-        S_CT ? (ST_CT == 1 ? row_pitch_s1(S_CT) : ST_CT * ST_CT * phase_pitch_for(S_CT, ST_CT))
+        S_CT ? LR * (ST_CT == 1 ? row_pitch_s1(S_CT, LR)
+                                : ST_CT * ST_CT * phase_pitch_for(S_CT, ST_CT))
              : 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ly = lane / LC, lx = lane % LC;  // lane row / column of this thread
     const int st = ST_CT ? ST_CT : p.stride;
-    const int row_step = st * p.row_pitch;
+    const int row_step = LR * st * p.row_pitch;  // between this lane's output rows
 
     const int split = p.split;
     int b = blockIdx.x;
@@ -232,8 +241,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int group = blockIdx.y;
     const int k_begin = kr * p.num_chunks / split;
     const int k_end = (kr + 1) * p.num_chunks / split;
-    const int iy0 = ty * P * st - p.pad;
-    const int ix0 = tx * kTileCols * st - p.pad;
+    const int iy0 = ty * (LR * P) * st - p.pad;
+    const int ix0 = tx * LC * st - p.pad;
 
     if (threadIdx.x == 0) {
         mbar_init(&bar[0], 1);
@@ -286,7 +295,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         failed = __syncthreads_or(!ok) != 0;
         if (failed) break;
         const unsigned char *base = smem + (size_t)s * p.stage_bytes;
-        const float *sb = reinterpret_cast<const float *>(base) + lane;
+        const float *sb = reinterpret_cast<const float *>(base) + ly * st * p.row_pitch + lx;
         const uint32_t *hdr = reinterpret_cast<const uint32_t *>(base + p.in_stage_bytes);
         const float2 *ent = reinterpret_cast<const float2 *>(hdr + p.hdr_words);
 #pragma unroll
@@ -304,7 +313,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     }
 
     const int slot0 = (group * kWarps + warp) * Q;
-    const int ox = tx * kTileCols + lane;
+    const int ox = tx * LC + lx;
+    const int oy0 = ty * (LR * P) + ly;  // this lane's output rows: oy0 + LR * r
     if (split == 1) {
         if (failed || ox >= p.F) return;
 #pragma unroll
@@ -314,7 +324,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
 #pragma unroll
             for (int r = 0; r < P; ++r) {
-                const int oy = ty * P + r;
+                const int oy = oy0 + LR * r;
                 if (oy < p.E) yo[(size_t)oy * p.F] = acc[q][r];
             }
         }
@@ -338,7 +348,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             if (m < 0) continue;
             float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
             for (int r = 0; r < P; ++r) {
-                const int oy = ty * P + r;
+                const int oy = oy0 + LR * r;
                 float sum = 0.f;
                 for (int j = 0; j < split; ++j) {
                     const float *rp = cluster.map_shared_rank(part, j);
@@ -354,38 +364,65 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 using KernelFn = void (*)(const KParams, const CUtensorMap);
 
 template <int P, int Q>
-KernelFn pick_sst(int S, int stride) {
-    if (S == 3 && stride == 1) return spconv_fwd_kernel<P, Q, 3, 1>;
-    if (S == 5 && stride == 1) return spconv_fwd_kernel<P, Q, 5, 1>;
-    if (S == 11 && stride == 4) return spconv_fwd_kernel<P, Q, 11, 4>;
-    if (stride == 1) return spconv_fwd_kernel<P, Q, 0, 1>;
-    return spconv_fwd_kernel<P, Q, 0, 0>;
+KernelFn pick_sst(int S, int stride, int LR) {
+    if (LR == 2) {
+        if (stride != 1) return nullptr;
+        if (S == 3) return spconv_fwd_kernel<P, Q, 3, 1, 2>;
+        return spconv_fwd_kernel<P, Q, 0, 1, 2>;
+    }
+    if (S == 3 && stride == 1) return spconv_fwd_kernel<P, Q, 3, 1, 1>;
+    if (S == 5 && stride == 1) return spconv_fwd_kernel<P, Q, 5, 1, 1>;
+    if (S == 11 && stride == 4) return spconv_fwd_kernel<P, Q, 11, 4, 1>;
+    if (stride == 1) return spconv_fwd_kernel<P, Q, 0, 1, 1>;
+    return spconv_fwd_kernel<P, Q, 0, 0, 1>;
 }
 
 template <int P>
-KernelFn pick_q(int S, int stride, int Q) {
+KernelFn pick_q(int S, int stride, int Q, int LR) {
     switch (Q) {
-        case 1: return pick_sst<P, 1>(S, stride);
-        case 2: return pick_sst<P, 2>(S, stride);
-        case 4: return pick_sst<P, 4>(S, stride);
+        case 1: return pick_sst<P, 1>(S, stride, LR);
+        case 2: return pick_sst<P, 2>(S, stride, LR);
+        case 4: return pick_sst<P, 4>(S, stride, LR);
         default: return nullptr;
     }
 }
 
-KernelFn pick(int S, int stride, int P, int Q) {
+KernelFn pick(int S, int stride, int P, int Q, int LR) {
+    if (LR != 1 && LR != 2) return nullptr;
     switch (P) {
-        case 7: return pick_q<7>(S, stride, Q);
-        case 8: return pick_q<8>(S, stride, Q);
+        case 7: return pick_q<7>(S, stride, Q, LR);
+        case 8: return pick_q<8>(S, stride, Q, LR);
         default: return nullptr;
     }
 }
 
 size_t stage_bytes(const Geometry &g) { return g.in_stage_bytes + g.blob_stage_bytes; }
 
+// The dynamic shared-memory limit is a per-function, per-device attribute:
+// raise it once to the largest size any plan uses, and remember that.
+cudaError_t raise_smem_limit(KernelFn fn) {
+    constexpr int kMaxDev = 64;
+    constexpr int kSlots = 256;
+    static std::mutex lock;
+    static std::pair<KernelFn, int> done[kSlots];
+    static int ndone = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(lock);
+    for (int i = 0; i < ndone; ++i)
+        if (done[i].first == fn && done[i].second == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
+    if (e != cudaSuccess) return e;
+    if (ndone < kSlots && dev < kMaxDev) done[ndone++] = {fn, dev};
+    return cudaSuccess;
+}
+
 }  // namespace
 
-int forward_variant_supported(int S, int stride, int P, int Q) {
-    return pick(S, stride, P, Q) ? 0 : -1;
+int forward_variant_supported(int S, int stride, int P, int Q, int LR) {
+    return pick(S, stride, P, Q, LR) ? 0 : -1;
 }
 
 size_t forward_smem_bytes(const Geometry &g, int split) {
@@ -400,14 +437,12 @@ size_t forward_smem_bytes(const Geometry &g, int split) {
 
 cudaError_t launch_forward(const Geometry &g, int N, int split, const float *x, float *y,
                            const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream) {
-    KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots);
+    KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows);
     if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks)
         return cudaErrorInvalidConfiguration;
     const size_t smem = forward_smem_bytes(g, split);
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = raise_smem_limit(fn);
         if (e != cudaSuccess) return e;
     }
     KParams p;

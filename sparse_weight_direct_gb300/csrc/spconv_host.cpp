@@ -60,7 +60,7 @@ struct spconv_packed {
 namespace {
 
 constexpr size_t kSmemBudget = 110 * 1024;  // two resident blocks per SM
-constexpr int kSMs = 152;                   // GB300 SM count, for the split heuristic
+constexpr int kSMs = 152;                   // GB300 SM count, for the grid heuristics
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -103,20 +103,25 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     g.C = C; g.H = H; g.W = W; g.M = M; g.R = R; g.S = S; g.stride = stride; g.pad = pad;
     g.E = out_extent(H, R, stride, pad);
     g.F = out_extent(W, S, stride, pad);
-    // rows per tile: the instance (7 or 8) that wastes the fewest rows
+    // two interleaved lane rows of 16 lanes for outputs at most 16 wide
+    g.lane_rows = (stride == 1 && g.F <= 16) ? 2 : 1;
+    g.tile_w = spconv::kLanes / g.lane_rows;
+    // rows per lane: the instance (7 or 8) that wastes the fewest rows
     int best_p = 8, best_waste = 1 << 30;
     for (int P : {8, 7}) {
-        const int waste = (g.E + P - 1) / P * P - g.E;
+        const int h = P * g.lane_rows;
+        const int waste = (g.E + h - 1) / h * h - g.E;
         if (waste < best_waste) { best_waste = waste; best_p = P; }
     }
     g.tile_rows = best_p;
-    g.tiles_y = (g.E + best_p - 1) / best_p;
-    g.tiles_x = (g.F + spconv::kTileCols - 1) / spconv::kTileCols;
-    g.in_rows = (best_p - 1) * stride + R;
-    g.in_cols = (spconv::kTileCols - 1) * stride + S;
+    g.tile_h = best_p * g.lane_rows;
+    g.tiles_y = (g.E + g.tile_h - 1) / g.tile_h;
+    g.tiles_x = (g.F + g.tile_w - 1) / g.tile_w;
+    g.in_rows = (g.tile_h - 1) * stride + R;
+    g.in_cols = (g.tile_w - 1) * stride + S;
     g.shift = spconv::align_shift_for(pad, stride);
     if (stride == 1) {
-        g.phase_pitch = spconv::row_pitch_s1(S);
+        g.phase_pitch = spconv::row_pitch_s1(S, g.lane_rows);
         g.row_pitch = g.phase_pitch;
     } else {
         g.phase_pitch = spconv::phase_pitch_for(S, stride);
@@ -124,13 +129,23 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     }
     g.plane = g.in_rows * g.row_pitch;
     g.warps = spconv::kWarps;
-    // output channels per warp: four when that still leaves >= 4 groups
-    g.slots = M >= 4 * spconv::kWarps * 4 ? 4 : (M >= 4 * spconv::kWarps * 2 ? 2 : 1);
+    // output channels per warp: the largest Q in {4, 2, 1} whose one-image
+    // grid, with the channels split over a full cluster, still covers ~80 % of
+    // the SMs (small layers trade per-warp reuse for parallelism)
+    const int64_t spatial = (int64_t)g.tiles_y * g.tiles_x;
+    g.slots = 1;
+    for (int Q : {4, 2}) {
+        const int64_t groups = (M + (int64_t)spconv::kWarps * Q - 1) / ((int64_t)spconv::kWarps * Q);
+        if (spatial * groups * spconv::kMaxSplit * 5 >= (int64_t)kSMs * 4) {
+            g.slots = Q;
+            break;
+        }
+    }
     g.groups = (M + spconv::kWarps * g.slots - 1) / (spconv::kWarps * g.slots);
     g.num_slots = g.groups * spconv::kWarps * g.slots;
     g.hdr_words = (int)round_up((size_t)spconv::kWarps * g.slots + 1, 4);
     if (g.groups > 65535) return SPCONV_ERR_UNSUPPORTED;
-    if (spconv::forward_variant_supported(S, stride, g.tile_rows, g.slots) != 0)
+    if (spconv::forward_variant_supported(S, stride, g.tile_rows, g.slots, g.lane_rows) != 0)
         return SPCONV_ERR_UNSUPPORTED;
     return SPCONV_OK;
 }
@@ -542,7 +557,8 @@ __attribute__((visibility("default"))) int spconv_packed_info_get(const spconv_p
     info->entries = p->nnz;
     info->tile_rows = g.tile_rows;
     info->shift = g.shift;
-    info->tile_cols = spconv::kTileCols;
+    info->tile_cols = g.tile_w;
+    info->lane_rows = g.lane_rows;
     info->tiles_y = g.tiles_y;
     info->tiles_x = g.tiles_x;
     info->in_rows = g.in_rows;

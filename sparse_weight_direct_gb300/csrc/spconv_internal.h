@@ -16,7 +16,7 @@
 
 namespace spconv {
 
-constexpr int kTileCols = 32;   // output columns of a tile: one per lane
+constexpr int kLanes = 32;
 constexpr int kWarps = 8;       // warps per block
 constexpr int kMaxSplit = 8;    // largest thread-block cluster of the channel split
 
@@ -26,7 +26,7 @@ constexpr int kMaxSplit = 8;    // largest thread-block cluster of the channel s
 // words.  For st dividing 32 the pitch is padded to 32/st (mod 32) so the
 // st sub-rows start in different banks.  Host planner and kernels share it.
 SPCONV_HD constexpr int phase_pitch_for(int S, int stride) {
-    const int in_cols = (kTileCols - 1) * stride + S;
+    const int in_cols = (kLanes - 1) * stride + S;
     if (stride == 1) return in_cols;
     int pp = (in_cols + stride - 1) / stride;
     if (32 % stride == 0) {
@@ -43,21 +43,30 @@ SPCONV_HD constexpr int align_shift_for(int pad, int stride) {
     return stride == 1 ? (4 - pad % 4) % 4 : 0;
 }
 
-// Words per staged input row for stride 1: the tile's columns plus room for
-// the largest alignment shift (3), rounded to 4 words (a TMA box row is a
-// multiple of 16 B).  Independent of pad so kernels can fix it at compile time.
-SPCONV_HD constexpr int row_pitch_s1(int S) {
-    return ((kTileCols - 1) + S + 3 + 3) / 4 * 4;
+// Words per staged input row for stride 1 with `lane_rows` lane rows of
+// 32 / lane_rows lanes: the tile's columns plus room for the largest alignment
+// shift (3), rounded to 4 words (a TMA box row is a multiple of 16 B).  With
+// two lane rows (interleaved output rows) the half-warps read rows one pitch
+// apart, so the pitch is also made 16 (mod 32) words: the halves then hit
+// disjoint banks.  Independent of pad so kernels can fix it at compile time.
+SPCONV_HD constexpr int row_pitch_s1(int S, int lane_rows) {
+    const int need = (kLanes / lane_rows - 1) + S + 3;
+    if (lane_rows == 1) return (need + 3) / 4 * 4;
+    int rp = 16;
+    while (rp < need) rp += 32;
+    return rp;
 }
 
 // Tiling of one layer, fixed at pack time.  The precomputed entry offsets
 // depend on it, so forward must use exactly this geometry.
 struct Geometry {
     int C, H, W, M, R, S, stride, pad, E, F;
-    int tile_rows;    // P: output rows of a tile; each lane carries P rows
+    int tile_rows;    // P: output rows each lane carries
+    int lane_rows;    // LR: lane rows of a warp (1, or 2 for outputs <= 16 wide)
+    int tile_h, tile_w;  // output tile: LR * P rows x 32 / LR columns
     int tiles_y, tiles_x;
-    int in_rows;      // (P - 1) * stride + R
-    int in_cols;      // (32 - 1) * stride + S
+    int in_rows;      // (tile_h - 1) * stride + R
+    int in_cols;      // (tile_w - 1) * stride + S
     int shift;        // staged column of input column ix0 (stride 1), else 0
     int phase_pitch;  // words of one stride-phase sub-row
     int row_pitch;    // words of one staged row
@@ -80,9 +89,9 @@ struct DeviceArrays {
     unsigned int *err;           // device error flags (bit 0: pipeline wait timed out)
 };
 
-// Kernel variants compiled for sm_103a.  Returns 0 if (S, stride, P, Q) has
-// an instance, else -1.
-int forward_variant_supported(int S, int stride, int P, int Q);
+// Kernel variants compiled for sm_103a.  Returns 0 if (S, stride, P, Q, LR)
+// has an instance, else -1.
+int forward_variant_supported(int S, int stride, int P, int Q, int LR);
 
 // Dynamic shared memory a launch needs with `split` blocks per cluster.
 size_t forward_smem_bytes(const Geometry &g, int split);

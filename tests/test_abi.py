@@ -111,9 +111,11 @@ def test_packed_layout_decodes_to_csr(name):
         want = sorted(zip(colidx[lo:hi].tolist(), value[lo:hi].astype(np.float64).tolist()))
         assert rows.get(m, []) == want
     # staged input tile covers every tap of every output of a tile
-    assert info["in_rows"] == (info["tile_rows"] - 1) * L.stride + L.R
+    tile_h = info["tile_rows"] * info["lane_rows"]
+    assert info["tile_cols"] * info["lane_rows"] == 32
+    assert info["in_rows"] == (tile_h - 1) * L.stride + L.R
     assert info["in_cols"] == (info["tile_cols"] - 1) * L.stride + L.S
-    assert info["tiles_y"] * info["tile_rows"] >= L.E
+    assert info["tiles_y"] * tile_h >= L.E
     assert info["tiles_x"] * info["tile_cols"] >= L.F
     assert info["smem_bytes"] <= 200 * 1024
     w.close()
