@@ -154,6 +154,8 @@ typedef struct spconv_packed_info {
     int32_t in_stage_bytes;   /* staged input of one chunk (bytes, to 128)      */
     int32_t lane_rows;        /* lane rows of a warp (output rows per tile =    */
                               /* lane_rows * tile_rows)                         */
+    int32_t dense_groups;     /* leading groups whose blobs are dense-tap       */
+    int32_t dense_mask_words; /* words of a dense blob's slot masks            */
 } spconv_packed_info;
 
 int spconv_packed_info_get(const spconv_packed *p, spconv_packed_info *info);
@@ -161,9 +163,12 @@ int spconv_packed_info_get(const spconv_packed *p, spconv_packed_info *info);
 /* Which host-side array spconv_packed_copy_array copies. */
 typedef enum spconv_array {
     SPCONV_ARRAY_BLOBS = 0,    /* the weight blobs, one per (group, chunk), each    */
-                               /* 16-byte aligned: hdr_words uint32 entry indices  */
-                               /* (slot w*Q+q spans [hdr[w*Q+q], hdr[w*Q+q+1])),   */
-                               /* then entries of {float value, int32 offset}      */
+                               /* 16-byte aligned.  Sparse groups: hdr_words       */
+                               /* uint32 entry indices (slot w*Q+q spans           */
+                               /* [hdr[w*Q+q], hdr[w*Q+q+1])), then entries of     */
+                               /* {float value, int32 offset}.  Dense groups:      */
+                               /* dense_mask_words uint32 slot masks [warp][chan], */
+                               /* then floats [warp][chan][slot][R*S rounded to 4] */
     SPCONV_ARRAY_BLOB_OFF = 1, /* uint32 [groups * num_chunks + 1]: blob starts in  */
                                /* 16-byte units                                     */
     SPCONV_ARRAY_SLOT_OC = 2   /* int32 [num_slots]: output channel of a slot or -1 */

@@ -49,7 +49,8 @@ class PackedInfo(ctypes.Structure):
         (n, ctypes.c_int64) for n in
         ("device_bytes", "smem_bytes", "max_warp_nnz", "mean_warp_nnz")] + [
         (n, ctypes.c_int32) for n in
-        ("hdr_words", "blob_stage_bytes", "in_stage_bytes", "lane_rows")]
+        ("hdr_words", "blob_stage_bytes", "in_stage_bytes", "lane_rows", "dense_groups",
+         "dense_mask_words")]
 
 
 def lib() -> ctypes.CDLL:

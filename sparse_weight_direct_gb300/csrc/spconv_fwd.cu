@@ -52,10 +52,11 @@ struct KParams {
     const unsigned char *blobs;
     const uint32_t *blob_off;
     const int *slot_oc;
+    const int *group_dense;  // per group: 1 = dense-tap blobs, 0 = sparse entries
     unsigned int *err;
     int N, C, H, W, M, E, F, stride, pad;
     int tiles_y, tiles_x, in_rows, in_cols, shift, phase_pitch, row_pitch, plane;
-    int chunk, num_chunks, split, hdr_words;
+    int chunk, num_chunks, split, hdr_words, dense_mask_words;
     int in_stage_bytes, stage_bytes, in_tma_bytes;
     int use_tma;
 };
@@ -182,6 +183,10 @@ __device__ __forceinline__ void stage_input_cp_async(const KParams &p, float *bu
 
 // ---------------------------------------------------------------- compute
 
+// Kernel instances that carry the dense-tap path: stride 1, K x K with K = 3, 5.
+template <int S_CT, int ST_CT>
+constexpr bool kDenseTaps = ST_CT == 1 && (S_CT == 3 || S_CT == 5);
+
 template <int P, int ROW_STEP>
 __device__ __forceinline__ void apply_entry(float (&acc)[P], const float *sb, float v, int off,
                                             int row_step) {
@@ -207,6 +212,53 @@ __device__ __forceinline__ void run_segment(float (&acc)[P], const float *sb, co
     if (j < j1) {  // tail
         const float2 e = ent[j];
         apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
+    }
+}
+
+// Dense-tap accumulation of one chunk for a warp of dense output channels: the
+// channel's input window (LR*(P-1)+K rows x K columns around this lane's output
+// column) is loaded into registers once and every tap of every slot of the
+// warp is applied to it with compile-time register indices.  The blob holds,
+// per (warp, channel), a mask of the slots with any nonzero in that channel
+// and, per (warp, channel, slot), the K*K weights (zeros included) padded to a
+// multiple of 4 floats.  Useful fraction = density of the channel's K x K
+// block; shared-memory reads per FMA drop by about the slot count.
+template <int P, int Q, int K, int LR, int RP>
+__device__ __forceinline__ void run_dense_chunk(float (&acc)[Q][P], const float *sb,
+                                                const uint32_t *dmask, const float4 *dw,
+                                                int warp, int chunk, int cc, int plane) {
+    constexpr int WR = LR * (P - 1) + K;  // window rows
+    constexpr int KK4 = (K * K + 3) / 4;  // float4 per weight block
+    for (int cl = 0; cl < cc; ++cl) {
+        const uint32_t mask = dmask[warp * chunk + cl];
+        if (mask == 0) continue;
+        const float *s = sb + cl * plane;
+        float win[WR][K];
+#pragma unroll
+        for (int i = 0; i < WR; ++i)
+#pragma unroll
+            for (int j = 0; j < K; ++j) win[i][j] = s[i * RP + j];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            if (!(mask & (1u << q))) continue;
+            const float4 *wq = dw + ((size_t)(warp * chunk + cl) * Q + q) * KK4;
+            float w[KK4 * 4];
+#pragma unroll
+            for (int t = 0; t < KK4; ++t) {
+                const float4 v = wq[t];
+                w[4 * t] = v.x;
+                w[4 * t + 1] = v.y;
+                w[4 * t + 2] = v.z;
+                w[4 * t + 3] = v.w;
+            }
+#pragma unroll
+            for (int r = 0; r < K; ++r)
+#pragma unroll
+                for (int c = 0; c < K; ++c)
+#pragma unroll
+                    for (int pr = 0; pr < P; ++pr)
+                        acc[q][pr] = fmaf(w[r * K + c], win[LR * pr + r][c], acc[q][pr]);
+        }
     }
 }
 
@@ -239,6 +291,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int ty = b % p.tiles_y;
     const int n = b / p.tiles_y;
     const int group = blockIdx.y;
+    const bool dense = p.group_dense[group] != 0;
     const int k_begin = kr * p.num_chunks / split;
     const int k_end = (kr + 1) * p.num_chunks / split;
     const int iy0 = ty * (LR * P) * st - p.pad;
@@ -297,12 +350,22 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         const unsigned char *base = smem + (size_t)s * p.stage_bytes;
         const float *sb = reinterpret_cast<const float *>(base) + ly * st * p.row_pitch + lx;
         const uint32_t *hdr = reinterpret_cast<const uint32_t *>(base + p.in_stage_bytes);
-        const float2 *ent = reinterpret_cast<const float2 *>(hdr + p.hdr_words);
+        if constexpr (kDenseTaps<S_CT, ST_CT>) {
+            if (dense) {
+                const int k = k_begin + it;
+                run_dense_chunk<P, Q, S_CT, LR, row_pitch_s1(S_CT, LR)>(
+                    acc, sb + p.shift, hdr, reinterpret_cast<const float4 *>(hdr + p.dense_mask_words),
+                    warp, p.chunk, min(p.chunk, p.C - k * p.chunk), p.plane);
+            }
+        }
+        if (!dense) {
+            const float2 *ent = reinterpret_cast<const float2 *>(hdr + p.hdr_words);
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const int j0 = (int)hdr[warp * Q + q];
-            const int j1 = (int)hdr[warp * Q + q + 1];
-            run_segment<P, ROW_STEP>(acc[q], sb, ent, j0, j1, row_step);
+            for (int q = 0; q < Q; ++q) {
+                const int j0 = (int)hdr[warp * Q + q];
+                const int j1 = (int)hdr[warp * Q + q + 1];
+                run_segment<P, ROW_STEP>(acc[q], sb, ent, j0, j1, row_step);
+            }
         }
         __syncthreads();  // stage s is free again
         if (it + 2 < nmine) issue(k_begin + it + 2, s);
@@ -421,6 +484,10 @@ cudaError_t raise_smem_limit(KernelFn fn) {
 
 }  // namespace
 
+bool dense_taps_supported(int R, int S, int stride, int LR) {
+    return stride == 1 && R == S && (S == 3 || (S == 5 && LR == 1));
+}
+
 int forward_variant_supported(int S, int stride, int P, int Q, int LR) {
     return pick(S, stride, P, Q, LR) ? 0 : -1;
 }
@@ -451,6 +518,7 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, const float *x, 
     p.blobs = d.blobs;
     p.blob_off = d.blob_off;
     p.slot_oc = d.slot_oc;
+    p.group_dense = d.group_dense;
     p.err = d.err;
     p.N = N; p.C = g.C; p.H = g.H; p.W = g.W; p.M = g.M; p.E = g.E; p.F = g.F;
     p.stride = g.stride; p.pad = g.pad;
@@ -458,6 +526,7 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, const float *x, 
     p.shift = g.shift; p.phase_pitch = g.phase_pitch; p.row_pitch = g.row_pitch;
     p.plane = g.plane; p.chunk = g.chunk; p.num_chunks = g.num_chunks; p.split = split;
     p.hdr_words = g.hdr_words;
+    p.dense_mask_words = g.dense_mask_words;
     p.in_stage_bytes = (int)g.in_stage_bytes;
     p.stage_bytes = (int)stage_bytes(g);
     p.in_tma_bytes = g.chunk * g.plane * (int)sizeof(float);

@@ -48,6 +48,7 @@ struct spconv_packed {
     std::vector<unsigned char> blobs;  // concatenated (group, chunk) blobs
     std::vector<uint32_t> blob_off;    // [groups * num_chunks + 1], 16-byte units
     std::vector<int32_t> slot_oc;      // [num_slots]
+    std::vector<int32_t> group_dense;  // [groups]
     int device = -1;
     void *dev_block = nullptr;
     size_t dev_bytes = 0;
@@ -61,6 +62,10 @@ namespace {
 
 constexpr size_t kSmemBudget = 110 * 1024;  // two resident blocks per SM
 constexpr int kSMs = 152;                   // GB300 SM count, for the grid heuristics
+// Rows at least this dense take the dense-tap path where the shape allows it:
+// it issues K*K FMAs per (slot, channel) block with zeros included, about four
+// times cheaper per FMA than a shared-memory load per FMA.
+constexpr double kDenseRowMin = 0.30;
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -150,28 +155,57 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     return SPCONV_OK;
 }
 
-// Longest row first onto the warp with the least work that has a free slot.
+// Output channels whose rows are dense enough go to leading "dense" groups
+// (densest first, dealt round-robin over the warps); the rest are binned onto
+// the warps of the sparse groups longest row first onto the least-loaded warp
+// that has a free slot.  Sets groups / num_slots / slot_oc / group_dense.
 void bin_channels(spconv_packed &P, const int32_t *rowptr) {
-    const spconv::Geometry &g = P.g;
-    std::vector<int> order(g.M);
-    std::iota(order.begin(), order.end(), 0);
-    std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
-        return rowptr[a + 1] - rowptr[a] > rowptr[b + 1] - rowptr[b];
-    });
-    const int nwarps = g.groups * g.warps;
+    spconv::Geometry &g = P.g;
+    const int per_group = g.warps * g.slots;
+    const double crs = (double)g.C * g.R * g.S;
+    std::vector<int> dense, sparse;
+    const bool can_dense = spconv::dense_taps_supported(g.R, g.S, g.stride, g.lane_rows);
+    for (int m = 0; m < g.M; ++m) {
+        const double d = (rowptr[m + 1] - rowptr[m]) / crs;
+        (can_dense && d >= kDenseRowMin ? dense : sparse).push_back(m);
+    }
+    auto nnz_of = [&](int m) { return (int64_t)rowptr[m + 1] - rowptr[m]; };
+    std::stable_sort(dense.begin(), dense.end(), [&](int a, int b) { return nnz_of(a) > nnz_of(b); });
+    // a dense group less than half full is not worth a group of its own
+    const int tail = (int)dense.size() % per_group;
+    if (tail && tail * 2 < per_group) {
+        sparse.insert(sparse.end(), dense.end() - tail, dense.end());
+        dense.resize(dense.size() - tail);
+    }
+    std::stable_sort(sparse.begin(), sparse.end(), [&](int a, int b) { return nnz_of(a) > nnz_of(b); });
+    const int gd = ((int)dense.size() + per_group - 1) / per_group;
+    const int gs = ((int)sparse.size() + per_group - 1) / per_group;
+    g.dense_groups = gd;
+    g.groups = std::max(1, gd + gs);
+    g.num_slots = g.groups * per_group;
+    P.slot_oc.assign(g.num_slots, -1);
+    P.group_dense.assign(g.groups, 0);
+    for (int grp = 0; grp < gd; ++grp) P.group_dense[grp] = 1;
+    // dense: the i-th densest channel goes to warp i % warps_total, slot i / warps_total
+    const int dwarps = gd * g.warps;
+    for (size_t i = 0; i < dense.size(); ++i) {
+        const int w = (int)(i % dwarps), q = (int)(i / dwarps);
+        P.slot_oc[(size_t)w * g.slots + q] = dense[i];
+    }
+    // sparse: LPT over the warps of the sparse groups
+    const int nwarps = gs * g.warps, w0 = gd * g.warps;
     using Item = std::pair<int64_t, int>;  // (load, warp)
     std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
     for (int w = 0; w < nwarps; ++w) heap.push({0, w});
     std::vector<int> fill(nwarps, 0);
     std::vector<int64_t> load(nwarps, 0);
-    P.slot_oc.assign(g.num_slots, -1);
-    for (int m : order) {
+    for (int m : sparse) {
         const Item it = heap.top();
         heap.pop();
         const int w = it.second;
-        P.slot_oc[(size_t)w * g.slots + fill[w]] = m;
+        P.slot_oc[(size_t)(w0 + w) * g.slots + fill[w]] = m;
         ++fill[w];
-        load[w] += rowptr[m + 1] - rowptr[m];
+        load[w] += nnz_of(m);
         if (fill[w] < g.slots) heap.push({load[w], w});
     }
     int64_t mx = 0, sum = 0, used = 0;
@@ -181,6 +215,12 @@ void bin_channels(spconv_packed &P, const int32_t *rowptr) {
     }
     P.max_warp_nnz = mx;
     P.mean_warp_nnz = used ? sum / used : 0;
+}
+
+size_t dense_blob_bytes(const spconv::Geometry &g, int chunk) {
+    const size_t mask_words = round_up((size_t)g.warps * chunk, 4);
+    const size_t kk4 = round_up((size_t)g.R * g.S, 4);
+    return mask_words * 4 + (size_t)g.warps * chunk * g.slots * kk4 * 4;
 }
 
 // Chunk size: the largest that keeps two pipeline stages (staged input plus
@@ -200,8 +240,8 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
     for (int chunk = cap; chunk >= 1; --chunk) {
         const int nch = (C + chunk - 1) / chunk;
         const size_t in_stage = round_up((size_t)chunk * g.plane * sizeof(float), 128);
-        size_t blob_max = 0;
-        for (int grp = 0; grp < g.groups; ++grp) {
+        size_t blob_max = g.dense_groups ? dense_blob_bytes(g, chunk) : 0;
+        for (int grp = g.dense_groups; grp < g.groups; ++grp) {
             const int64_t *pre = &gpre[(size_t)grp * (C + 1)];
             for (int k = 0; k < nch; ++k) {
                 const int c0 = k * chunk, c1 = std::min(C, c0 + chunk);
@@ -214,6 +254,7 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
         if (total <= kSmemBudget || (chunk == 1 && total <= 200 * 1024)) {
             g.chunk = chunk;
             g.num_chunks = nch;
+            g.dense_mask_words = (int)round_up((size_t)g.warps * chunk, 4);
             g.in_stage_bytes = in_stage;
             g.blob_stage_bytes = round_up(blob_max, 128);
             return SPCONV_OK;
@@ -262,19 +303,44 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
         for (int k = 0; k < nch; ++k) {
             const int c0 = k * g.chunk, c1 = std::min(g.C, c0 + g.chunk);
             P.blob_off[(size_t)grp * nch + k] = (uint32_t)(total / 16);
-            total += (size_t)g.hdr_words * 4 + round_up((size_t)(pre[c1] - pre[c0]) * 8, 16);
+            if (P.group_dense[grp])
+                total += dense_blob_bytes(g, g.chunk);
+            else
+                total += (size_t)g.hdr_words * 4 + round_up((size_t)(pre[c1] - pre[c0]) * 8, 16);
         }
     }
     P.blob_off[(size_t)g.groups * nch] = (uint32_t)(total / 16);
     if (total / 16 >= ((size_t)1 << 32)) return SPCONV_ERR_UNSUPPORTED;
     P.blobs.assign(total, 0);
+    const int kk4 = (int)round_up((size_t)RS, 4);
     std::vector<size_t> cursor(g.num_slots, 0);  // next sorted entry of each slot
     for (int grp = 0; grp < g.groups; ++grp) {
         for (int k = 0; k < nch; ++k) {
             unsigned char *blob = P.blobs.data() + (size_t)P.blob_off[(size_t)grp * nch + k] * 16;
+            const int c_end = std::min(g.C, (k + 1) * g.chunk);
+            if (P.group_dense[grp]) {
+                // [warp][channel] slot masks, then [warp][channel][slot][R*S (to 4)] weights
+                uint32_t *mask = reinterpret_cast<uint32_t *>(blob);
+                float *wts = reinterpret_cast<float *>(blob + (size_t)g.dense_mask_words * 4);
+                for (int w = 0; w < g.warps; ++w)
+                    for (int q = 0; q < g.slots; ++q) {
+                        const int slot = (grp * g.warps + w) * g.slots + q;
+                        const std::vector<int64_t> &idx = order[slot];
+                        size_t &t = cursor[slot];
+                        for (; t < idx.size(); ++t) {
+                            const int col = colidx[idx[t]];
+                            const int c = col / RS;
+                            if (c >= c_end) break;
+                            const int cl = c - k * g.chunk;
+                            mask[w * g.chunk + cl] |= 1u << q;
+                            wts[((size_t)(w * g.chunk + cl) * g.slots + q) * kk4 + col % RS] =
+                                value[idx[t]];
+                        }
+                    }
+                continue;
+            }
             uint32_t *hdr = reinterpret_cast<uint32_t *>(blob);
             HostEntry *ent = reinterpret_cast<HostEntry *>(blob + (size_t)g.hdr_words * 4);
-            const int c_end = std::min(g.C, (k + 1) * g.chunk);
             uint32_t e = 0;
             for (int ls = 0; ls < slots_per_group; ++ls) {
                 const int slot = grp * slots_per_group + ls;
@@ -334,8 +400,9 @@ int upload(spconv_packed *P, cudaStream_t stream) {
     const size_t b_blobs = round_up(std::max<size_t>(P->blobs.size(), 16), 256);
     const size_t b_off = round_up(P->blob_off.size() * sizeof(uint32_t), 256);
     const size_t b_slot = round_up(P->slot_oc.size() * sizeof(int32_t), 256);
+    const size_t b_gd = round_up(P->group_dense.size() * sizeof(int32_t), 256);
     const size_t b_err = 256;
-    P->dev_bytes = b_blobs + b_off + b_slot + b_err;
+    P->dev_bytes = b_blobs + b_off + b_slot + b_gd + b_err;
     void *blk = nullptr;
     if (cudaMalloc(&blk, P->dev_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -353,6 +420,9 @@ int upload(spconv_packed *P, cudaStream_t stream) {
     ok = ok && cudaMemcpyAsync(base + b_blobs + b_off, P->slot_oc.data(),
                                P->slot_oc.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
                                stream) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(base + b_blobs + b_off + b_slot, P->group_dense.data(),
+                               P->group_dense.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                               stream) == cudaSuccess;
     ok = ok && cudaStreamSynchronize(stream) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
@@ -361,7 +431,8 @@ int upload(spconv_packed *P, cudaStream_t stream) {
     P->d.blobs = reinterpret_cast<const unsigned char *>(base);
     P->d.blob_off = reinterpret_cast<const uint32_t *>(base + b_blobs);
     P->d.slot_oc = reinterpret_cast<const int *>(base + b_blobs + b_off);
-    P->d.err = reinterpret_cast<unsigned int *>(base + b_blobs + b_off + b_slot);
+    P->d.group_dense = reinterpret_cast<const int *>(base + b_blobs + b_off + b_slot);
+    P->d.err = reinterpret_cast<unsigned int *>(base + b_blobs + b_off + b_slot + b_gd);
     return SPCONV_OK;
 }
 
@@ -580,6 +651,8 @@ __attribute__((visibility("default"))) int spconv_packed_info_get(const spconv_p
     info->hdr_words = g.hdr_words;
     info->blob_stage_bytes = (int32_t)g.blob_stage_bytes;
     info->in_stage_bytes = (int32_t)g.in_stage_bytes;
+    info->dense_groups = g.dense_groups;
+    info->dense_mask_words = g.dense_mask_words;
     return SPCONV_OK;
 }
 

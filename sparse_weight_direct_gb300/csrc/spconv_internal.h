@@ -77,7 +77,9 @@ struct Geometry {
     int warps;        // warps per block
     int groups;       // output-channel groups (grid y)
     int num_slots;    // groups * warps * slots
-    int hdr_words;    // words of a weight blob header (warps * slots + 1, to 4)
+    int hdr_words;    // words of a sparse blob header (warps * slots + 1, to 4)
+    int dense_groups; // leading groups whose blobs are dense-tap (0 if none)
+    int dense_mask_words;  // words of a dense blob's slot masks (warps * chunk, to 4)
     size_t in_stage_bytes;    // staged input of one chunk, rounded to 128 B
     size_t blob_stage_bytes;  // largest weight blob, rounded to 128 B
 };
@@ -86,12 +88,17 @@ struct DeviceArrays {
     const unsigned char *blobs;  // weight blobs, each 16-byte aligned
     const uint32_t *blob_off;    // [groups * num_chunks + 1] in 16-byte units
     const int *slot_oc;          // [num_slots]
+    const int *group_dense;      // [groups]: 1 = dense-tap blob, 0 = sparse entries
     unsigned int *err;           // device error flags (bit 0: pipeline wait timed out)
 };
 
 // Kernel variants compiled for sm_103a.  Returns 0 if (S, stride, P, Q, LR)
 // has an instance, else -1.
 int forward_variant_supported(int S, int stride, int P, int Q, int LR);
+
+// Whether a layer shape can use the dense-tap path (output channels with dense
+// rows get their K x K blocks applied from a register window).
+bool dense_taps_supported(int R, int S, int stride, int LR);
 
 // Dynamic shared memory a launch needs with `split` blocks per cluster.
 size_t forward_smem_bytes(const Geometry &g, int split);

@@ -59,10 +59,32 @@ def decode_layout(w):
     assert boff.size == G * nch + 1 and boff[-1] == blobs.size
     assert np.all(boff % 16 == 0) and np.all(np.diff(boff) >= hw * 4)
     rows = {}
+    RS = R * info["S"]
+    kk4 = (RS + 3) // 4 * 4
+    Q, NW, chunk = info["slots_per_warp"], info["warps"], info["chunk"]
     for g in range(G):
         for k in range(nch):
             blob = blobs[boff[g * nch + k]:boff[g * nch + k + 1]]
             assert blob.size <= info["blob_stage_bytes"]
+            if g < info["dense_groups"]:
+                mw = info["dense_mask_words"]
+                mask = blob[:mw * 4].view(np.uint32)[:NW * chunk].reshape(NW, chunk)
+                wts = blob[mw * 4:].view(np.float32).reshape(NW, chunk, Q, kk4)
+                assert np.all(wts[..., RS:] == 0)
+                for w in range(NW):
+                    for q in range(Q):
+                        m = int(slot_oc[(g * NW + w) * Q + q])
+                        for cl in range(chunk):
+                            blk = wts[w, cl, q, :RS]
+                            present = bool(mask[w, cl] >> q & 1)
+                            if m < 0 or not present:
+                                assert not blk.any()
+                                continue
+                            c = k * chunk + cl
+                            assert c < info["C"]
+                            for t in np.nonzero(blk)[0]:
+                                rows.setdefault(m, []).append((c * RS + int(t), float(blk[t])))
+                continue
             hdr = blob[:hw * 4].view(np.uint32)
             ent = blob[hw * 4:].view([("value", "<f4"), ("off", "<i4")])
             assert hdr[0] == 0 and np.all(np.diff(hdr[:spg + 1].astype(np.int64)) >= 0)
@@ -108,8 +130,10 @@ def test_packed_layout_decodes_to_csr(name):
     assert sorted(used.tolist()) == list(range(L.M))
     for m in range(L.M):
         lo, hi = rowptr[m], rowptr[m + 1]
-        want = sorted(zip(colidx[lo:hi].tolist(), value[lo:hi].astype(np.float64).tolist()))
-        assert rows.get(m, []) == want
+        want = sorted((c, v) for c, v in zip(colidx[lo:hi].tolist(),
+                                              value[lo:hi].astype(np.float64).tolist()) if v != 0)
+        got = [(c, v) for c, v in rows.get(m, []) if v != 0]
+        assert got == want
     # staged input tile covers every tap of every output of a tile
     tile_h = info["tile_rows"] * info["lane_rows"]
     assert info["tile_cols"] * info["lane_rows"] == 32
