@@ -171,7 +171,12 @@ typedef enum spconv_array {
                                /* then floats [warp][chan][slot][R*S rounded to 4] */
     SPCONV_ARRAY_BLOB_OFF = 1, /* uint32 [groups * num_chunks + 1]: blob starts in  */
                                /* 16-byte units                                     */
-    SPCONV_ARRAY_SLOT_OC = 2   /* int32 [num_slots]: output channel of a slot or -1 */
+    SPCONV_ARRAY_SLOT_OC = 2,  /* int32 [num_slots]: output channel of a head slot,  */
+                               /* -1 for empty slots and later parts of split rows */
+    SPCONV_ARRAY_SLOT_NEXT = 3,/* int32 [num_slots]: group-local slot of the next   */
+                               /* part of the same output channel, or -1            */
+    SPCONV_ARRAY_GROUP_FLAGS = 4 /* int32 [groups]: bit 0 dense-tap blobs, bit 1    */
+                               /* the group has split rows                          */
 } spconv_array;
 
 /* Copies one packed array into dst (host, dst_bytes long).  *needed (if not

@@ -55,8 +55,8 @@ class PackedWeights:
 
     def array(self, which: str) -> np.ndarray:
         """Copy of a packed host array: 'blobs' (raw bytes), 'blob_off'
-        (uint32, 16-byte units) or 'slot_oc' (int32)."""
-        code = {"blobs": 0, "blob_off": 1, "slot_oc": 2}[which]
+        (uint32, 16-byte units), 'slot_oc', 'slot_next' or 'group_flags' (int32)."""
+        code = {"blobs": 0, "blob_off": 1, "slot_oc": 2, "slot_next": 3, "group_flags": 4}[which]
         need = ctypes.c_int64(0)
         L = _lib.lib()
         _lib.check(L.spconv_packed_copy_array(self.handle, code, None, 0, ctypes.byref(need)),

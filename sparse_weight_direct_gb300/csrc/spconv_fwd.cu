@@ -51,8 +51,9 @@ struct KParams {
     float *y;
     const unsigned char *blobs;
     const uint32_t *blob_off;
-    const int *slot_oc;
-    const int *group_dense;  // per group: 1 = dense-tap blobs, 0 = sparse entries
+    const int *slot_oc;      // head slot -> output channel; -1 empty or a later part
+    const int *slot_next;    // next part of the same output channel (group-local), -1
+    const int *group_flags;  // per group: bit 0 dense-tap blobs, bit 1 split rows
     unsigned int *err;
     int N, C, H, W, M, E, F, stride, pad;
     int tiles_y, tiles_x, in_rows, in_cols, shift, phase_pitch, row_pitch, plane;
@@ -291,7 +292,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int ty = b % p.tiles_y;
     const int n = b / p.tiles_y;
     const int group = blockIdx.y;
-    const bool dense = p.group_dense[group] != 0;
+    const int gflags = p.group_flags[group];
+    const bool dense = (gflags & 1) != 0;
+    const bool has_parts = (gflags & 2) != 0;
     const int k_begin = kr * p.num_chunks / split;
     const int k_end = (kr + 1) * p.num_chunks / split;
     const int iy0 = ty * (LR * P) * st - p.pad;
@@ -375,10 +378,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (threadIdx.x == 0) atomicOr(p.err, 1u);
     }
 
-    const int slot0 = (group * kWarps + warp) * Q;
+    const int nslot = kWarps * Q;
+    const int slot0 = group * nslot + warp * Q;
     const int ox = tx * LC + lx;
     const int oy0 = ty * (LR * P) + ly;  // this lane's output rows: oy0 + LR * r
-    if (split == 1) {
+    if (split == 1 && !has_parts) {
         if (failed || ox >= p.F) return;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
@@ -394,16 +398,36 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         return;
     }
 
-    // ---- cluster reduction of the channel split through distributed smem
-    cg::cluster_group cluster = cg::this_cluster();
+    // ---- partial sums through shared memory: parts of split rows (summed in
+    // chain order) and/or the blocks of a channel-split cluster (summed in rank
+    // order, through distributed shared memory).  Both orders are fixed, so the
+    // result is deterministic.  The stage buffers are free: every issued copy
+    // has been consumed.
     float *part = reinterpret_cast<float *>(smem);  // [warp * Q + q][P][32]
-    // every block of the cluster has left its pipeline before partials land
 #pragma unroll
     for (int q = 0; q < Q; ++q)
 #pragma unroll
         for (int r = 0; r < P; ++r) part[((warp * Q + q) * P + r) * 32 + lane] = acc[q][r];
+    if (split == 1) {
+        __syncthreads();
+        if (failed || ox >= p.F) return;
+        for (int q = 0; q < Q; ++q) {
+            const int sl = warp * Q + q;
+            const int m = p.slot_oc[group * nslot + sl];
+            if (m < 0) continue;
+            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
+            for (int r = 0; r < P; ++r) {
+                float sum = 0.f;
+                for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c])
+                    sum += part[(c * P + r) * 32 + lane];
+                const int oy = oy0 + LR * r;
+                if (oy < p.E) yo[(size_t)oy * p.F] = sum;
+            }
+        }
+        return;
+    }
+    cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
-    const int nslot = kWarps * Q;
     const int s_begin = kr * nslot / split, s_end = (kr + 1) * nslot / split;
     if (!failed && ox < p.F) {
         for (int sl = s_begin + warp; sl < s_end; sl += kWarps) {
@@ -411,12 +435,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             if (m < 0) continue;
             float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
             for (int r = 0; r < P; ++r) {
-                const int oy = oy0 + LR * r;
                 float sum = 0.f;
-                for (int j = 0; j < split; ++j) {
-                    const float *rp = cluster.map_shared_rank(part, j);
-                    sum += rp[(sl * P + r) * 32 + lane];
-                }
+                for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c])
+                    for (int j = 0; j < split; ++j) {
+                        const float *rp = cluster.map_shared_rank(part, j);
+                        sum += rp[(c * P + r) * 32 + lane];
+                    }
+                const int oy = oy0 + LR * r;
                 if (oy < p.E) yo[(size_t)oy * p.F] = sum;
             }
         }
@@ -495,10 +520,9 @@ int forward_variant_supported(int S, int stride, int P, int Q, int LR) {
 size_t forward_smem_bytes(const Geometry &g, int split) {
     const int per_block = (g.num_chunks + split - 1) / split;
     size_t bytes = (size_t)(per_block > 1 ? 2 : 1) * stage_bytes(g);
-    if (split > 1) {
-        const size_t part = (size_t)g.warps * g.slots * g.tile_rows * 32 * sizeof(float);
-        if (part > bytes) bytes = part;
-    }
+    // room for the partial sums of split rows / a channel-split cluster
+    const size_t part = (size_t)g.warps * g.slots * g.tile_rows * 32 * sizeof(float);
+    if (part > bytes) bytes = part;
     return bytes + 128;  // room to align the stage buffers to 128 bytes
 }
 
@@ -518,7 +542,8 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, const float *x, 
     p.blobs = d.blobs;
     p.blob_off = d.blob_off;
     p.slot_oc = d.slot_oc;
-    p.group_dense = d.group_dense;
+    p.slot_next = d.slot_next;
+    p.group_flags = d.group_flags;
     p.err = d.err;
     p.N = N; p.C = g.C; p.H = g.H; p.W = g.W; p.M = g.M; p.E = g.E; p.F = g.F;
     p.stride = g.stride; p.pad = g.pad;

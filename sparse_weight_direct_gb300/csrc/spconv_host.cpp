@@ -47,8 +47,10 @@ struct spconv_packed {
     int64_t max_warp_nnz = 0, mean_warp_nnz = 0;
     std::vector<unsigned char> blobs;  // concatenated (group, chunk) blobs
     std::vector<uint32_t> blob_off;    // [groups * num_chunks + 1], 16-byte units
-    std::vector<int32_t> slot_oc;      // [num_slots]
-    std::vector<int32_t> group_dense;  // [groups]
+    std::vector<int32_t> slot_oc;      // [num_slots]: head slot -> output channel, else -1
+    std::vector<int32_t> slot_next;    // [num_slots]: next part (group-local slot) or -1
+    std::vector<int32_t> group_flags;  // [groups]: bit 0 dense, bit 1 split rows
+    std::vector<std::vector<int64_t>> slot_entries;  // CSR indices per slot, column order
     int device = -1;
     void *dev_block = nullptr;
     size_t dev_bytes = 0;
@@ -66,6 +68,7 @@ constexpr int kSMs = 152;                   // GB300 SM count, for the grid heur
 // it issues K*K FMAs per (slot, channel) block with zeros included, about four
 // times cheaper per FMA than a shared-memory load per FMA.
 constexpr double kDenseRowMin = 0.30;
+constexpr int64_t kMinPart = 32;  // smallest part a split row is cut into
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -156,20 +159,23 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
 }
 
 // Output channels whose rows are dense enough go to leading "dense" groups
-// (densest first, dealt round-robin over the warps); the rest are binned onto
-// the warps of the sparse groups longest row first onto the least-loaded warp
-// that has a free slot.  Sets groups / num_slots / slot_oc / group_dense.
-void bin_channels(spconv_packed &P, const int32_t *rowptr) {
+// (densest first, dealt round-robin over the warps).  The rest are sparse:
+// they are spread over the sparse groups longest row first onto the group with
+// the least work that has room; a row heavier than 1.5x a warp's fair share
+// is split into parts (its column-ordered nonzeros dealt round-robin, so every
+// part spans all chunks), and inside each group the parts are bound to warp
+// slots longest first onto the least-loaded warp with a free slot.  The parts
+// of one row stay in one group and are summed in the epilogue.  Sets groups,
+// num_slots, slot_oc, slot_next, group_flags and the per-slot entry lists.
+int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx) {
     spconv::Geometry &g = P.g;
     const int per_group = g.warps * g.slots;
     const double crs = (double)g.C * g.R * g.S;
+    auto nnz_of = [&](int m) { return (int64_t)rowptr[m + 1] - rowptr[m]; };
     std::vector<int> dense, sparse;
     const bool can_dense = spconv::dense_taps_supported(g.R, g.S, g.stride, g.lane_rows);
-    for (int m = 0; m < g.M; ++m) {
-        const double d = (rowptr[m + 1] - rowptr[m]) / crs;
-        (can_dense && d >= kDenseRowMin ? dense : sparse).push_back(m);
-    }
-    auto nnz_of = [&](int m) { return (int64_t)rowptr[m + 1] - rowptr[m]; };
+    for (int m = 0; m < g.M; ++m)
+        (can_dense && nnz_of(m) / crs >= kDenseRowMin ? dense : sparse).push_back(m);
     std::stable_sort(dense.begin(), dense.end(), [&](int a, int b) { return nnz_of(a) > nnz_of(b); });
     // a dense group less than half full is not worth a group of its own
     const int tail = (int)dense.size() % per_group;
@@ -179,42 +185,122 @@ void bin_channels(spconv_packed &P, const int32_t *rowptr) {
     }
     std::stable_sort(sparse.begin(), sparse.end(), [&](int a, int b) { return nnz_of(a) > nnz_of(b); });
     const int gd = ((int)dense.size() + per_group - 1) / per_group;
-    const int gs = ((int)sparse.size() + per_group - 1) / per_group;
+
+    // parts per sparse row: rows above the mean warp load are split
+    int gs = std::max(((int)sparse.size() + per_group - 1) / per_group, sparse.empty() ? 0 : 1);
+    int64_t total = 0;
+    for (int m : sparse) total += nnz_of(m);
+    std::vector<int> parts(g.M, 1);
+    for (int iter = 0; iter < 4 && gs > 0; ++iter) {
+        const int64_t cap = std::max<int64_t>(1, (total + (int64_t)gs * g.warps - 1) / ((int64_t)gs * g.warps));
+        int64_t nparts = 0;
+        for (int m : sparse) {
+            // only rows well above the fair share are worth the extra slots
+            // (and only into parts of at least kMinPart entries)
+            parts[m] = nnz_of(m) * 2 > cap * 3
+                           ? (int)std::min<int64_t>({(nnz_of(m) + cap - 1) / cap, g.warps,
+                                                     std::max<int64_t>(1, nnz_of(m) / kMinPart)})
+                           : 1;
+            nparts += parts[m];
+        }
+        // with split rows keep ~10 % of the slots free so the group-level
+        // balancing is not forced by capacity
+        const int64_t want = nparts > (int64_t)sparse.size() ? nparts + nparts / 10 : nparts;
+        const int need = (int)((want + per_group - 1) / per_group);
+        if (need <= gs) break;
+        gs = need;
+    }
     g.dense_groups = gd;
     g.groups = std::max(1, gd + gs);
+    if (g.groups > 65535) return SPCONV_ERR_UNSUPPORTED;
     g.num_slots = g.groups * per_group;
     P.slot_oc.assign(g.num_slots, -1);
-    P.group_dense.assign(g.groups, 0);
-    for (int grp = 0; grp < gd; ++grp) P.group_dense[grp] = 1;
-    // dense: the i-th densest channel goes to warp i % warps_total, slot i / warps_total
+    P.slot_next.assign(g.num_slots, -1);
+    P.group_flags.assign(g.groups, 0);
+    P.slot_entries.assign(g.num_slots, {});
+    auto sorted_entries = [&](int m) {
+        std::vector<int64_t> idx(nnz_of(m));
+        std::iota(idx.begin(), idx.end(), (int64_t)rowptr[m]);
+        std::sort(idx.begin(), idx.end(), [&](int64_t a, int64_t b) { return colidx[a] < colidx[b]; });
+        return idx;
+    };
+
+    // dense groups: the i-th densest channel goes to warp i % warps_total, slot i / warps_total
+    for (int grp = 0; grp < gd; ++grp) P.group_flags[grp] = 1;
     const int dwarps = gd * g.warps;
     for (size_t i = 0; i < dense.size(); ++i) {
-        const int w = (int)(i % dwarps), q = (int)(i / dwarps);
-        P.slot_oc[(size_t)w * g.slots + q] = dense[i];
+        const int slot = (int)(i % dwarps) * g.slots + (int)(i / dwarps);
+        P.slot_oc[slot] = dense[i];
+        P.slot_entries[slot] = sorted_entries(dense[i]);
     }
-    // sparse: LPT over the warps of the sparse groups
-    const int nwarps = gs * g.warps, w0 = gd * g.warps;
-    using Item = std::pair<int64_t, int>;  // (load, warp)
-    std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
-    for (int w = 0; w < nwarps; ++w) heap.push({0, w});
-    std::vector<int> fill(nwarps, 0);
-    std::vector<int64_t> load(nwarps, 0);
+
+    // sparse rows onto groups (least load with room for the row's parts)
+    std::vector<std::vector<int>> members(gs);
+    std::vector<int64_t> gload(gs, 0);
+    std::vector<int> gfree(gs, per_group);
     for (int m : sparse) {
-        const Item it = heap.top();
-        heap.pop();
-        const int w = it.second;
-        P.slot_oc[(size_t)(w0 + w) * g.slots + fill[w]] = m;
-        ++fill[w];
-        load[w] += nnz_of(m);
-        if (fill[w] < g.slots) heap.push({load[w], w});
+        int best = -1;
+        for (int q = 0; q < gs; ++q)
+            if (gfree[q] >= parts[m] && (best < 0 || gload[q] < gload[best])) best = q;
+        if (best < 0) {  // no group has room for all parts: use the roomiest
+            best = 0;
+            for (int q = 1; q < gs; ++q)
+                if (gfree[q] > gfree[best]) best = q;
+            parts[m] = std::max(1, gfree[best]);
+        }
+        members[best].push_back(m);
+        gload[best] += nnz_of(m);
+        gfree[best] -= parts[m];
     }
+    // inside each group: parts onto warps, longest first onto the least-loaded
     int64_t mx = 0, sum = 0, used = 0;
-    for (int w = 0; w < nwarps; ++w) {
-        mx = std::max(mx, load[w]);
-        if (fill[w]) { sum += load[w]; ++used; }
+    for (int q = 0; q < gs; ++q) {
+        const int grp = gd + q;
+        struct Part { int m, k, n; int64_t load; };
+        std::vector<Part> plist;
+        for (int m : members[q])
+            for (int k = 0; k < parts[m]; ++k)
+                plist.push_back({m, k, parts[m], (nnz_of(m) - k + parts[m] - 1) / parts[m]});
+        std::stable_sort(plist.begin(), plist.end(),
+                         [](const Part &a, const Part &b) { return a.load > b.load; });
+        using Item = std::pair<int64_t, int>;  // (load, warp)
+        std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
+        for (int w = 0; w < g.warps; ++w) heap.push({0, w});
+        std::vector<int> fill(g.warps, 0);
+        std::vector<int64_t> load(g.warps, 0);
+        std::vector<std::vector<int>> part_slot(g.M);
+        for (const Part &pt : plist) {
+            if (heap.empty()) return SPCONV_ERR_UNSUPPORTED;  // cannot happen: sized above
+            const Item it = heap.top();
+            heap.pop();
+            const int w = it.second;
+            const int local = w * g.slots + fill[w];
+            ++fill[w];
+            load[w] += pt.load;
+            if (fill[w] < g.slots) heap.push({load[w], w});
+            if (part_slot[pt.m].empty()) part_slot[pt.m].assign(pt.n, -1);
+            part_slot[pt.m][pt.k] = local;
+        }
+        for (int m : members[q]) {
+            const std::vector<int> &ps = part_slot[m];
+            const std::vector<int64_t> idx = sorted_entries(m);
+            for (size_t k = 0; k < ps.size(); ++k) {
+                const int slot = grp * per_group + ps[k];
+                if (k == 0) P.slot_oc[slot] = m;
+                if (k + 1 < ps.size()) P.slot_next[slot] = ps[k + 1];
+                std::vector<int64_t> &mine = P.slot_entries[slot];
+                for (size_t t = k; t < idx.size(); t += ps.size()) mine.push_back(idx[t]);
+            }
+            if (ps.size() > 1) P.group_flags[grp] |= 2;
+        }
+        for (int w = 0; w < g.warps; ++w) {
+            mx = std::max(mx, load[w]);
+            if (fill[w]) { sum += load[w]; ++used; }
+        }
     }
     P.max_warp_nnz = mx;
     P.mean_warp_nnz = used ? sum / used : 0;
+    return SPCONV_OK;
 }
 
 size_t dense_blob_bytes(const spconv::Geometry &g, int chunk) {
@@ -268,24 +354,23 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
                  const float *value) {
     spconv::Geometry &g = P.g;
     const int RS = g.R * g.S;
-    bin_channels(P, rowptr);
-
-    // per-slot entries sorted by column ((c, r, s) order); duplicates rejected
-    std::vector<std::vector<int64_t>> order(g.num_slots);
+    // duplicate columns are rejected before anything else
+    {
+        std::vector<int32_t> cols;
+        for (int m = 0; m < g.M; ++m) {
+            cols.assign(colidx + rowptr[m], colidx + rowptr[m + 1]);
+            std::sort(cols.begin(), cols.end());
+            if (std::adjacent_find(cols.begin(), cols.end()) != cols.end()) return SPCONV_ERR_BAD_CSR;
+        }
+    }
+    int bst = bin_channels(P, rowptr, colidx);
+    if (bst) return bst;
+    const std::vector<std::vector<int64_t>> &order = P.slot_entries;
     std::vector<int64_t> gpre((size_t)g.groups * (g.C + 1), 0);
     const int slots_per_group = g.warps * g.slots;
     for (int slot = 0; slot < g.num_slots; ++slot) {
-        const int m = P.slot_oc[slot];
-        if (m < 0) continue;
-        std::vector<int64_t> &idx = order[slot];
-        idx.resize(rowptr[m + 1] - rowptr[m]);
-        std::iota(idx.begin(), idx.end(), (int64_t)rowptr[m]);
-        std::sort(idx.begin(), idx.end(),
-                  [&](int64_t a, int64_t b) { return colidx[a] < colidx[b]; });
-        for (size_t t = 1; t < idx.size(); ++t)
-            if (colidx[idx[t]] == colidx[idx[t - 1]]) return SPCONV_ERR_BAD_CSR;
         int64_t *pre = &gpre[(size_t)(slot / slots_per_group) * (g.C + 1)];
-        for (int64_t j : idx) pre[colidx[j] / RS + 1] += 1;
+        for (int64_t j : order[slot]) pre[colidx[j] / RS + 1] += 1;
     }
     for (int grp = 0; grp < g.groups; ++grp) {
         int64_t *pre = &gpre[(size_t)grp * (g.C + 1)];
@@ -303,7 +388,7 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
         for (int k = 0; k < nch; ++k) {
             const int c0 = k * g.chunk, c1 = std::min(g.C, c0 + g.chunk);
             P.blob_off[(size_t)grp * nch + k] = (uint32_t)(total / 16);
-            if (P.group_dense[grp])
+            if (P.group_flags[grp] & 1)
                 total += dense_blob_bytes(g, g.chunk);
             else
                 total += (size_t)g.hdr_words * 4 + round_up((size_t)(pre[c1] - pre[c0]) * 8, 16);
@@ -318,7 +403,7 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
         for (int k = 0; k < nch; ++k) {
             unsigned char *blob = P.blobs.data() + (size_t)P.blob_off[(size_t)grp * nch + k] * 16;
             const int c_end = std::min(g.C, (k + 1) * g.chunk);
-            if (P.group_dense[grp]) {
+            if (P.group_flags[grp] & 1) {
                 // [warp][channel] slot masks, then [warp][channel][slot][R*S (to 4)] weights
                 uint32_t *mask = reinterpret_cast<uint32_t *>(blob);
                 float *wts = reinterpret_cast<float *>(blob + (size_t)g.dense_mask_words * 4);
@@ -369,6 +454,8 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
     }
     for (int slot = 0; slot < g.num_slots; ++slot)
         if (cursor[slot] != order[slot].size()) return SPCONV_ERR_BAD_CSR;
+    P.slot_entries.clear();
+    P.slot_entries.shrink_to_fit();
     return SPCONV_OK;
 }
 
@@ -400,9 +487,10 @@ int upload(spconv_packed *P, cudaStream_t stream) {
     const size_t b_blobs = round_up(std::max<size_t>(P->blobs.size(), 16), 256);
     const size_t b_off = round_up(P->blob_off.size() * sizeof(uint32_t), 256);
     const size_t b_slot = round_up(P->slot_oc.size() * sizeof(int32_t), 256);
-    const size_t b_gd = round_up(P->group_dense.size() * sizeof(int32_t), 256);
+    const size_t b_next = round_up(P->slot_next.size() * sizeof(int32_t), 256);
+    const size_t b_gd = round_up(P->group_flags.size() * sizeof(int32_t), 256);
     const size_t b_err = 256;
-    P->dev_bytes = b_blobs + b_off + b_slot + b_gd + b_err;
+    P->dev_bytes = b_blobs + b_off + b_slot + b_next + b_gd + b_err;
     void *blk = nullptr;
     if (cudaMalloc(&blk, P->dev_bytes) != cudaSuccess) {
         cudaGetLastError();
@@ -420,8 +508,11 @@ int upload(spconv_packed *P, cudaStream_t stream) {
     ok = ok && cudaMemcpyAsync(base + b_blobs + b_off, P->slot_oc.data(),
                                P->slot_oc.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
                                stream) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(base + b_blobs + b_off + b_slot, P->group_dense.data(),
-                               P->group_dense.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+    ok = ok && cudaMemcpyAsync(base + b_blobs + b_off + b_slot, P->slot_next.data(),
+                               P->slot_next.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                               stream) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(base + b_blobs + b_off + b_slot + b_next, P->group_flags.data(),
+                               P->group_flags.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
                                stream) == cudaSuccess;
     ok = ok && cudaStreamSynchronize(stream) == cudaSuccess;
     if (!ok) {
@@ -431,8 +522,9 @@ int upload(spconv_packed *P, cudaStream_t stream) {
     P->d.blobs = reinterpret_cast<const unsigned char *>(base);
     P->d.blob_off = reinterpret_cast<const uint32_t *>(base + b_blobs);
     P->d.slot_oc = reinterpret_cast<const int *>(base + b_blobs + b_off);
-    P->d.group_dense = reinterpret_cast<const int *>(base + b_blobs + b_off + b_slot);
-    P->d.err = reinterpret_cast<unsigned int *>(base + b_blobs + b_off + b_slot + b_gd);
+    P->d.slot_next = reinterpret_cast<const int *>(base + b_blobs + b_off + b_slot);
+    P->d.group_flags = reinterpret_cast<const int *>(base + b_blobs + b_off + b_slot + b_next);
+    P->d.err = reinterpret_cast<unsigned int *>(base + b_blobs + b_off + b_slot + b_next + b_gd);
     return SPCONV_OK;
 }
 
@@ -673,6 +765,14 @@ __attribute__((visibility("default"))) int spconv_packed_copy_array(
         case SPCONV_ARRAY_SLOT_OC:
             src = p->slot_oc.data();
             n = (int64_t)(p->slot_oc.size() * sizeof(int32_t));
+            break;
+        case SPCONV_ARRAY_SLOT_NEXT:
+            src = p->slot_next.data();
+            n = (int64_t)(p->slot_next.size() * sizeof(int32_t));
+            break;
+        case SPCONV_ARRAY_GROUP_FLAGS:
+            src = p->group_flags.data();
+            n = (int64_t)(p->group_flags.size() * sizeof(int32_t));
             break;
         default: return SPCONV_ERR_INVALID_ARG;
     }

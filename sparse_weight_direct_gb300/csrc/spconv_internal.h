@@ -87,8 +87,9 @@ struct Geometry {
 struct DeviceArrays {
     const unsigned char *blobs;  // weight blobs, each 16-byte aligned
     const uint32_t *blob_off;    // [groups * num_chunks + 1] in 16-byte units
-    const int *slot_oc;          // [num_slots]
-    const int *group_dense;      // [groups]: 1 = dense-tap blob, 0 = sparse entries
+    const int *slot_oc;          // [num_slots]: head slot -> output channel, else -1
+    const int *slot_next;        // [num_slots]: next part (group-local slot) or -1
+    const int *group_flags;      // [groups]: bit 0 dense-tap blobs, bit 1 split rows
     unsigned int *err;           // device error flags (bit 0: pipeline wait timed out)
 };
 

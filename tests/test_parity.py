@@ -61,7 +61,8 @@ def test_layer_full_size(name):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["resnet3x3", "vgg3x3", "sweep90", "alex11x11", "conv5x5"])
+@pytest.mark.parametrize("name", ["resnet3x3", "vgg3x3", "sweep90", "sweep95", "sweep50",
+                                  "alex11x11", "conv5x5"])
 def test_integer_variant_bit_exact(name):
     """The same shapes with integer weights in {-3..3}\\{0} and inputs in
     {0..7}: the GPU result must equal the oracle exactly."""
@@ -100,6 +101,37 @@ def test_edge_shapes(case, integer):
     got = run_gpu(x, rowptr, colidx, value, C, H, W, M, R, S, st, pad)
     ref, mag = oracle.csr(x, rowptr, colidx, value, M, R, S, st, pad)
     check(got, ref, mag, exact=integer, what=str(case))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("integer", [False, True])
+@pytest.mark.parametrize("heavy_density,every,want_flag", [(0.6, 7, 1), (0.95, 7, 1),
+                                                           (0.6, 40, 2), (0.95, 40, 2)])
+def test_heavy_rows_split_and_dense(heavy_density, every, want_flag, integer):
+    """Very heavy rows among sparse ones.  Many of them (every 7th row) form
+    dense-tap groups; a few (every 40th) are too few for a dense group and are
+    split into parts in several warps, summed in the epilogue."""
+    rng = np.random.default_rng(int(heavy_density * 100) + integer + every)
+    N, C, H, W, M, K = 2, 24, 12, 12, 96, 3
+    CRS = C * K * K
+    rows = []
+    for m in range(M):
+        d = heavy_density if m % every == 0 else 0.05
+        keep = np.nonzero(rng.random(CRS) < d)[0]
+        rows.append(keep)
+    rowptr = np.concatenate([[0], np.cumsum([r.size for r in rows])]).astype(np.int32)
+    colidx = np.concatenate(rows).astype(np.int32)
+    if integer:
+        value = rng.choice(np.array([-3, -2, -1, 1, 2, 3], np.float32), size=colidx.size)
+    else:
+        value = rng.normal(0, 0.05, size=colidx.size).astype(np.float32)
+    x = workloads.random_input((N, C, H, W), rng, integer=integer)
+    w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=K, S=K, stride=1, pad=1)
+    assert (w.array("group_flags") & want_flag).any()
+    w.close()
+    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, K, K, 1, 1)
+    ref, mag = oracle.csr(x, rowptr, colidx, value, M, K, K, 1, 1)
+    check(got, ref, mag, exact=integer, what=f"heavy {heavy_density}")
 
 
 @pytest.mark.gpu
