@@ -271,6 +271,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     spconv_fwd_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar[2];
+    __shared__ int stage_done[2];  // warps that have released a stage (TMA path)
     // stage buffers start on a 128-byte boundary (TMA destination)
     unsigned char *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     constexpr int LC = kLanes / LR;  // lanes per lane row = output columns of a tile
@@ -303,20 +304,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     if (threadIdx.x == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
+        stage_done[0] = 0;
+        stage_done[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     }
     __syncthreads();
 
-    // Enqueue chunk k into stage s: thread 0 issues the bulk copies, every
-    // thread its share of the cp.async input staging when there is no TMA.
-    auto issue = [&](int k, int s) {
+    // Enqueue chunk k into stage s.  `issuer` (one thread) arms the stage's
+    // mbarrier and issues the bulk copies; without TMA every thread also
+    // stages its share of the input with cp.async.
+    auto issue = [&](int k, int s, bool issuer) {
         unsigned char *base = smem + (size_t)s * p.stage_bytes;
-        const uint32_t o0 = p.blob_off[group * p.num_chunks + k];
-        const uint32_t o1 = p.blob_off[group * p.num_chunks + k + 1];
-        const uint32_t blob_bytes = (o1 - o0) * 16u;
         const int c0 = k * p.chunk;
-        if (threadIdx.x == 0) {
+        if (issuer) {
+            const uint32_t o0 = p.blob_off[group * p.num_chunks + k];
+            const uint32_t o1 = p.blob_off[group * p.num_chunks + k + 1];
+            const uint32_t blob_bytes = (o1 - o0) * 16u;
             asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
             mbar_expect_tx(&bar[s], blob_bytes + (p.use_tma ? (uint32_t)p.in_tma_bytes : 0u));
             bulk_load(base + p.in_stage_bytes, p.blobs + (size_t)o0 * 16u, blob_bytes, &bar[s]);
@@ -337,8 +341,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 
     const int nmine = k_end - k_begin;
     bool failed = false;
-    if (nmine > 0) issue(k_begin, 0);
-    if (nmine > 1) issue(k_begin + 1, 1);
+    if (nmine > 0) issue(k_begin, 0, threadIdx.x == 0);
+    if (nmine > 1) issue(k_begin + 1, 1, threadIdx.x == 0);
     for (int it = 0; it < nmine && !failed; ++it) {
         const int s = it & 1;
         if (!p.use_tma) {
@@ -348,7 +352,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                 cp_async_wait_all();
         }
         const bool ok = mbar_wait_bounded(&bar[s], (uint32_t)((it >> 1) & 1));
-        failed = __syncthreads_or(!ok) != 0;
+        if (p.use_tma) {
+            // warps run independently; a warp that timed out stops
+            failed = !ok;
+        } else {
+            failed = __syncthreads_or(!ok) != 0;  // cp.async data of all threads
+        }
         if (failed) break;
         const unsigned char *base = smem + (size_t)s * p.stage_bytes;
         const float *sb = reinterpret_cast<const float *>(base) + ly * st * p.row_pitch + lx;
@@ -370,12 +379,32 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                 run_segment<P, ROW_STEP>(acc[q], sb, ent, j0, j1, row_step);
             }
         }
-        __syncthreads();  // stage s is free again
-        if (it + 2 < nmine) issue(k_begin + it + 2, s);
+        if (p.use_tma) {
+            // Release stage s without a block barrier: each warp counts itself
+            // out; the warp that completes the count refills the stage (its
+            // generic-proxy reads are ordered before the async-proxy copy by
+            // the fences).  Faster warps move on to the other stage.
+            if (it + 2 < nmine) {
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence_block();
+                    const int old = atomicAdd(&stage_done[s], 1);
+                    if (old == kWarps - 1) {
+                        stage_done[s] = 0;
+                        __threadfence_block();
+                        issue(k_begin + it + 2, s, true);
+                    }
+                }
+            }
+        } else {
+            __syncthreads();  // stage s is free again
+            if (it + 2 < nmine) issue(k_begin + it + 2, s, threadIdx.x == 0);
+        }
     }
+    if (p.use_tma) __syncthreads();  // every warp is out of the pipeline
     if (failed) {
         if (!p.use_tma) cp_async_wait_all();
-        if (threadIdx.x == 0) atomicOr(p.err, 1u);
+        if (lane == 0) atomicOr(p.err, 1u);
     }
 
     const int nslot = kWarps * Q;
