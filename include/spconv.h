@@ -124,6 +124,18 @@ int spconv_pack_host(int C, int H, int W, int M, int R, int S, int stride, int p
  */
 int spconv_device_status(const spconv_packed *p, void *stream, int32_t *flags);
 
+/*
+ * spconv_selftest_wait -- exercises, on the current device, the bounded wait
+ * the forward kernel uses for its copy pipeline: a one-warp kernel waits on a
+ * shared-memory barrier with a 20 ms limit.  complete = 0 leaves the barrier
+ * incomplete, so the wait runs out, the kernel records the timeout and
+ * returns (the context stays usable); complete != 0 completes it first.
+ * Synchronises `stream`.  *flags receives bit 0 (timed out) / bit 1
+ * (completed).  Returns SPCONV_ERR_DEVICE when the wait timed out, SPCONV_OK
+ * when it completed; INVALID_ARG (flags NULL), ALLOC, CUDA.
+ */
+int spconv_selftest_wait(int complete, void *stream, int32_t *flags);
+
 /* Geometry and sizes of a packed handle (all counts are plain integers). */
 typedef struct spconv_packed_info {
     int32_t C, H, W, M, R, S, stride, pad, E, F;

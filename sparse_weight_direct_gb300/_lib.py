@@ -24,8 +24,8 @@ SPCONV_ERR_DEVICE = -7
 
 # Every symbol include/spconv.h declares.
 EXPORTS = ("spconv_pack", "spconv_forward", "spconv_packed_free", "spconv_status_string",
-           "spconv_pack_host", "spconv_device_status", "spconv_packed_info_get",
-           "spconv_packed_copy_array")
+           "spconv_pack_host", "spconv_device_status", "spconv_selftest_wait",
+           "spconv_packed_info_get", "spconv_packed_copy_array")
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.spconv_packed_copy_array.restype = i
         L.spconv_device_status.argtypes = [p, p, ctypes.POINTER(ctypes.c_int32)]
         L.spconv_device_status.restype = i
+        L.spconv_selftest_wait.argtypes = [i, p, ctypes.POINTER(ctypes.c_int32)]
+        L.spconv_selftest_wait.restype = i
         _lib = L
         return L
 

@@ -98,12 +98,13 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Waits for the stage's phase with a time limit; false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+        if ((i & 63) == 0 && global_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -478,6 +479,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     cluster.sync();  // partials stay readable until every block is done
 }
 
+// Exercises the bounded pipeline wait: one warp waits on an mbarrier whose
+// phase nothing completes (armed for one arrival that never comes), with a
+// short limit; the wait gives up, the kernel records bit 0 in `flags` and
+// returns.  A second launch mode arrives first, so the wait succeeds.
+__global__ void wait_selftest_kernel(unsigned int *flags, unsigned long long limit_ns,
+                                     int arrive) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) mbar_init(&bar, 1);
+    __syncwarp();
+    if (arrive && threadIdx.x == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&bar)) : "memory");
+    __syncwarp();
+    const bool ok = mbar_wait_bounded(&bar, 0u, limit_ns);
+    if (!ok && threadIdx.x == 0) atomicOr(flags, 1u);
+    if (ok && threadIdx.x == 0) atomicOr(flags, 2u);
+}
+
 using KernelFn = void (*)(const KParams, const CUtensorMap);
 
 template <int P, int Q>
@@ -537,6 +555,11 @@ cudaError_t raise_smem_limit(KernelFn fn) {
 }
 
 }  // namespace
+
+cudaError_t launch_wait_selftest(unsigned int *flags, int arrive, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(flags, 20000000ull /* 20 ms */, arrive);
+    return cudaGetLastError();
+}
 
 bool dense_taps_supported(int R, int S, int stride, int LR) {
     return stride == 1 && R == S && (S == 3 || (S == 5 && LR == 1));

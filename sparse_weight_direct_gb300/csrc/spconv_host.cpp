@@ -682,6 +682,29 @@ __attribute__((visibility("default"))) int spconv_device_status(const spconv_pac
     return word ? SPCONV_ERR_DEVICE : SPCONV_OK;
 }
 
+__attribute__((visibility("default"))) int spconv_selftest_wait(int complete, void *stream,
+                                                                int32_t *flags) {
+    if (!flags) return SPCONV_ERR_INVALID_ARG;
+    unsigned int *d = nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMalloc(&d, sizeof(unsigned int)) != cudaSuccess) {
+        cudaGetLastError();
+        return SPCONV_ERR_ALLOC;
+    }
+    unsigned int word = 0;
+    bool ok = cudaMemsetAsync(d, 0, sizeof(unsigned int), s) == cudaSuccess &&
+              spconv::launch_wait_selftest(d, complete ? 1 : 0, s) == cudaSuccess &&
+              cudaMemcpyAsync(&word, d, sizeof(word), cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+              cudaStreamSynchronize(s) == cudaSuccess;
+    cudaFree(d);
+    if (!ok) {
+        cudaGetLastError();
+        return SPCONV_ERR_CUDA;
+    }
+    *flags = (int32_t)word;
+    return (word & 1u) ? SPCONV_ERR_DEVICE : SPCONV_OK;
+}
+
 __attribute__((visibility("default"))) void spconv_packed_free(spconv_packed *p) {
     if (!p) return;
     if (p->dev_block) {

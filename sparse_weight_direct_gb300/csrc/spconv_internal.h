@@ -101,6 +101,10 @@ int forward_variant_supported(int S, int stride, int P, int Q, int LR);
 // rows get their K x K blocks applied from a register window).
 bool dense_taps_supported(int R, int S, int stride, int LR);
 
+// Launches the bounded-wait self-test (flags: bit 0 = the wait timed out,
+// bit 1 = it completed).  arrive = 0 leaves the barrier incomplete.
+cudaError_t launch_wait_selftest(unsigned int *flags, int arrive, cudaStream_t stream);
+
 // Dynamic shared memory a launch needs with `split` blocks per cluster.
 size_t forward_smem_bytes(const Geometry &g, int split);
 
