@@ -386,6 +386,11 @@ def run_ours(args, L):
         "clocks": clk,
         "wall_s": wall,
     }
+    if args.compare_dense:
+        line["dense_conv"] = time_dense_conv(L, rowptr, colidx, value, x, y, flush, stream,
+                                             max(3, min(args.steps, 50)))
+        line["dense_conv"]["speedup_fp32"] = line["dense_conv"]["fp32_us"] / us_kernel
+        line["dense_conv"]["speedup_tf32"] = line["dense_conv"]["tf32_us"] / us_kernel
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us_cpu, threads, sample, _ = time_oracle(L, rowptr, colidx, value, x_host,
                                                  budget_s=args.cpu_budget, steps=3)
@@ -399,19 +404,57 @@ def run_ours(args, L):
     return 0
 
 
+def time_dense_conv(L, rowptr, colidx, value, x, y, flush, stream, steps):
+    """PyTorch's dense conv2d (cuDNN) on the same layer, the pages' baseline:
+    fp32 with TF32 disabled, and PyTorch's default (TF32 allowed), each timed
+    like the sparse kernel (L2 flushed, CUDA events).  Library run only."""
+    import torch
+    import torch.nn.functional as Fn
+    w = np.zeros((L.M, L.CRS), dtype=np.float32)
+    for m in range(L.M):
+        w[m, colidx[rowptr[m]:rowptr[m + 1]]] = value[rowptr[m]:rowptr[m + 1]]
+    wd = torch.from_numpy(w.reshape(L.M, L.C, L.R, L.S)).to(x.device)
+    out = {}
+    prev = torch.backends.cudnn.allow_tf32
+    try:
+        for key, tf32 in (("fp32_us", False), ("tf32_us", True)):
+            torch.backends.cudnn.allow_tf32 = tf32
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    Fn.conv2d(x, wd, stride=L.stride, padding=L.pad)
+                ts = []
+                for _ in range(steps):
+                    flush.zero_()
+                    s0 = torch.cuda.Event(enable_timing=True)
+                    s1 = torch.cuda.Event(enable_timing=True)
+                    s0.record(stream)
+                    Fn.conv2d(x, wd, stride=L.stride, padding=L.pad)
+                    s1.record(stream)
+                    ts.append((s0, s1))
+            torch.cuda.synchronize()
+            out[key] = statistics.mean(a.elapsed_time(b) for a, b in ts) * 1e3
+    finally:
+        torch.backends.cudnn.allow_tf32 = prev
+    out["library"] = f"torch {torch.__version__} cudnn {torch.backends.cudnn.version()}"
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default=workloads.BENCH_DEFAULT, choices=sorted(workloads.LAYERS))
+    ap.add_argument("--config", default=workloads.BENCH_DEFAULT,
+                    choices=sorted(workloads.ALL_LAYERS))
+    ap.add_argument("--compare-dense", action="store_true",
+                    help="also time PyTorch's dense conv2d (cuDNN) on the same layer")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
-    L = workloads.LAYERS[args.config]
+    L = workloads.ALL_LAYERS[args.config]
     if args.impl == "reference":
         return run_reference(args, L)
     return run_ours(args, L)

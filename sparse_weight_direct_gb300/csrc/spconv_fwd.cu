@@ -60,6 +60,7 @@ struct KParams {
     int chunk, num_chunks, split, hdr_words, dense_mask_words;
     int in_stage_bytes, stage_bytes, in_tma_bytes;
     int use_tma;
+    int group_fast, groups;  // block order; number of groups
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -285,15 +286,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int st = ST_CT ? ST_CT : p.stride;
     const int row_step = LR * st * p.row_pitch;  // between this lane's output rows
 
+    // Block order (clusters run along x): channel-split rank fastest, then
+    // either the tile (groups in grid y: the heaviest groups, dense ones,
+    // start first) or, when the input does not fit in L2, the group (grid y =
+    // 1: all groups of a tile run together and share its input through L2).
     const int split = p.split;
     int b = blockIdx.x;
-    const int kr = b % split;  // rank inside the cluster (clusters run along x)
+    const int kr = b % split;
     b /= split;
+    int group = blockIdx.y;
+    if (p.group_fast) {
+        group = b % p.groups;
+        b /= p.groups;
+    }
     const int tx = b % p.tiles_x;
     b /= p.tiles_x;
     const int ty = b % p.tiles_y;
     const int n = b / p.tiles_y;
-    const int group = blockIdx.y;
     const int gflags = p.group_flags[group];
     const bool dense = (gflags & 1) != 0;
     const bool has_parts = (gflags & 2) != 0;
@@ -578,8 +587,9 @@ size_t forward_smem_bytes(const Geometry &g, int split) {
     return bytes + 128;  // room to align the stage buffers to 128 bytes
 }
 
-cudaError_t launch_forward(const Geometry &g, int N, int split, const float *x, float *y,
-                           const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream) {
+cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast, const float *x,
+                           float *y, const DeviceArrays &d, const CUtensorMap *tmap,
+                           cudaStream_t stream) {
     KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows);
     if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks)
         return cudaErrorInvalidConfiguration;
@@ -615,7 +625,13 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, const float *x, 
     }
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((int64_t)N * g.tiles_y * g.tiles_x * split), (unsigned)g.groups, 1);
+    p.groups = g.groups;
+    p.group_fast = group_fast ? 1 : 0;
+    const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x * split;
+    if (p.group_fast)
+        cfg.gridDim = dim3((unsigned)(tiles * g.groups), 1, 1);
+    else
+        cfg.gridDim = dim3((unsigned)tiles, (unsigned)g.groups, 1);
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

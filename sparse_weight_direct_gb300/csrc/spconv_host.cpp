@@ -587,6 +587,23 @@ const CUtensorMap *input_tmap(const spconv_packed *P, const float *x, int N, CUt
     return &tmp;
 }
 
+// Whether to run all channel groups of a tile together.  With tiles first
+// (the default order) every group streams the whole input from HBM once the
+// input exceeds L2; with groups first the tile's input is read from HBM once
+// and shared through L2, but all groups then hit the same lines at once.
+// Groups first wins when re-streaming the input would take longer than a
+// quarter of the layer's compute at the sparse path's rate (~18 % of fp32
+// peak); the quarter is the crossover measured on GB300 over the first
+// page's 256 x 256 sweep (90 % sparse: tiles first; 98 %: groups first).
+bool choose_group_fast(const spconv::Geometry &g, int N, int64_t nnz) {
+    const double in_bytes = 4.0 * N * g.C * g.H * g.W;
+    if (g.groups < 2 || in_bytes < 64.0 * (1 << 20)) return false;
+    const double hbm_bps = 6.7e12, sparse_flops = 0.18 * kSMs * 128 * 2 * 2.07e9;
+    const double restream_s = (g.groups - 1) * in_bytes / hbm_bps;
+    const double compute_s = 2.0 * nnz * N * g.E * g.F / sparse_flops;
+    return restream_s * 4.0 > compute_s;
+}
+
 // Blocks per cluster along the channel chunks: enough to fill the GPU once.
 int choose_split(const spconv::Geometry &g, int N) {
     const int64_t blocks = (int64_t)N * g.tiles_y * g.tiles_x * g.groups;
@@ -640,7 +657,7 @@ __attribute__((visibility("default"))) int spconv_forward(
     if (N == 0) return SPCONV_OK;
     if (!input || !output) return SPCONV_ERR_INVALID_ARG;
     if (((uintptr_t)input & 15) || ((uintptr_t)output & 3)) return SPCONV_ERR_INVALID_ARG;
-    const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x * spconv::kMaxSplit;
+    const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x * spconv::kMaxSplit * g.groups;
     if (tiles > 0x7fffffffLL) return SPCONV_ERR_UNSUPPORTED;
     const size_t in_bytes = (size_t)N * C * H * W * sizeof(float);
     const size_t out_bytes = (size_t)N * M * g.E * g.F * sizeof(float);
@@ -652,8 +669,9 @@ __attribute__((visibility("default"))) int spconv_forward(
         CUtensorMap tmp;
         const CUtensorMap *tmap = input_tmap(packed, input, N, tmp);
         const int split = choose_split(g, N);
-        cudaError_t e = spconv::launch_forward(g, N, split, input, output, packed->d, tmap,
-                                               static_cast<cudaStream_t>(stream));
+        const bool group_fast = choose_group_fast(g, N, packed->nnz);
+        cudaError_t e = spconv::launch_forward(g, N, split, group_fast, input, output, packed->d,
+                                               tmap, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) {
             cudaGetLastError();
             return SPCONV_ERR_CUDA;

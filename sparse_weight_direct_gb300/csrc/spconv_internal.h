@@ -110,8 +110,11 @@ size_t forward_smem_bytes(const Geometry &g, int split);
 
 // Enqueues the forward kernel.  tmap is a tiled tensor map of the input for
 // stride-1 layers whose row stride is a multiple of 16 bytes (nullptr:
-// stage with cp.async).  Returns cudaSuccess or the launch error.
-cudaError_t launch_forward(const Geometry &g, int N, int split, const float *x, float *y,
-                           const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream);
+// stage with cp.async).  group_fast orders blocks so all channel groups of a
+// tile run together (they then share the tile's input through L2).  Returns
+// cudaSuccess or the launch error.
+cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast, const float *x,
+                           float *y, const DeviceArrays &d, const CUtensorMap *tmap,
+                           cudaStream_t stream);
 
 }  // namespace spconv

@@ -218,3 +218,28 @@ def test_forward_argument_errors():
     assert lib.spconv_forward(*args, P(x.data_ptr()), w.handle, P(x.data_ptr()), None) == -1
     torch.cuda.synchronize()
     w.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["p1_oc64_s90", "p1_oc128_s98", "p1_oc256_s94"])
+def test_p1_sweep_sampled(name):
+    """The first page's A100 sweep shapes at full size (N=32, 32 -> OC,
+    256x256): 20 000 sampled outputs against the oracle evaluated one output
+    at a time (Eq.(3)), and every output written (the buffer is prefilled
+    with NaN)."""
+    L = workloads.P1_LAYERS[name]
+    rowptr, colidx, value = workloads.make_weights(L)
+    x = workloads.make_input(L)
+    w = swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
+                 stride=L.stride, pad=L.pad)
+    xd = torch.from_numpy(x).cuda()
+    out = torch.full((L.N, L.M, L.E, L.F), float("nan"), device="cuda")
+    swd.forward(xd, w, out=out)
+    torch.cuda.synchronize()
+    assert not torch.isnan(out).any()
+    rng = np.random.default_rng(7)
+    idx = rng.integers(0, out.numel(), size=20000)
+    got = out.reshape(-1)[torch.from_numpy(idx).cuda()].cpu().numpy().astype(np.float64)
+    ref, mag = oracle.csr_points(x, rowptr, colidx, value, L.M, L.R, L.S, L.stride, L.pad, idx)
+    check(got, ref, mag, what=name)
+    w.close()

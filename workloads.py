@@ -85,6 +85,26 @@ def _layers() -> List[Layer]:
 
 LAYERS: Dict[str, Layer] = {l.name: l for l in _layers()}
 
+
+def _p1_sweep() -> List[Layer]:
+    """The first page's A100 sweep (Tuteja et al., Sec. 6.1, Fig. 5a/6a/7a):
+    N=32, IC=32, H=W=256, 3x3, stride 1, same-size output, OC 48..256,
+    sparsity 90..98 %.  The page's weight generator draws positions with
+    Python's random module and states no value distribution; Bernoulli
+    positions and N(0, 0.05) values stand in."""
+    out = []
+    for oc in (48, 64, 80, 96, 112, 128, 256):
+        for sp in (90, 92, 94, 96, 98):
+            out.append(Layer(f"p1_oc{oc}_s{sp}", 32, 32, 256, 256, oc, 3, 3, 1, 1,
+                             round(1.0 - sp / 100.0, 4), seed=5000 + oc * 100 + sp))
+    return out
+
+
+# Shapes of the pages' own dense-vs-sparse comparison (not part of the
+# default parity sweep: each input is 268 MB).
+P1_LAYERS: Dict[str, Layer] = {l.name: l for l in _p1_sweep()}
+ALL_LAYERS: Dict[str, Layer] = {**LAYERS, **P1_LAYERS}
+
 # The layer the benchmark times by default: the ResNet-style 3x3 layer at 90 %.
 BENCH_DEFAULT = "resnet3x3"
 
