@@ -97,6 +97,23 @@ int spconv_forward(int N, int C, int H, int W, int M, int R, int S, int stride, 
                    const float *input, const spconv_packed *packed, float *output,
                    void *stream);
 
+/* Activations of the fused epilogue of spconv_forward_ex. */
+typedef enum spconv_act { SPCONV_ACT_NONE = 0, SPCONV_ACT_RELU = 1 } spconv_act;
+
+/*
+ * spconv_forward_ex -- spconv_forward with a fused epilogue applied in the
+ * kernel's write-back:  Y[n,m,e,f] = act(conv[n,m,e,f] + bias[m]).
+ * (The first page names bias/activation fusion and layer chaining as its
+ * follow-on work, Sec. 7.)
+ *   bias  device pointer to M floats (4-byte aligned), or NULL for no bias
+ *   act   SPCONV_ACT_NONE or SPCONV_ACT_RELU (y = max(y, 0))
+ * Every other argument, and the errors, as for spconv_forward; INVALID_ARG
+ * also for an unknown act or a bias overlapping the output.
+ */
+int spconv_forward_ex(int N, int C, int H, int W, int M, int R, int S, int stride, int pad,
+                      const float *input, const spconv_packed *packed, const float *bias,
+                      int act, float *output, void *stream);
+
 /* Frees the handle and its device buffers.  NULL-safe.  The caller must make
  * sure no forward that uses the handle is still running. */
 void spconv_packed_free(spconv_packed *p);

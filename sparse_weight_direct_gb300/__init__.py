@@ -140,10 +140,12 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def forward(x, packed: PackedWeights, out=None, stream=None):
+def forward(x, packed: PackedWeights, out=None, stream=None, bias=None, relu: bool = False):
     """Y = conv(x, packed) on the GPU.  x: (N, C, H, W) contiguous float32
     CUDA tensor; out (optional): (N, M, E, F) float32 CUDA tensor, overwritten.
-    Asynchronous on ``stream`` (default: the current torch stream)."""
+    bias (optional): (M,) float32 CUDA tensor added in the kernel's write-back;
+    relu: apply max(y, 0) there too.  Asynchronous on ``stream`` (default: the
+    current torch stream)."""
     import torch
     sh = packed.shape
     if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32
@@ -158,9 +160,21 @@ def forward(x, packed: PackedWeights, out=None, stream=None):
     elif not (out.is_cuda and out.dtype == torch.float32 and out.is_contiguous()
               and tuple(out.shape) == (N, sh["M"], E, F)):
         raise SpconvError(_lib.SPCONV_ERR_INVALID_ARG, "out has the wrong shape/dtype/layout")
-    rc = _lib.lib().spconv_forward(N, x.shape[1], x.shape[2], x.shape[3], sh["M"], sh["R"],
-                                   sh["S"], sh["stride"], sh["pad"],
-                                   ctypes.c_void_p(x.data_ptr()), packed.handle,
-                                   ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream))
-    _lib.check(rc, "spconv_forward")
+    if bias is None and not relu:
+        rc = _lib.lib().spconv_forward(N, x.shape[1], x.shape[2], x.shape[3], sh["M"], sh["R"],
+                                       sh["S"], sh["stride"], sh["pad"],
+                                       ctypes.c_void_p(x.data_ptr()), packed.handle,
+                                       ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream))
+        _lib.check(rc, "spconv_forward")
+        return out
+    if bias is not None and not (bias.is_cuda and bias.dtype == torch.float32
+                                 and bias.is_contiguous() and bias.numel() == sh["M"]):
+        raise SpconvError(_lib.SPCONV_ERR_INVALID_ARG, "bias must be M contiguous float32 on the GPU")
+    rc = _lib.lib().spconv_forward_ex(N, x.shape[1], x.shape[2], x.shape[3], sh["M"], sh["R"],
+                                      sh["S"], sh["stride"], sh["pad"],
+                                      ctypes.c_void_p(x.data_ptr()), packed.handle,
+                                      ctypes.c_void_p(bias.data_ptr() if bias is not None else 0),
+                                      1 if relu else 0, ctypes.c_void_p(out.data_ptr()),
+                                      _stream_ptr(stream))
+    _lib.check(rc, "spconv_forward_ex")
     return out

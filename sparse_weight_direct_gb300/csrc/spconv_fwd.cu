@@ -49,6 +49,8 @@ constexpr int kMaxDynamicSmem = 200 * 1024;                   // upper bound of 
 struct KParams {
     const float *x;
     float *y;
+    const float *bias;  // [M] or nullptr
+    int act;            // 0 identity, 1 ReLU
     const unsigned char *blobs;
     const uint32_t *blob_off;
     const int *slot_oc;      // head slot -> output channel; -1 empty or a later part
@@ -185,6 +187,13 @@ __device__ __forceinline__ void stage_input_cp_async(const KParams &p, float *bu
 }
 
 // ---------------------------------------------------------------- compute
+
+// Fused epilogue: bias, then the activation.
+__device__ __forceinline__ float finish(const KParams &p, int m, float v) {
+    if (p.bias) v += __ldg(p.bias + m);
+    if (p.act == 1) v = fmaxf(v, 0.f);
+    return v;
+}
 
 // Kernel instances that carry the dense-tap path: stride 1, K x K with K = 3, 5.
 template <int S_CT, int ST_CT>
@@ -431,7 +440,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 #pragma unroll
             for (int r = 0; r < P; ++r) {
                 const int oy = oy0 + LR * r;
-                if (oy < p.E) yo[(size_t)oy * p.F] = acc[q][r];
+                if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, acc[q][r]);
             }
         }
         return;
@@ -460,7 +469,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                 for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c])
                     sum += part[(c * P + r) * 32 + lane];
                 const int oy = oy0 + LR * r;
-                if (oy < p.E) yo[(size_t)oy * p.F] = sum;
+                if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, sum);
             }
         }
         return;
@@ -481,7 +490,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                         sum += rp[(c * P + r) * 32 + lane];
                     }
                 const int oy = oy0 + LR * r;
-                if (oy < p.E) yo[(size_t)oy * p.F] = sum;
+                if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, sum);
             }
         }
     }
@@ -588,8 +597,8 @@ size_t forward_smem_bytes(const Geometry &g, int split) {
 }
 
 cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast, const float *x,
-                           float *y, const DeviceArrays &d, const CUtensorMap *tmap,
-                           cudaStream_t stream) {
+                           float *y, const float *bias, int act, const DeviceArrays &d,
+                           const CUtensorMap *tmap, cudaStream_t stream) {
     KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows);
     if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks)
         return cudaErrorInvalidConfiguration;
@@ -601,6 +610,8 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
     KParams p;
     p.x = x;
     p.y = y;
+    p.bias = bias;
+    p.act = act;
     p.blobs = d.blobs;
     p.blob_off = d.blob_off;
     p.slot_oc = d.slot_oc;

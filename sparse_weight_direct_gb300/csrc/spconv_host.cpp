@@ -138,13 +138,13 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     g.plane = g.in_rows * g.row_pitch;
     g.warps = spconv::kWarps;
     // output channels per warp: the largest Q in {4, 2, 1} whose one-image
-    // grid, with the channels split over a full cluster, still covers ~80 % of
-    // the SMs (small layers trade per-warp reuse for parallelism)
+    // grid, with the channels split over a full cluster, still gives ~1.5
+    // blocks per SM (small layers trade per-warp reuse for parallelism)
     const int64_t spatial = (int64_t)g.tiles_y * g.tiles_x;
     g.slots = 1;
     for (int Q : {4, 2}) {
         const int64_t groups = (M + (int64_t)spconv::kWarps * Q - 1) / ((int64_t)spconv::kWarps * Q);
-        if (spatial * groups * spconv::kMaxSplit * 5 >= (int64_t)kSMs * 4) {
+        if (spatial * groups * spconv::kMaxSplit * 2 >= (int64_t)kSMs * 3) {
             g.slots = Q;
             break;
         }
@@ -317,10 +317,10 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
     const int C = g.C;
     const int64_t base_blocks = (int64_t)g.tiles_y * g.tiles_x * g.groups;
     int want_split = (int)std::min<int64_t>(spconv::kMaxSplit,
-                                            (kSMs + base_blocks - 1) / std::max<int64_t>(base_blocks, 1));
+                                            (2 * kSMs + base_blocks - 1) / std::max<int64_t>(base_blocks, 1));
     want_split = std::max(want_split, 1);
     int cap = std::min(C, 256);  // TMA box extent limit
-    if (want_split > 1 && C / want_split >= 16)
+    if (want_split > 1 && C / want_split >= 32)
         cap = std::min(cap, (C + want_split - 1) / want_split);
     const size_t hdr_bytes = (size_t)g.hdr_words * 4;
     for (int chunk = cap; chunk >= 1; --chunk) {
@@ -604,11 +604,13 @@ bool choose_group_fast(const spconv::Geometry &g, int N, int64_t nnz) {
     return restream_s * 4.0 > compute_s;
 }
 
-// Blocks per cluster along the channel chunks: enough to fill the GPU once.
+// Blocks per cluster along the channel chunks: none when the grid already
+// fills the GPU, else enough for about two blocks per SM (measured best on
+// the one-image ResNet-style layer).
 int choose_split(const spconv::Geometry &g, int N) {
     const int64_t blocks = (int64_t)N * g.tiles_y * g.tiles_x * g.groups;
     if (blocks >= kSMs) return 1;
-    int s = (int)std::min<int64_t>(spconv::kMaxSplit, (kSMs + blocks - 1) / blocks);
+    int s = (int)std::min<int64_t>(spconv::kMaxSplit, (2 * kSMs + blocks - 1) / blocks);
     return std::max(1, std::min(s, g.num_chunks));
 }
 
@@ -645,10 +647,11 @@ __attribute__((visibility("default"))) int spconv_pack(
     }
 }
 
-__attribute__((visibility("default"))) int spconv_forward(
+__attribute__((visibility("default"))) int spconv_forward_ex(
     int N, int C, int H, int W, int M, int R, int S, int stride, int pad, const float *input,
-    const spconv_packed *packed, float *output, void *stream) {
+    const spconv_packed *packed, const float *bias, int act, float *output, void *stream) {
     if (!packed || N < 0) return SPCONV_ERR_INVALID_ARG;
+    if (act != SPCONV_ACT_NONE && act != SPCONV_ACT_RELU) return SPCONV_ERR_INVALID_ARG;
     const spconv::Geometry &g = packed->g;
     if (C != g.C || H != g.H || W != g.W || M != g.M || R != g.R || S != g.S ||
         stride != g.stride || pad != g.pad)
@@ -656,12 +659,15 @@ __attribute__((visibility("default"))) int spconv_forward(
     if (!packed->dev_block) return SPCONV_ERR_MISMATCH;
     if (N == 0) return SPCONV_OK;
     if (!input || !output) return SPCONV_ERR_INVALID_ARG;
-    if (((uintptr_t)input & 15) || ((uintptr_t)output & 3)) return SPCONV_ERR_INVALID_ARG;
+    if (((uintptr_t)input & 15) || ((uintptr_t)output & 3) || ((uintptr_t)bias & 3))
+        return SPCONV_ERR_INVALID_ARG;
     const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x * spconv::kMaxSplit * g.groups;
     if (tiles > 0x7fffffffLL) return SPCONV_ERR_UNSUPPORTED;
     const size_t in_bytes = (size_t)N * C * H * W * sizeof(float);
     const size_t out_bytes = (size_t)N * M * g.E * g.F * sizeof(float);
     if (ranges_overlap(input, in_bytes, output, out_bytes)) return SPCONV_ERR_INVALID_ARG;
+    if (bias && ranges_overlap(bias, (size_t)M * sizeof(float), output, out_bytes))
+        return SPCONV_ERR_INVALID_ARG;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return SPCONV_ERR_CUDA;
     if (dev != packed->device) return SPCONV_ERR_MISMATCH;
@@ -670,8 +676,8 @@ __attribute__((visibility("default"))) int spconv_forward(
         const CUtensorMap *tmap = input_tmap(packed, input, N, tmp);
         const int split = choose_split(g, N);
         const bool group_fast = choose_group_fast(g, N, packed->nnz);
-        cudaError_t e = spconv::launch_forward(g, N, split, group_fast, input, output, packed->d,
-                                               tmap, static_cast<cudaStream_t>(stream));
+        cudaError_t e = spconv::launch_forward(g, N, split, group_fast, input, output, bias, act,
+                                               packed->d, tmap, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) {
             cudaGetLastError();
             return SPCONV_ERR_CUDA;
@@ -680,6 +686,13 @@ __attribute__((visibility("default"))) int spconv_forward(
         return SPCONV_ERR_ALLOC;
     }
     return SPCONV_OK;
+}
+
+__attribute__((visibility("default"))) int spconv_forward(
+    int N, int C, int H, int W, int M, int R, int S, int stride, int pad, const float *input,
+    const spconv_packed *packed, float *output, void *stream) {
+    return spconv_forward_ex(N, C, H, W, M, R, S, stride, pad, input, packed, nullptr,
+                             SPCONV_ACT_NONE, output, stream);
 }
 
 __attribute__((visibility("default"))) int spconv_device_status(const spconv_packed *p,

@@ -112,9 +112,10 @@ size_t forward_smem_bytes(const Geometry &g, int split);
 // stride-1 layers whose row stride is a multiple of 16 bytes (nullptr:
 // stage with cp.async).  group_fast orders blocks so all channel groups of a
 // tile run together (they then share the tile's input through L2).  Returns
-// cudaSuccess or the launch error.
+// cudaSuccess or the launch error.  bias (M floats or nullptr) and act
+// (0 identity, 1 ReLU) form the fused epilogue y = act(conv + bias).
 cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast, const float *x,
-                           float *y, const DeviceArrays &d, const CUtensorMap *tmap,
-                           cudaStream_t stream);
+                           float *y, const float *bias, int act, const DeviceArrays &d,
+                           const CUtensorMap *tmap, cudaStream_t stream);
 
 }  // namespace spconv
