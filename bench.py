@@ -158,12 +158,12 @@ def whole_job_us_per_layer(max_total_ms: float, steps: int, world: int) -> float
     return max_total_ms * 1e3 / (steps * world)
 
 
-def layer_numbers(L, nnz: int):
+def layer_numbers(L, nnz: int, entry_bytes: int = roofline.ENTRY_BYTES):
     E, F = L.E, L.F
     return {
         "useful_flop": roofline.useful_flops(nnz, L.N, E, F),
         "dense_flop": roofline.dense_equiv_flops(L.N, E, F, L.M, L.C, L.R, L.S),
-        "alg_bytes": roofline.algorithmic_bytes(L.N, L.C, L.H, L.W, L.M, E, F, nnz),
+        "alg_bytes": roofline.algorithmic_bytes(L.N, L.C, L.H, L.W, L.M, E, F, nnz, entry_bytes),
     }
 
 
@@ -274,7 +274,7 @@ def run_ours(args, L):
 
     t0 = time.perf_counter()
     w = swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
-                 stride=L.stride, pad=L.pad, stream=stream)
+                 stride=L.stride, pad=L.pad, stream=stream, fmt=args.fmt)
     pack_ms = (time.perf_counter() - t0) * 1e3
     info = w.info()
 
@@ -338,7 +338,7 @@ def run_ours(args, L):
     ms_step = total_ms / args.steps
     us_layer = whole_job_us_per_layer(total_ms, args.steps, world)
     us_kernel = ms_step * 1e3                                 # one launch on one GPU
-    num = layer_numbers(L, nnz)
+    num = layer_numbers(L, nnz, 4 if args.fmt == "packed32" else roofline.ENTRY_BYTES)
     peaks, peak_kind = measured_peaks()
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     p_fp32 = fp32_peak_flops(sm_count, float(peaks.get("sm_max_mhz", 2070.0)))
@@ -365,7 +365,8 @@ def run_ours(args, L):
         "metric": METRIC, "value": us_layer, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic", "config": describe(L),
+        "dtype": "f32" if args.fmt == "f32" else "f32 (fp16 weights)", "data": "synthetic",
+        "config": {**describe(L), "weight_format": args.fmt},
         "dense_equiv_tflops": num["dense_flop"] / (us_kernel * 1e-6) / 1e12,
         "useful_gflops": num["useful_flop"] / (us_kernel * 1e-6) / 1e9,
         "alg_gbs": num["alg_bytes"] / (us_kernel * 1e-6) / 1e9,
@@ -446,6 +447,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default=workloads.BENCH_DEFAULT,
                     choices=sorted(workloads.ALL_LAYERS))
+    ap.add_argument("--fmt", default="f32", choices=["f32", "packed32"],
+                    help="packed weight format (packed32: the first page's 32-bit words, FP16)")
     ap.add_argument("--compare-dense", action="store_true",
                     help="also time PyTorch's dense conv2d (cuDNN) on the same layer")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -77,6 +77,26 @@ int spconv_pack(int C, int H, int W, int M, int R, int S, int stride, int pad,
                 const int32_t *rowptr, const int32_t *colidx, const float *value,
                 void *stream, spconv_packed **out);
 
+/* Packed weight formats of spconv_pack_ex. */
+typedef enum spconv_format {
+    SPCONV_FORMAT_F32 = 0,      /* 8-byte entries: fp32 value + int32 precomputed offset    */
+    SPCONV_FORMAT_PACKED32 = 1  /* 4-byte words of the first page's Sec. 5.3 / Fig. 4:      */
+                                /* [31:16] FP16 value, [15:8] input channel (within the     */
+                                /* chunk), [7:4] kernel column, [3:0] kernel row; R, S <= 16 */
+} spconv_format;
+
+/*
+ * spconv_pack_ex -- spconv_pack with a choice of entry format and of where
+ * the handle lives.  format: spconv_format (PACKED32 rounds every weight to
+ * FP16 once, round-to-nearest-even, and halves the sparse entry stream; dense
+ * rows keep their FP16-rounded values as fp32).  host_only != 0: as
+ * spconv_pack_host (no device work, stream ignored).  Errors as spconv_pack;
+ * INVALID_ARG for an unknown format, UNSUPPORTED for PACKED32 with R or S > 16.
+ */
+int spconv_pack_ex(int C, int H, int W, int M, int R, int S, int stride, int pad,
+                   const int32_t *rowptr, const int32_t *colidx, const float *value, int format,
+                   int host_only, void *stream, spconv_packed **out);
+
 /*
  * spconv_forward -- Y = conv(X, packed weights); the hot path.
  *
@@ -185,6 +205,8 @@ typedef struct spconv_packed_info {
                               /* lane_rows * tile_rows)                         */
     int32_t dense_groups;     /* leading groups whose blobs are dense-tap       */
     int32_t dense_mask_words; /* words of a dense blob's slot masks            */
+    int32_t format;           /* spconv_format of the sparse entries           */
+    int32_t reserved;
 } spconv_packed_info;
 
 int spconv_packed_info_get(const spconv_packed *p, spconv_packed_info *info);
@@ -195,7 +217,8 @@ typedef enum spconv_array {
                                /* 16-byte aligned.  Sparse groups: hdr_words       */
                                /* uint32 entry indices (slot w*Q+q spans           */
                                /* [hdr[w*Q+q], hdr[w*Q+q+1])), then entries of     */
-                               /* {float value, int32 offset}.  Dense groups:      */
+                               /* {float value, int32 offset} (F32) or 32-bit      */
+                               /* packed words (PACKED32).  Dense groups:          */
                                /* dense_mask_words uint32 slot masks [warp][chan], */
                                /* then floats [warp][chan][slot][R*S rounded to 4] */
     SPCONV_ARRAY_BLOB_OFF = 1, /* uint32 [groups * num_chunks + 1]: blob starts in  */

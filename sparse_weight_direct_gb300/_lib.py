@@ -23,7 +23,7 @@ SPCONV_ERR_MISMATCH = -6
 SPCONV_ERR_DEVICE = -7
 
 # Every symbol include/spconv.h declares.
-EXPORTS = ("spconv_pack", "spconv_forward", "spconv_forward_ex", "spconv_packed_free",
+EXPORTS = ("spconv_pack", "spconv_pack_ex", "spconv_forward", "spconv_forward_ex", "spconv_packed_free",
            "spconv_status_string",
            "spconv_pack_host", "spconv_device_status", "spconv_selftest_wait",
            "spconv_packed_info_get", "spconv_packed_copy_array")
@@ -51,7 +51,7 @@ class PackedInfo(ctypes.Structure):
         ("device_bytes", "smem_bytes", "max_warp_nnz", "mean_warp_nnz")] + [
         (n, ctypes.c_int32) for n in
         ("hdr_words", "blob_stage_bytes", "in_stage_bytes", "lane_rows", "dense_groups",
-         "dense_mask_words")]
+         "dense_mask_words", "format", "reserved")]
 
 
 def lib() -> ctypes.CDLL:
@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
         L.spconv_pack.restype = i
         L.spconv_pack_host.argtypes = [i] * 8 + [p, p, p, ctypes.POINTER(ctypes.c_void_p)]
         L.spconv_pack_host.restype = i
+        L.spconv_pack_ex.argtypes = [i] * 8 + [p, p, p, i, i, p, ctypes.POINTER(ctypes.c_void_p)]
+        L.spconv_pack_ex.restype = i
         L.spconv_forward.argtypes = [i] * 9 + [p, p, p, p]
         L.spconv_forward.restype = i
         L.spconv_forward_ex.argtypes = [i] * 9 + [p, p, p, i, p, p]

@@ -30,6 +30,7 @@
 // partial tiles: Sec. 5.5 of the first page).
 #include <cooperative_groups.h>
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -62,6 +63,7 @@ struct KParams {
     int chunk, num_chunks, split, hdr_words, dense_mask_words;
     int in_stage_bytes, stage_bytes, in_tma_bytes;
     int use_tma;
+    int fmt;  // sparse entries: 0 = {fp32 value, int32 offset}, 1 = 32-bit packed word
     int group_fast, groups;  // block order; number of groups
 };
 
@@ -274,6 +276,36 @@ __device__ __forceinline__ void run_dense_chunk(float (&acc)[Q][P], const float 
     }
 }
 
+// The first page's packed weight word (Tuteja et al., Sec. 5.3, Fig. 4):
+// [31:16] FP16 value, [15:8] input channel (here: within the chunk), [7:4]
+// kernel column px, [3:0] kernel row py.  The offset into the staged tile is
+// rebuilt from (channel, py, px) per entry.
+template <int P, int ROW_STEP, int ST_CT>
+__device__ __forceinline__ void apply_word(float (&acc)[P], const float *sb, uint32_t w,
+                                           const KParams &p, int row_step) {
+    const float v = __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+    const int cl = (int)((w >> 8) & 0xffu), px = (int)((w >> 4) & 0xfu), py = (int)(w & 0xfu);
+    const int st = ST_CT ? ST_CT : p.stride;
+    const int col = (st == 1) ? px + p.shift : (px % st) * p.phase_pitch + px / st;
+    apply_entry<P, ROW_STEP>(acc, sb, v, cl * p.plane + py * p.row_pitch + col, row_step);
+}
+
+template <int P, int ROW_STEP, int ST_CT>
+__device__ __forceinline__ void run_segment_words(float (&acc)[P], const float *sb,
+                                                  const uint32_t *ent, int j, int j1,
+                                                  const KParams &p, int row_step) {
+    for (; (j & 3) && j < j1; ++j)  // head: bring j to a 16-byte boundary
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, ent[j], p, row_step);
+    for (; j + 3 < j1; j += 4) {
+        const uint4 e = *reinterpret_cast<const uint4 *>(ent + j);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.x, p, row_step);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.y, p, row_step);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.z, p, row_step);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.w, p, row_step);
+    }
+    for (; j < j1; ++j) apply_word<P, ROW_STEP, ST_CT>(acc, sb, ent[j], p, row_step);  // tail
+}
+
 // P: output rows per lane; Q: output channels per warp; LR: lane rows (1, or 2
 // interleaved half-warps of 16 lanes for outputs at most 16 wide); S_CT/ST_CT:
 // kernel width and stride when known at compile time (0 = read from p).
@@ -389,13 +421,21 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                     warp, p.chunk, min(p.chunk, p.C - k * p.chunk), p.plane);
             }
         }
-        if (!dense) {
+        if (!dense && p.fmt == 0) {
             const float2 *ent = reinterpret_cast<const float2 *>(hdr + p.hdr_words);
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
                 const int j0 = (int)hdr[warp * Q + q];
                 const int j1 = (int)hdr[warp * Q + q + 1];
                 run_segment<P, ROW_STEP>(acc[q], sb, ent, j0, j1, row_step);
+            }
+        } else if (!dense) {
+            const uint32_t *ent = hdr + p.hdr_words;
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int j0 = (int)hdr[warp * Q + q];
+                const int j1 = (int)hdr[warp * Q + q + 1];
+                run_segment_words<P, ROW_STEP, ST_CT>(acc[q], sb, ent, j0, j1, p, row_step);
             }
         }
         if (p.use_tma) {
@@ -629,6 +669,7 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
     p.stage_bytes = (int)stage_bytes(g);
     p.in_tma_bytes = g.chunk * g.plane * (int)sizeof(float);
     p.use_tma = tmap ? 1 : 0;
+    p.fmt = g.format;
     CUtensorMap dummy;
     if (!tmap) {
         for (int i = 0; i < 16; ++i) dummy.opaque[i] = 0;

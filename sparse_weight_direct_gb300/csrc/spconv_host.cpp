@@ -13,6 +13,7 @@
 // "Theoretical and Empirical Analysis of Sparse Convolution", Sec. 5.3.
 #include "../../include/spconv.h"
 
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -303,6 +304,11 @@ int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx)
     return SPCONV_OK;
 }
 
+size_t entry_bytes(const spconv::Geometry &g) { return g.format == 1 ? 4 : 8; }
+
+// FP16 rounding used by the 32-bit packed format (round to nearest even).
+float to_half_and_back(float v) { return __half2float(__float2half_rn(v)); }
+
 size_t dense_blob_bytes(const spconv::Geometry &g, int chunk) {
     const size_t mask_words = round_up((size_t)g.warps * chunk, 4);
     const size_t kk4 = round_up((size_t)g.R * g.S, 4);
@@ -331,7 +337,8 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
             const int64_t *pre = &gpre[(size_t)grp * (C + 1)];
             for (int k = 0; k < nch; ++k) {
                 const int c0 = k * chunk, c1 = std::min(C, c0 + chunk);
-                const size_t bytes = hdr_bytes + round_up((size_t)(pre[c1] - pre[c0]) * 8, 16);
+                const size_t bytes =
+                    hdr_bytes + round_up((size_t)(pre[c1] - pre[c0]) * entry_bytes(g), 16);
                 blob_max = std::max(blob_max, bytes);
             }
         }
@@ -391,7 +398,8 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
             if (P.group_flags[grp] & 1)
                 total += dense_blob_bytes(g, g.chunk);
             else
-                total += (size_t)g.hdr_words * 4 + round_up((size_t)(pre[c1] - pre[c0]) * 8, 16);
+                total += (size_t)g.hdr_words * 4 +
+                         round_up((size_t)(pre[c1] - pre[c0]) * entry_bytes(g), 16);
         }
     }
     P.blob_off[(size_t)g.groups * nch] = (uint32_t)(total / 16);
@@ -418,14 +426,16 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
                             if (c >= c_end) break;
                             const int cl = c - k * g.chunk;
                             mask[w * g.chunk + cl] |= 1u << q;
-                            wts[((size_t)(w * g.chunk + cl) * g.slots + q) * kk4 + col % RS] =
-                                value[idx[t]];
+                            const float v = g.format == 1 ? to_half_and_back(value[idx[t]])
+                                                          : value[idx[t]];
+                            wts[((size_t)(w * g.chunk + cl) * g.slots + q) * kk4 + col % RS] = v;
                         }
                     }
                 continue;
             }
             uint32_t *hdr = reinterpret_cast<uint32_t *>(blob);
             HostEntry *ent = reinterpret_cast<HostEntry *>(blob + (size_t)g.hdr_words * 4);
+            uint32_t *word = reinterpret_cast<uint32_t *>(blob + (size_t)g.hdr_words * 4);
             uint32_t e = 0;
             for (int ls = 0; ls < slots_per_group; ++ls) {
                 const int slot = grp * slots_per_group + ls;
@@ -439,6 +449,14 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
                     const int r = (col / g.S) % g.R;
                     const int s = col % g.S;
                     const int cl = c - k * g.chunk;
+                    if (g.format == 1) {
+                        // [31:16] FP16 value, [15:8] channel, [7:4] px (column), [3:0] py (row)
+                        const __half hv = __float2half_rn(value[idx[t]]);
+                        const uint32_t bits = (uint32_t)__half_as_ushort(hv);
+                        word[e++] = (bits << 16) | ((uint32_t)cl << 8) | ((uint32_t)s << 4) |
+                                    (uint32_t)r;
+                        continue;
+                    }
                     HostEntry h;
                     h.value = value[idx[t]];
                     if (g.stride == 1)
@@ -460,11 +478,14 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
 }
 
 int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
-                const int32_t *rowptr, const int32_t *colidx, const float *value,
+                const int32_t *rowptr, const int32_t *colidx, const float *value, int format,
                 spconv_packed **out) {
     if (!out) return SPCONV_ERR_INVALID_ARG;
+    if (format != SPCONV_FORMAT_F32 && format != SPCONV_FORMAT_PACKED32)
+        return SPCONV_ERR_INVALID_ARG;
     int st = validate_shape(C, H, W, M, R, S, stride, pad);
     if (st) return st;
+    if (format == SPCONV_FORMAT_PACKED32 && (R > 16 || S > 16)) return SPCONV_ERR_UNSUPPORTED;
     int64_t nnz = 0;
     st = validate_csr(M, (int64_t)C * R * S, rowptr, colidx, value, &nnz);
     if (st) return st;
@@ -472,6 +493,7 @@ int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
     spconv_packed *P = new (std::nothrow) spconv_packed();
     if (!P) return SPCONV_ERR_ALLOC;
     P->nnz = nnz;
+    P->g.format = format;
     st = plan_tiles(P->g, C, H, W, M, R, S, stride, pad);
     if (!st) st = build_layout(*P, rowptr, colidx, value);
     if (st) {
@@ -618,33 +640,40 @@ int choose_split(const spconv::Geometry &g, int N) {
 
 extern "C" {
 
-__attribute__((visibility("default"))) int spconv_pack_host(
+__attribute__((visibility("default"))) int spconv_pack_ex(
     int C, int H, int W, int M, int R, int S, int stride, int pad, const int32_t *rowptr,
-    const int32_t *colidx, const float *value, spconv_packed **out) {
-    try {
-        return make_handle(C, H, W, M, R, S, stride, pad, rowptr, colidx, value, out);
-    } catch (...) {
-        return SPCONV_ERR_ALLOC;
-    }
-}
-
-__attribute__((visibility("default"))) int spconv_pack(
-    int C, int H, int W, int M, int R, int S, int stride, int pad, const int32_t *rowptr,
-    const int32_t *colidx, const float *value, void *stream, spconv_packed **out) {
+    const int32_t *colidx, const float *value, int format, int host_only, void *stream,
+    spconv_packed **out) {
     try {
         spconv_packed *P = nullptr;
-        int st = make_handle(C, H, W, M, R, S, stride, pad, rowptr, colidx, value, &P);
+        int st = make_handle(C, H, W, M, R, S, stride, pad, rowptr, colidx, value, format, &P);
         if (st) return st;
-        st = upload(P, static_cast<cudaStream_t>(stream));
-        if (st) {
-            spconv_packed_free(P);
-            return st;
+        if (!host_only) {
+            st = upload(P, static_cast<cudaStream_t>(stream));
+            if (st) {
+                spconv_packed_free(P);
+                return st;
+            }
         }
         *out = P;
         return SPCONV_OK;
     } catch (...) {
         return SPCONV_ERR_ALLOC;
     }
+}
+
+__attribute__((visibility("default"))) int spconv_pack_host(
+    int C, int H, int W, int M, int R, int S, int stride, int pad, const int32_t *rowptr,
+    const int32_t *colidx, const float *value, spconv_packed **out) {
+    return spconv_pack_ex(C, H, W, M, R, S, stride, pad, rowptr, colidx, value, SPCONV_FORMAT_F32,
+                          1, nullptr, out);
+}
+
+__attribute__((visibility("default"))) int spconv_pack(
+    int C, int H, int W, int M, int R, int S, int stride, int pad, const int32_t *rowptr,
+    const int32_t *colidx, const float *value, void *stream, spconv_packed **out) {
+    return spconv_pack_ex(C, H, W, M, R, S, stride, pad, rowptr, colidx, value, SPCONV_FORMAT_F32,
+                          0, stream, out);
 }
 
 __attribute__((visibility("default"))) int spconv_forward_ex(
@@ -798,6 +827,7 @@ __attribute__((visibility("default"))) int spconv_packed_info_get(const spconv_p
     info->blob_stage_bytes = (int32_t)g.blob_stage_bytes;
     info->in_stage_bytes = (int32_t)g.in_stage_bytes;
     info->dense_groups = g.dense_groups;
+    info->format = g.format;
     info->dense_mask_words = g.dense_mask_words;
     return SPCONV_OK;
 }

@@ -42,9 +42,9 @@ def test_status_strings():
     assert "unknown" in swd.status_string(-99)
 
 
-def _pack_host(L, rowptr, colidx, value):
+def _pack_host(L, rowptr, colidx, value, fmt="f32"):
     return swd.pack_host(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
-                         stride=L.stride, pad=L.pad)
+                         stride=L.stride, pad=L.pad, fmt=fmt)
 
 
 def decode_layout(w):
@@ -105,8 +105,25 @@ def decode_layout(w):
                                 rows.setdefault(m, []).append((c * RS + int(t), float(blk[t])))
                 continue
             hdr = blob[:hw * 4].view(np.uint32)
-            ent = blob[hw * 4:].view([("value", "<f4"), ("off", "<i4")])
             assert hdr[0] == 0 and np.all(np.diff(hdr[:spg + 1].astype(np.int64)) >= 0)
+            if info["format"] == 1:
+                # [31:16] fp16 value, [15:8] channel in chunk, [7:4] column, [3:0] row
+                words = blob[hw * 4:].view(np.uint32)
+                assert hdr[spg] <= words.size and words.size - hdr[spg] <= 3
+                for ls in range(spg):
+                    m = int(slot_oc[g * spg + ls])
+                    seg = words[hdr[ls]:hdr[ls + 1]]
+                    if m < 0:
+                        assert seg.size == 0
+                        continue
+                    for wd in seg.tolist():
+                        v = float(np.array([wd >> 16], np.uint16).view(np.float16)[0])
+                        cl, s, r = (wd >> 8) & 0xFF, (wd >> 4) & 0xF, wd & 0xF
+                        assert cl < info["chunk"] and r < R and s < S
+                        c = k * info["chunk"] + cl
+                        rows.setdefault(m, []).append(((c * R + r) * S + s, v))
+                continue
+            ent = blob[hw * 4:].view([("value", "<f4"), ("off", "<i4")])
             assert hdr[spg] <= ent.size and ent.size - hdr[spg] <= 1  # 16-byte padding
             for ls in range(spg):
                 m = int(slot_oc[g * spg + ls])
@@ -133,12 +150,15 @@ def decode_layout(w):
     return info, rows, slot_oc
 
 
+@pytest.mark.parametrize("fmt", ["f32", "packed32"])
 @pytest.mark.parametrize("name", ["tiny", "tiny_int", "resnet3x3", "vgg3x3", "sweep90",
                                   "sweep99", "alex11x11", "conv5x5"])
-def test_packed_layout_decodes_to_csr(name):
+def test_packed_layout_decodes_to_csr(name, fmt):
     L = workloads.LAYERS[name]
     rowptr, colidx, value = workloads.make_weights(L)
-    w = _pack_host(L, rowptr, colidx, value)
+    if fmt == "packed32":  # the format stores FP16 values (round to nearest even)
+        value = value.astype(np.float16).astype(np.float32)
+    w = _pack_host(L, rowptr, colidx, value, fmt)
     info, rows, slot_oc = decode_layout(w)
     assert info["on_device"] == 0 and info["nnz"] == colidx.size == info["entries"]
     assert info["in_stage_bytes"] + info["blob_stage_bytes"] <= 110 * 1024
@@ -204,6 +224,21 @@ def _status_of(**kw):
         return 0
     except swd.SpconvError as e:
         return e.status
+
+
+def test_packed32_limits():
+    rowptr = np.array([0, 1], np.int32)
+    colidx, value = np.array([0], np.int32), np.array([1.0], np.float32)
+    with pytest.raises(swd.SpconvError) as e:
+        swd.pack_host(rowptr, colidx, value, C=1, H=40, W=40, M=1, R=17, S=3, stride=1, pad=1,
+                      fmt="packed32")
+    assert e.value.status == _lib.SPCONV_ERR_UNSUPPORTED
+    h = ctypes.c_void_p()
+    rc = _lib.lib().spconv_pack_ex(1, 5, 5, 1, 3, 3, 1, 1, rowptr.ctypes.data_as(ctypes.c_void_p),
+                                   colidx.ctypes.data_as(ctypes.c_void_p),
+                                   value.ctypes.data_as(ctypes.c_void_p), 9, 1, None,
+                                   ctypes.byref(h))
+    assert rc == _lib.SPCONV_ERR_INVALID_ARG
 
 
 def test_pack_validation():

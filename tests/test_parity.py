@@ -19,8 +19,9 @@ ATOL = 1e-7
 
 
 def run_gpu(x, rowptr, colidx, value, C, H, W, M, R, S, stride, pad, stream=None,
-            prefill=float("nan")):
-    w = swd.pack(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=R, S=S, stride=stride, pad=pad)
+            prefill=float("nan"), fmt="f32"):
+    w = swd.pack(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=R, S=S, stride=stride, pad=pad,
+                 fmt=fmt)
     xd = torch.from_numpy(np.ascontiguousarray(x)).cuda()
     E = swd.out_extent(H, R, stride, pad)
     F = swd.out_extent(W, S, stride, pad)
@@ -243,3 +244,21 @@ def test_p1_sweep_sampled(name):
     ref, mag = oracle.csr_points(x, rowptr, colidx, value, L.M, L.R, L.S, L.stride, L.pad, idx)
     check(got, ref, mag, what=name)
     w.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("integer", [False, True])
+@pytest.mark.parametrize("name", ["tiny", "resnet3x3", "vgg3x3", "sweep90", "sweep95",
+                                  "alex11x11", "conv5x5"])
+def test_packed32_format(name, integer):
+    """The first page's 32-bit packed words (FP16 values): parity against the
+    oracle on the FP16-rounded weights (round to nearest even, once)."""
+    import dataclasses
+    L = dataclasses.replace(workloads.LAYERS[name], integer=integer)
+    rowptr, colidx, value = workloads.make_weights(L)
+    x = workloads.make_input(L, min(L.N, 4))
+    v16 = value.astype(np.float16).astype(np.float32)
+    got = run_gpu(x, rowptr, colidx, value, L.C, L.H, L.W, L.M, L.R, L.S, L.stride, L.pad,
+                  fmt="packed32")
+    ref, mag = oracle.csr(x, rowptr, colidx, v16, L.M, L.R, L.S, L.stride, L.pad)
+    check(got, ref, mag, exact=integer, what=name + " packed32")
