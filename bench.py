@@ -40,7 +40,8 @@ UNIT = "µs/layer"
 FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 SM_COUNT_NOMINAL = 152
 FP32_LANES_PER_SM = 128
-KERNEL_SOURCE = os.path.join(ROOT, "sparse_weight_direct_gb300", "csrc", "spconv_fwd.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "sparse_weight_direct_gb300", "csrc", f)
+                  for f in ("spconv_kernel.cuh", "spconv_fwd.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
@@ -60,7 +61,7 @@ def fp32_peak_flops(sm_count: int, sm_mhz: float) -> float:
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for p in (KERNEL_SOURCE,):
+    for p in KERNEL_SOURCES:
         with open(p, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]

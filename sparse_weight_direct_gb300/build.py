@@ -1,8 +1,9 @@
 """Builds libspconv.so in-tree for sm_103a (GB300) with nvcc.
 
-Two translation units (the CUDA kernels and the host library) compile in
-parallel and link against the shared CUDA runtime, so the library and PyTorch
-share one runtime and one primary context.
+The translation units (the kernel instances, one per output-channels-per-warp
+count, the launcher and the host library) compile in parallel and link against
+the shared CUDA runtime, so the library and PyTorch share one runtime and one
+primary context.
 """
 from __future__ import annotations
 
@@ -17,8 +18,10 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspconv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["spconv_fwd.cu", "spconv_host.cpp"]
-HEADERS = [os.path.join(CSRC, "spconv_internal.h"), os.path.join(ROOT, "include", "spconv.h")]
+SOURCES = ["spconv_fwd.cu", "spconv_fwd_q1.cu", "spconv_fwd_q2.cu", "spconv_fwd_q4.cu",
+           "spconv_fwd_q8.cu", "spconv_host.cpp"]
+HEADERS = [os.path.join(CSRC, "spconv_internal.h"), os.path.join(CSRC, "spconv_kernel.cuh"),
+           os.path.join(ROOT, "include", "spconv.h")]
 
 
 def cuda_home() -> str:

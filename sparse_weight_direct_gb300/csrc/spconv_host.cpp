@@ -108,7 +108,7 @@ int validate_csr(int M, int64_t CRS, const int32_t *rowptr, const int32_t *colid
 
 // Tile shape and channel group size (everything but the chunking).
 int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, int stride,
-               int pad) {
+               int pad, int64_t nnz) {
     g.C = C; g.H = H; g.W = W; g.M = M; g.R = R; g.S = S; g.stride = stride; g.pad = pad;
     g.E = out_extent(H, R, stride, pad);
     g.F = out_extent(W, S, stride, pad);
@@ -142,13 +142,27 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     // grid, with the channels split over a full cluster, still gives ~1.5
     // blocks per SM (small layers trade per-warp reuse for parallelism)
     const int64_t spatial = (int64_t)g.tiles_y * g.tiles_x;
+    auto groups_of = [&](int Q) {
+        return (M + (int64_t)spconv::kWarps * Q - 1) / ((int64_t)spconv::kWarps * Q);
+    };
     g.slots = 1;
     for (int Q : {4, 2}) {
-        const int64_t groups = (M + (int64_t)spconv::kWarps * Q - 1) / ((int64_t)spconv::kWarps * Q);
-        if (spatial * groups * spconv::kMaxSplit * 2 >= (int64_t)kSMs * 3) {
+        if (spatial * groups_of(Q) * spconv::kMaxSplit * 2 >= (int64_t)kSMs * 3) {
             g.slots = Q;
             break;
         }
+    }
+    // Very sparse layers are bound by staging: every channel group re-stages
+    // the whole input.  Eight channels per warp halve the groups when there
+    // are many (>= 8 at four per warp) and the estimated staging time (L2 ->
+    // shared at ~7 TB/s) exceeds the compute time (the sparse path's ~18 % of
+    // fp32 peak), per image.
+    if (g.slots == 4 && groups_of(4) >= 8 &&
+        spatial * groups_of(8) * spconv::kMaxSplit * 2 >= (int64_t)kSMs * 3) {
+        const double staged = (double)groups_of(4) * spatial * g.plane * C * sizeof(float);
+        const double staging_s = staged / 7.0e12;
+        const double compute_s = 2.0 * nnz * g.E * g.F / (0.18 * kSMs * 128 * 2 * 2.07e9);
+        if (staging_s > compute_s) g.slots = 8;
     }
     g.groups = (M + spconv::kWarps * g.slots - 1) / (spconv::kWarps * g.slots);
     g.num_slots = g.groups * spconv::kWarps * g.slots;
@@ -174,7 +188,7 @@ int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx)
     const double crs = (double)g.C * g.R * g.S;
     auto nnz_of = [&](int m) { return (int64_t)rowptr[m + 1] - rowptr[m]; };
     std::vector<int> dense, sparse;
-    const bool can_dense = spconv::dense_taps_supported(g.R, g.S, g.stride, g.lane_rows);
+    const bool can_dense = spconv::dense_taps_supported(g.R, g.S, g.stride, g.lane_rows, g.slots);
     for (int m = 0; m < g.M; ++m)
         (can_dense && nnz_of(m) / crs >= kDenseRowMin ? dense : sparse).push_back(m);
     std::stable_sort(dense.begin(), dense.end(), [&](int a, int b) { return nnz_of(a) > nnz_of(b); });
@@ -187,8 +201,12 @@ int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx)
     std::stable_sort(sparse.begin(), sparse.end(), [&](int a, int b) { return nnz_of(a) > nnz_of(b); });
     const int gd = ((int)dense.size() + per_group - 1) / per_group;
 
-    // parts per sparse row: rows above the mean warp load are split
-    int gs = std::max(((int)sparse.size() + per_group - 1) / per_group, sparse.empty() ? 0 : 1);
+    // parts per sparse row: rows above the mean warp load are split.  With
+    // eight slots per warp a full group forces coarse warp loads, so those
+    // plans keep ~10 % of the slots free.
+    const int64_t want0 = g.slots >= 8 ? (int64_t)sparse.size() + (int64_t)sparse.size() / 10
+                                       : (int64_t)sparse.size();
+    int gs = std::max((int)((want0 + per_group - 1) / per_group), sparse.empty() ? 0 : 1);
     int64_t total = 0;
     for (int m : sparse) total += nnz_of(m);
     std::vector<int> parts(g.M, 1);
@@ -494,7 +512,7 @@ int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
     if (!P) return SPCONV_ERR_ALLOC;
     P->nnz = nnz;
     P->g.format = format;
-    st = plan_tiles(P->g, C, H, W, M, R, S, stride, pad);
+    st = plan_tiles(P->g, C, H, W, M, R, S, stride, pad, nnz);
     if (!st) st = build_layout(*P, rowptr, colidx, value);
     if (st) {
         delete P;

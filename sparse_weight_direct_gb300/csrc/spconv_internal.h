@@ -100,7 +100,7 @@ int forward_variant_supported(int S, int stride, int P, int Q, int LR);
 
 // Whether a layer shape can use the dense-tap path (output channels with dense
 // rows get their K x K blocks applied from a register window).
-bool dense_taps_supported(int R, int S, int stride, int LR);
+bool dense_taps_supported(int R, int S, int stride, int LR, int Q);
 
 // Launches the bounded-wait self-test (flags: bit 0 = the wait timed out,
 // bit 1 = it completed).  arrive = 0 leaves the barrier incomplete.

@@ -1,0 +1,577 @@
+// Internal: the forward kernel template and its device helpers, shared by the
+// per-Q translation units (spconv_fwd_q*.cu) and the launcher (spconv_fwd.cu).
+#pragma once
+// Forward kernel of the sparse-weight direct convolution (sm_103a).
+//
+// What it computes: Tuteja et al., "Theoretical and Empirical Analysis of
+// Sparse Convolution", Sec. 3 Eq.(3) -- each output is the sum, over the
+// nonzeros of its output channel, of value * input at the padding-shifted
+// position -- with stride (Escoin, arXiv 1802.10280, Algorithm 2).
+//
+// Work decomposition.  A block owns one output tile (P rows x 32 columns of one
+// image) and one group of 8 * Q output channels; a thread-block cluster of
+// `split` blocks shares the tile and splits the input-channel chunks between
+// them.  Per chunk, a pipeline stage holds
+//   * the input tile plus halo of the chunk's channels (Sec. 5.1 of the first
+//     page: each input region is read once per block and reused by all of the
+//     block's output channels and rows), fetched by one TMA tensor copy with
+//     hardware zero fill for the padding, or by cp.async where the input row
+//     stride is not 16-byte aligned; and
+//   * the chunk's weight blob of the block's channel group (a header of per-warp
+//     entry ranges, then 8-byte (value, offset) entries), fetched by one bulk
+//     asynchronous copy.
+// Both complete on the stage's mbarrier; two stages overlap copy and compute.
+// Each warp carries Q output channels; each lane owns one output column and P
+// rows in registers.  A warp walks its entries with 16-byte shared-memory
+// broadcasts (two entries per load) and does P FMAs per entry, reading
+// smem[lane + offset + p * row_step]: consecutive lanes read consecutive words,
+// so the reads are conflict free.  Offsets were precomputed per nonzero on the
+// host against this tile layout (Escoin's weight stretching).  With split > 1
+// the blocks of a cluster add their partial sums through distributed shared
+// memory in a fixed rank order (deterministic), then write back; otherwise the
+// accumulators are written directly (coalesced along the row, predicated for
+// partial tiles: Sec. 5.5 of the first page).
+#include <cooperative_groups.h>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <type_traits>
+
+#include "spconv_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace spconv {
+namespace kern {
+
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
+constexpr int kMaxDynamicSmem = 200 * 1024;                   // upper bound of any plan
+
+struct KParams {
+    const float *x;
+    float *y;
+    const float *bias;  // [M] or nullptr
+    int act;            // 0 identity, 1 ReLU
+    const unsigned char *blobs;
+    const uint32_t *blob_off;
+    const int *slot_oc;      // head slot -> output channel; -1 empty or a later part
+    const int *slot_next;    // next part of the same output channel (group-local), -1
+    const int *group_flags;  // per group: bit 0 dense-tap blobs, bit 1 split rows
+    unsigned int *err;
+    int N, C, H, W, M, E, F, stride, pad;
+    int tiles_y, tiles_x, in_rows, in_cols, shift, phase_pitch, row_pitch, plane;
+    int chunk, num_chunks, split, hdr_words, dense_mask_words;
+    int in_stage_bytes, stage_bytes, in_tma_bytes;
+    int use_tma;
+    int fmt;  // sparse entries: 0 = {fp32 value, int32 offset}, 1 = 32-bit packed word
+    int group_fast, groups;  // block order; number of groups
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+static __device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+static __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+static __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+static __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+static __device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+// Waits for the stage's phase with a time limit; false on timeout.
+static __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 0 && global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+static __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tmap, int x, int y,
+                                            int c, int n, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(c), "r"(n),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+static __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];\n" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+static __device__ __forceinline__ void cp_async_4(float *smem_dst, const float *gsrc, bool pred) {
+    const int src_size = pred ? 4 : 0;  // 0 -> the 4 destination bytes are zero-filled
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(src_size)
+                 : "memory");
+}
+static __device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+static __device__ __forceinline__ void cp_async_wait_all_but_one() {
+    asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+}
+static __device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+}
+
+// ---------------------------------------------------------------- staging
+
+// cp.async staging of channels [c0, c0 + cc) of image n: staged element
+// (channel cl, row, col) holds input (c0 + cl, iy0 + row, ix0 + col), zero
+// outside the image.  A thread owns fixed positions (row, col) of the staged
+// plane (its validity and both offsets do not depend on the channel) and walks
+// the chunk's channels for each, so the inner loop is two adds and a cp.async;
+// consecutive threads take consecutive columns (coalesced per channel).
+template <int ST_CT>
+static __device__ __forceinline__ void stage_input_cp_async(const KParams &p, float *buf, int n, int c0,
+                                                     int cc, int iy0, int ix0) {
+    const int st = ST_CT ? ST_CT : p.stride;
+    const int in_cols = p.in_cols;
+    const int plane_elems = p.in_rows * in_cols;
+    const size_t hw = (size_t)p.H * p.W;
+    const float *xc0 = p.x + ((size_t)n * p.C + c0) * hw;
+    const int T = blockDim.x;
+    int row = threadIdx.x / in_cols, col = threadIdx.x - row * in_cols;
+    const int drow = T / in_cols, dcol = T - drow * in_cols;
+    for (int e = threadIdx.x; e < plane_elems; e += T) {
+        const int gy = iy0 + row, gx = ix0 + col;
+        const bool ok = (unsigned)gy < (unsigned)p.H && (unsigned)gx < (unsigned)p.W;
+        const float *src = ok ? xc0 + (size_t)gy * p.W + gx : p.x;
+        const size_t src_step = ok ? hw : 0;
+        const int phys = (st == 1) ? col + p.shift : (col % st) * p.phase_pitch + col / st;
+        float *dst = buf + row * p.row_pitch + phys;
+        for (int cl = 0; cl < cc; ++cl) {
+            cp_async_4(dst, src, ok);
+            dst += p.plane;
+            src += src_step;
+        }
+        row += drow;
+        col += dcol;
+        if (col >= in_cols) {
+            col -= in_cols;
+            ++row;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- compute
+
+// Fused epilogue: bias, then the activation.
+static __device__ __forceinline__ float finish(const KParams &p, int m, float v) {
+    if (p.bias) v += __ldg(p.bias + m);
+    if (p.act == 1) v = fmaxf(v, 0.f);
+    return v;
+}
+
+// Kernel instances that carry the dense-tap path: stride 1, K x K with K = 3, 5.
+template <int S_CT, int ST_CT>
+constexpr bool kDenseTaps = ST_CT == 1 && (S_CT == 3 || S_CT == 5);
+
+template <int P, int ROW_STEP>
+static __device__ __forceinline__ void apply_entry(float (&acc)[P], const float *sb, float v, int off,
+                                            int row_step) {
+    const float *s = sb + off;
+#pragma unroll
+    for (int r = 0; r < P; ++r)
+        acc[r] = fmaf(v, s[r * (ROW_STEP ? ROW_STEP : row_step)], acc[r]);
+}
+
+template <int P, int ROW_STEP>
+static __device__ __forceinline__ void run_segment(float (&acc)[P], const float *sb, const float2 *ent,
+                                            int j, int j1, int row_step) {
+    if ((j & 1) && j < j1) {  // head: bring j to a 16-byte boundary
+        const float2 e = ent[j];
+        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
+        ++j;
+    }
+    for (; j + 1 < j1; j += 2) {
+        const float4 e = *reinterpret_cast<const float4 *>(ent + j);
+        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
+        apply_entry<P, ROW_STEP>(acc, sb, e.z, __float_as_int(e.w), row_step);
+    }
+    if (j < j1) {  // tail
+        const float2 e = ent[j];
+        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
+    }
+}
+
+// Dense-tap accumulation of one chunk for a warp of dense output channels: the
+// channel's input window (LR*(P-1)+K rows x K columns around this lane's output
+// column) is loaded into registers once and every tap of every slot of the
+// warp is applied to it with compile-time register indices.  The blob holds,
+// per (warp, channel), a mask of the slots with any nonzero in that channel
+// and, per (warp, channel, slot), the K*K weights (zeros included) padded to a
+// multiple of 4 floats.  Useful fraction = density of the channel's K x K
+// block; shared-memory reads per FMA drop by about the slot count.
+template <int P, int Q, int K, int LR, int RP>
+static __device__ __forceinline__ void run_dense_chunk(float (&acc)[Q][P], const float *sb,
+                                                const uint32_t *dmask, const float4 *dw,
+                                                int warp, int chunk, int cc, int plane) {
+    constexpr int WR = LR * (P - 1) + K;  // window rows
+    constexpr int KK4 = (K * K + 3) / 4;  // float4 per weight block
+    for (int cl = 0; cl < cc; ++cl) {
+        const uint32_t mask = dmask[warp * chunk + cl];
+        if (mask == 0) continue;
+        const float *s = sb + cl * plane;
+        float win[WR][K];
+#pragma unroll
+        for (int i = 0; i < WR; ++i)
+#pragma unroll
+            for (int j = 0; j < K; ++j) win[i][j] = s[i * RP + j];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            if (!(mask & (1u << q))) continue;
+            const float4 *wq = dw + ((size_t)(warp * chunk + cl) * Q + q) * KK4;
+            float w[KK4 * 4];
+#pragma unroll
+            for (int t = 0; t < KK4; ++t) {
+                const float4 v = wq[t];
+                w[4 * t] = v.x;
+                w[4 * t + 1] = v.y;
+                w[4 * t + 2] = v.z;
+                w[4 * t + 3] = v.w;
+            }
+#pragma unroll
+            for (int r = 0; r < K; ++r)
+#pragma unroll
+                for (int c = 0; c < K; ++c)
+#pragma unroll
+                    for (int pr = 0; pr < P; ++pr)
+                        acc[q][pr] = fmaf(w[r * K + c], win[LR * pr + r][c], acc[q][pr]);
+        }
+    }
+}
+
+// The first page's packed weight word (Tuteja et al., Sec. 5.3, Fig. 4):
+// [31:16] FP16 value, [15:8] input channel (here: within the chunk), [7:4]
+// kernel column px, [3:0] kernel row py.  The offset into the staged tile is
+// rebuilt from (channel, py, px) per entry.
+template <int P, int ROW_STEP, int ST_CT>
+static __device__ __forceinline__ void apply_word(float (&acc)[P], const float *sb, uint32_t w,
+                                           const KParams &p, int row_step) {
+    const float v = __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+    const int cl = (int)((w >> 8) & 0xffu), px = (int)((w >> 4) & 0xfu), py = (int)(w & 0xfu);
+    const int st = ST_CT ? ST_CT : p.stride;
+    const int col = (st == 1) ? px + p.shift : (px % st) * p.phase_pitch + px / st;
+    apply_entry<P, ROW_STEP>(acc, sb, v, cl * p.plane + py * p.row_pitch + col, row_step);
+}
+
+template <int P, int ROW_STEP, int ST_CT>
+static __device__ __forceinline__ void run_segment_words(float (&acc)[P], const float *sb,
+                                                  const uint32_t *ent, int j, int j1,
+                                                  const KParams &p, int row_step) {
+    for (; (j & 3) && j < j1; ++j)  // head: bring j to a 16-byte boundary
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, ent[j], p, row_step);
+    for (; j + 3 < j1; j += 4) {
+        const uint4 e = *reinterpret_cast<const uint4 *>(ent + j);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.x, p, row_step);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.y, p, row_step);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.z, p, row_step);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.w, p, row_step);
+    }
+    for (; j < j1; ++j) apply_word<P, ROW_STEP, ST_CT>(acc, sb, ent[j], p, row_step);  // tail
+}
+
+// P: output rows per lane; Q: output channels per warp; LR: lane rows (1, or 2
+// interleaved half-warps of 16 lanes for outputs at most 16 wide); S_CT/ST_CT:
+// kernel width and stride when known at compile time (0 = read from p).
+template <int P, int Q, int S_CT, int ST_CT, int LR>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    spconv_fwd_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap) {
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bar[2];
+    __shared__ int stage_done[2];  // warps that have released a stage (TMA path)
+    // stage buffers start on a 128-byte boundary (TMA destination)
+    unsigned char *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    constexpr int LC = kLanes / LR;  // lanes per lane row = output columns of a tile
+    constexpr int ROW_STEP =
+        S_CT ? LR * (ST_CT == 1 ? row_pitch_s1(S_CT, LR)
+                                : ST_CT * ST_CT * phase_pitch_for(S_CT, ST_CT))
+             : 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ly = lane / LC, lx = lane % LC;  // lane row / column of this thread
+    const int st = ST_CT ? ST_CT : p.stride;
+    const int row_step = LR * st * p.row_pitch;  // between this lane's output rows
+
+    // Block order (clusters run along x): channel-split rank fastest, then
+    // either the tile (groups in grid y: the heaviest groups, dense ones,
+    // start first) or, when the input does not fit in L2, the group (grid y =
+    // 1: all groups of a tile run together and share its input through L2).
+    const int split = p.split;
+    int b = blockIdx.x;
+    const int kr = b % split;
+    b /= split;
+    int group = blockIdx.y;
+    if (p.group_fast) {
+        group = b % p.groups;
+        b /= p.groups;
+    }
+    const int tx = b % p.tiles_x;
+    b /= p.tiles_x;
+    const int ty = b % p.tiles_y;
+    const int n = b / p.tiles_y;
+    const int gflags = p.group_flags[group];
+    const bool dense = (gflags & 1) != 0;
+    const bool has_parts = (gflags & 2) != 0;
+    const int k_begin = kr * p.num_chunks / split;
+    const int k_end = (kr + 1) * p.num_chunks / split;
+    const int iy0 = ty * (LR * P) * st - p.pad;
+    const int ix0 = tx * LC * st - p.pad;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        stage_done[0] = 0;
+        stage_done[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    }
+    __syncthreads();
+
+    // Enqueue chunk k into stage s.  `issuer` (one thread) arms the stage's
+    // mbarrier and issues the bulk copies; without TMA every thread also
+    // stages its share of the input with cp.async.
+    auto issue = [&](int k, int s, bool issuer) {
+        unsigned char *base = smem + (size_t)s * p.stage_bytes;
+        const int c0 = k * p.chunk;
+        if (issuer) {
+            const uint32_t o0 = p.blob_off[group * p.num_chunks + k];
+            const uint32_t o1 = p.blob_off[group * p.num_chunks + k + 1];
+            const uint32_t blob_bytes = (o1 - o0) * 16u;
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            mbar_expect_tx(&bar[s], blob_bytes + (p.use_tma ? (uint32_t)p.in_tma_bytes : 0u));
+            bulk_load(base + p.in_stage_bytes, p.blobs + (size_t)o0 * 16u, blob_bytes, &bar[s]);
+            if (p.use_tma) tma_load_4d(base, &tmap, ix0 - p.shift, iy0, c0, n, &bar[s]);
+        }
+        if (!p.use_tma) {
+            stage_input_cp_async<ST_CT>(p, reinterpret_cast<float *>(base), n, c0,
+                                        min(p.chunk, p.C - c0), iy0, ix0);
+            cp_async_commit();
+        }
+    };
+
+    float acc[Q][P];
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+#pragma unroll
+        for (int r = 0; r < P; ++r) acc[q][r] = 0.f;
+
+    const int nmine = k_end - k_begin;
+    bool failed = false;
+    if (nmine > 0) issue(k_begin, 0, threadIdx.x == 0);
+    if (nmine > 1) issue(k_begin + 1, 1, threadIdx.x == 0);
+    for (int it = 0; it < nmine && !failed; ++it) {
+        const int s = it & 1;
+        if (!p.use_tma) {
+            if (it + 1 < nmine)
+                cp_async_wait_all_but_one();
+            else
+                cp_async_wait_all();
+        }
+        const bool ok = mbar_wait_bounded(&bar[s], (uint32_t)((it >> 1) & 1));
+        if (p.use_tma) {
+            // warps run independently; a warp that timed out stops
+            failed = !ok;
+        } else {
+            failed = __syncthreads_or(!ok) != 0;  // cp.async data of all threads
+        }
+        if (failed) break;
+        const unsigned char *base = smem + (size_t)s * p.stage_bytes;
+        const float *sb = reinterpret_cast<const float *>(base) + ly * st * p.row_pitch + lx;
+        const uint32_t *hdr = reinterpret_cast<const uint32_t *>(base + p.in_stage_bytes);
+        if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4) {
+            if (dense) {
+                const int k = k_begin + it;
+                run_dense_chunk<P, Q, S_CT, LR, row_pitch_s1(S_CT, LR)>(
+                    acc, sb + p.shift, hdr, reinterpret_cast<const float4 *>(hdr + p.dense_mask_words),
+                    warp, p.chunk, min(p.chunk, p.C - k * p.chunk), p.plane);
+            }
+        }
+        if (!dense && p.fmt == 0) {
+            const float2 *ent = reinterpret_cast<const float2 *>(hdr + p.hdr_words);
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int j0 = (int)hdr[warp * Q + q];
+                const int j1 = (int)hdr[warp * Q + q + 1];
+                run_segment<P, ROW_STEP>(acc[q], sb, ent, j0, j1, row_step);
+            }
+        } else if (!dense) {
+            const uint32_t *ent = hdr + p.hdr_words;
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int j0 = (int)hdr[warp * Q + q];
+                const int j1 = (int)hdr[warp * Q + q + 1];
+                run_segment_words<P, ROW_STEP, ST_CT>(acc[q], sb, ent, j0, j1, p, row_step);
+            }
+        }
+        if (p.use_tma) {
+            // Release stage s without a block barrier: each warp counts itself
+            // out; the warp that completes the count refills the stage (its
+            // generic-proxy reads are ordered before the async-proxy copy by
+            // the fences).  Faster warps move on to the other stage.
+            if (it + 2 < nmine) {
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence_block();
+                    const int old = atomicAdd(&stage_done[s], 1);
+                    if (old == kWarps - 1) {
+                        stage_done[s] = 0;
+                        __threadfence_block();
+                        issue(k_begin + it + 2, s, true);
+                    }
+                }
+            }
+        } else {
+            __syncthreads();  // stage s is free again
+            if (it + 2 < nmine) issue(k_begin + it + 2, s, threadIdx.x == 0);
+        }
+    }
+    if (p.use_tma) __syncthreads();  // every warp is out of the pipeline
+    if (failed) {
+        if (!p.use_tma) cp_async_wait_all();
+        if (lane == 0) atomicOr(p.err, 1u);
+    }
+
+    const int nslot = kWarps * Q;
+    const int slot0 = group * nslot + warp * Q;
+    const int ox = tx * LC + lx;
+    const int oy0 = ty * (LR * P) + ly;  // this lane's output rows: oy0 + LR * r
+    if (split == 1 && !has_parts) {
+        if (failed || ox >= p.F) return;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const int m = p.slot_oc[slot0 + q];
+            if (m < 0) continue;
+            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
+#pragma unroll
+            for (int r = 0; r < P; ++r) {
+                const int oy = oy0 + LR * r;
+                if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, acc[q][r]);
+            }
+        }
+        return;
+    }
+
+    // ---- partial sums through shared memory: parts of split rows (summed in
+    // chain order) and/or the blocks of a channel-split cluster (summed in rank
+    // order, through distributed shared memory).  Both orders are fixed, so the
+    // result is deterministic.  The stage buffers are free: every issued copy
+    // has been consumed.
+    float *part = reinterpret_cast<float *>(smem);  // [warp * Q + q][P][32]
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+#pragma unroll
+        for (int r = 0; r < P; ++r) part[((warp * Q + q) * P + r) * 32 + lane] = acc[q][r];
+    if (split == 1) {
+        __syncthreads();
+        if (failed || ox >= p.F) return;
+        for (int q = 0; q < Q; ++q) {
+            const int sl = warp * Q + q;
+            const int m = p.slot_oc[group * nslot + sl];
+            if (m < 0) continue;
+            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
+            for (int r = 0; r < P; ++r) {
+                float sum = 0.f;
+                for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c])
+                    sum += part[(c * P + r) * 32 + lane];
+                const int oy = oy0 + LR * r;
+                if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, sum);
+            }
+        }
+        return;
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int s_begin = kr * nslot / split, s_end = (kr + 1) * nslot / split;
+    if (!failed && ox < p.F) {
+        for (int sl = s_begin + warp; sl < s_end; sl += kWarps) {
+            const int m = p.slot_oc[group * nslot + sl];
+            if (m < 0) continue;
+            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
+            for (int r = 0; r < P; ++r) {
+                float sum = 0.f;
+                for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c])
+                    for (int j = 0; j < split; ++j) {
+                        const float *rp = cluster.map_shared_rank(part, j);
+                        sum += rp[(c * P + r) * 32 + lane];
+                    }
+                const int oy = oy0 + LR * r;
+                if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, sum);
+            }
+        }
+    }
+    cluster.sync();  // partials stay readable until every block is done
+}
+
+using KernelFn = void (*)(const KParams, const CUtensorMap);
+
+// Instances of one output-channel-per-warp count Q (one translation unit each,
+// compiled in parallel): the kernel for (S, stride, P, LR), or nullptr.
+KernelFn pick_q1(int S, int stride, int P, int LR);
+KernelFn pick_q2(int S, int stride, int P, int LR);
+KernelFn pick_q4(int S, int stride, int P, int LR);
+KernelFn pick_q8(int S, int stride, int P, int LR);
+
+// Instantiates the kernels of one Q for the supported kernel widths, strides,
+// rows per lane and lane rows.
+template <int Q>
+KernelFn pick_instances(int S, int stride, int P, int LR) {
+    auto by_p = [&](auto pc) -> KernelFn {
+        constexpr int PP = decltype(pc)::value;
+        if (LR == 2) {
+            if (stride != 1) return nullptr;
+            if (S == 3) return spconv_fwd_kernel<PP, Q, 3, 1, 2>;
+            return spconv_fwd_kernel<PP, Q, 0, 1, 2>;
+        }
+        if (LR != 1) return nullptr;
+        if (S == 3 && stride == 1) return spconv_fwd_kernel<PP, Q, 3, 1, 1>;
+        if (S == 5 && stride == 1) return spconv_fwd_kernel<PP, Q, 5, 1, 1>;
+        if (S == 11 && stride == 4) return spconv_fwd_kernel<PP, Q, 11, 4, 1>;
+        if (stride == 1) return spconv_fwd_kernel<PP, Q, 0, 1, 1>;
+        return spconv_fwd_kernel<PP, Q, 0, 0, 1>;
+    };
+    switch (P) {
+        case 7: return by_p(std::integral_constant<int, 7>{});
+        case 8: return by_p(std::integral_constant<int, 8>{});
+        default: return nullptr;
+    }
+}
+
+}  // namespace kern
+}  // namespace spconv
