@@ -275,7 +275,7 @@ def run_ours(args, L):
 
     t0 = time.perf_counter()
     w = swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
-                 stride=L.stride, pad=L.pad, stream=stream, fmt=args.fmt)
+                 stride=L.stride, pad=L.pad, stream=stream, fmt=args.fmt, batch_hint=L.N)
     pack_ms = (time.perf_counter() - t0) * 1e3
     info = w.info()
 

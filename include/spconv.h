@@ -86,16 +86,21 @@ typedef enum spconv_format {
 } spconv_format;
 
 /*
- * spconv_pack_ex -- spconv_pack with a choice of entry format and of where
- * the handle lives.  format: spconv_format (PACKED32 rounds every weight to
- * FP16 once, round-to-nearest-even, and halves the sparse entry stream; dense
- * rows keep their FP16-rounded values as fp32).  host_only != 0: as
- * spconv_pack_host (no device work, stream ignored).  Errors as spconv_pack;
- * INVALID_ARG for an unknown format, UNSUPPORTED for PACKED32 with R or S > 16.
+ * spconv_pack_ex -- spconv_pack with a choice of entry format, a batch-size
+ * hint for the tiling plan, and of where the handle lives.
+ *   format      spconv_format (PACKED32 rounds every weight to FP16 once,
+ *               round-to-nearest-even, and halves the sparse entry stream;
+ *               dense rows keep their FP16-rounded values as fp32)
+ *   batch_hint  batch size the forwards will mostly use (0 = unknown).  It
+ *               only shapes the plan (output channels per warp, channel chunk
+ *               size); forwards accept any N either way.
+ *   host_only   != 0: as spconv_pack_host (no device work, stream ignored)
+ * Errors as spconv_pack; INVALID_ARG for an unknown format or a negative
+ * batch_hint, UNSUPPORTED for PACKED32 with R or S > 16.
  */
 int spconv_pack_ex(int C, int H, int W, int M, int R, int S, int stride, int pad,
                    const int32_t *rowptr, const int32_t *colidx, const float *value, int format,
-                   int host_only, void *stream, spconv_packed **out);
+                   int batch_hint, int host_only, void *stream, spconv_packed **out);
 
 /*
  * spconv_forward -- Y = conv(X, packed weights); the hot path.
@@ -206,7 +211,7 @@ typedef struct spconv_packed_info {
     int32_t dense_groups;     /* leading groups whose blobs are dense-tap       */
     int32_t dense_mask_words; /* words of a dense blob's slot masks            */
     int32_t format;           /* spconv_format of the sparse entries           */
-    int32_t reserved;
+    int32_t batch_hint;       /* batch size the plan targets (0 = unknown)     */
 } spconv_packed_info;
 
 int spconv_packed_info_get(const spconv_packed *p, spconv_packed_info *info);

@@ -106,31 +106,37 @@ def _ptr(a: np.ndarray):
 FORMATS = {"f32": 0, "packed32": 1}
 
 
-def _pack(rowptr, colidx, value, C, H, W, M, R, S, stride, pad, fmt, host_only, stream):
+def _pack(rowptr, colidx, value, C, H, W, M, R, S, stride, pad, fmt, batch_hint, host_only,
+          stream):
     rowptr, colidx, value = _csr_arrays(rowptr, colidx, value)
     if rowptr.size != M + 1:
         raise SpconvError(_lib.SPCONV_ERR_INVALID_ARG, "rowptr must have M + 1 entries")
     h = ctypes.c_void_p()
     _lib.check(_lib.lib().spconv_pack_ex(C, H, W, M, R, S, stride, pad, _ptr(rowptr),
                                          _ptr(colidx), _ptr(value), FORMATS[fmt],
-                                         1 if host_only else 0,
+                                         int(batch_hint), 1 if host_only else 0,
                                          None if host_only else _stream_ptr(stream),
                                          ctypes.byref(h)), "spconv_pack_ex")
     return PackedWeights(h, dict(C=C, H=H, W=W, M=M, R=R, S=S, stride=stride, pad=pad))
 
 
 def pack(rowptr, colidx, value, *, C: int, H: int, W: int, M: int, R: int, S: int,
-         stride: int = 1, pad: int = 0, stream=None, fmt: str = "f32") -> PackedWeights:
+         stride: int = 1, pad: int = 0, stream=None, fmt: str = "f32",
+         batch_hint: int = 0) -> PackedWeights:
     """CSR (host arrays) -> packed device layout on the current CUDA device.
     fmt: "f32" (fp32 values, precomputed offsets) or "packed32" (the first
-    page's 32-bit words with FP16 values)."""
-    return _pack(rowptr, colidx, value, C, H, W, M, R, S, stride, pad, fmt, False, stream)
+    page's 32-bit words with FP16 values).  batch_hint: the batch size the
+    forwards will mostly use (0 = unknown); it only shapes the tiling plan."""
+    return _pack(rowptr, colidx, value, C, H, W, M, R, S, stride, pad, fmt, batch_hint, False,
+                 stream)
 
 
 def pack_host(rowptr, colidx, value, *, C: int, H: int, W: int, M: int, R: int, S: int,
-              stride: int = 1, pad: int = 0, fmt: str = "f32") -> PackedWeights:
+              stride: int = 1, pad: int = 0, fmt: str = "f32",
+              batch_hint: int = 0) -> PackedWeights:
     """The same packing kept in host memory only (inspection; needs no GPU)."""
-    return _pack(rowptr, colidx, value, C, H, W, M, R, S, stride, pad, fmt, True, None)
+    return _pack(rowptr, colidx, value, C, H, W, M, R, S, stride, pad, fmt, batch_hint, True,
+                 None)
 
 
 def _stream_ptr(stream):

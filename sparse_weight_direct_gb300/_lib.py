@@ -51,7 +51,7 @@ class PackedInfo(ctypes.Structure):
         ("device_bytes", "smem_bytes", "max_warp_nnz", "mean_warp_nnz")] + [
         (n, ctypes.c_int32) for n in
         ("hdr_words", "blob_stage_bytes", "in_stage_bytes", "lane_rows", "dense_groups",
-         "dense_mask_words", "format", "reserved")]
+         "dense_mask_words", "format", "batch_hint")]
 
 
 def lib() -> ctypes.CDLL:
@@ -70,7 +70,8 @@ def lib() -> ctypes.CDLL:
         L.spconv_pack.restype = i
         L.spconv_pack_host.argtypes = [i] * 8 + [p, p, p, ctypes.POINTER(ctypes.c_void_p)]
         L.spconv_pack_host.restype = i
-        L.spconv_pack_ex.argtypes = [i] * 8 + [p, p, p, i, i, p, ctypes.POINTER(ctypes.c_void_p)]
+        L.spconv_pack_ex.argtypes = [i] * 8 + [p, p, p, i, i, i, p,
+                                               ctypes.POINTER(ctypes.c_void_p)]
         L.spconv_pack_ex.restype = i
         L.spconv_forward.argtypes = [i] * 9 + [p, p, p, p]
         L.spconv_forward.restype = i

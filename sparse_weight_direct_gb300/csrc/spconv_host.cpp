@@ -141,7 +141,8 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     // output channels per warp: the largest Q in {4, 2, 1} whose one-image
     // grid, with the channels split over a full cluster, still gives ~1.5
     // blocks per SM (small layers trade per-warp reuse for parallelism)
-    const int64_t spatial = (int64_t)g.tiles_y * g.tiles_x;
+    // blocks of one launch per channel group, at the planned batch size
+    const int64_t spatial = (int64_t)g.tiles_y * g.tiles_x * std::max(1, g.batch_hint);
     auto groups_of = [&](int Q) {
         return (M + (int64_t)spconv::kWarps * Q - 1) / ((int64_t)spconv::kWarps * Q);
     };
@@ -159,7 +160,7 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     // fp32 peak), per image.
     if (g.slots == 4 && groups_of(4) >= 8 &&
         spatial * groups_of(8) * spconv::kMaxSplit * 2 >= (int64_t)kSMs * 3) {
-        const double staged = (double)groups_of(4) * spatial * g.plane * C * sizeof(float);
+        const double staged = (double)groups_of(4) * g.tiles_y * g.tiles_x * g.plane * C * sizeof(float);
         const double staging_s = staged / 7.0e12;
         const double compute_s = 2.0 * nnz * g.E * g.F / (0.18 * kSMs * 128 * 2 * 2.07e9);
         if (staging_s > compute_s) g.slots = 8;
@@ -339,13 +340,22 @@ size_t dense_blob_bytes(const spconv::Geometry &g, int chunk) {
 int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
     // gpre[(group) * (C + 1) + c]: entries of the group in channels [0, c)
     const int C = g.C;
-    const int64_t base_blocks = (int64_t)g.tiles_y * g.tiles_x * g.groups;
-    int want_split = (int)std::min<int64_t>(spconv::kMaxSplit,
-                                            (2 * kSMs + base_blocks - 1) / std::max<int64_t>(base_blocks, 1));
+    const int64_t base_blocks =
+        (int64_t)g.tiles_y * g.tiles_x * g.groups * std::max(1, g.batch_hint);
+    int want_split = base_blocks >= kSMs
+                         ? 1
+                         : (int)std::min<int64_t>(spconv::kMaxSplit,
+                                                  (2 * kSMs + base_blocks - 1) / base_blocks);
     want_split = std::max(want_split, 1);
     int cap = std::min(C, 256);  // TMA box extent limit
     if (want_split > 1 && C / want_split >= 32)
         cap = std::min(cap, (C + want_split - 1) / want_split);
+    // When the planned launch (known batch size) splits the chunks over a
+    // cluster with one chunk per block, a single stage is enough: allow it up
+    // to 200 KB (larger batches of the same plan then run two stages, one
+    // block per SM).
+    const bool one_per_block =
+        g.batch_hint > 0 && want_split > 1 && (int64_t)cap * want_split >= C;
     const size_t hdr_bytes = (size_t)g.hdr_words * 4;
     for (int chunk = cap; chunk >= 1; --chunk) {
         const int nch = (C + chunk - 1) / chunk;
@@ -362,7 +372,9 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
         }
         const size_t stage = in_stage + round_up(blob_max, 128);
         const size_t total = (nch > 1 ? 2 : 1) * stage + 128;
-        if (total <= kSmemBudget || (chunk == 1 && total <= 200 * 1024)) {
+        const bool fits_split = one_per_block && chunk * want_split >= C &&
+                                2 * stage + 128 <= 200 * 1024;
+        if (total <= kSmemBudget || fits_split || (chunk == 1 && total <= 200 * 1024)) {
             g.chunk = chunk;
             g.num_chunks = nch;
             g.dense_mask_words = (int)round_up((size_t)g.warps * chunk, 4);
@@ -497,10 +509,11 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
 
 int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
                 const int32_t *rowptr, const int32_t *colidx, const float *value, int format,
-                spconv_packed **out) {
+                int batch_hint, spconv_packed **out) {
     if (!out) return SPCONV_ERR_INVALID_ARG;
     if (format != SPCONV_FORMAT_F32 && format != SPCONV_FORMAT_PACKED32)
         return SPCONV_ERR_INVALID_ARG;
+    if (batch_hint < 0) return SPCONV_ERR_INVALID_ARG;
     int st = validate_shape(C, H, W, M, R, S, stride, pad);
     if (st) return st;
     if (format == SPCONV_FORMAT_PACKED32 && (R > 16 || S > 16)) return SPCONV_ERR_UNSUPPORTED;
@@ -512,6 +525,7 @@ int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
     if (!P) return SPCONV_ERR_ALLOC;
     P->nnz = nnz;
     P->g.format = format;
+    P->g.batch_hint = batch_hint > 0 ? batch_hint : 0;
     st = plan_tiles(P->g, C, H, W, M, R, S, stride, pad, nnz);
     if (!st) st = build_layout(*P, rowptr, colidx, value);
     if (st) {
@@ -660,11 +674,12 @@ extern "C" {
 
 __attribute__((visibility("default"))) int spconv_pack_ex(
     int C, int H, int W, int M, int R, int S, int stride, int pad, const int32_t *rowptr,
-    const int32_t *colidx, const float *value, int format, int host_only, void *stream,
-    spconv_packed **out) {
+    const int32_t *colidx, const float *value, int format, int batch_hint, int host_only,
+    void *stream, spconv_packed **out) {
     try {
         spconv_packed *P = nullptr;
-        int st = make_handle(C, H, W, M, R, S, stride, pad, rowptr, colidx, value, format, &P);
+        int st = make_handle(C, H, W, M, R, S, stride, pad, rowptr, colidx, value, format,
+                             batch_hint, &P);
         if (st) return st;
         if (!host_only) {
             st = upload(P, static_cast<cudaStream_t>(stream));
@@ -684,14 +699,14 @@ __attribute__((visibility("default"))) int spconv_pack_host(
     int C, int H, int W, int M, int R, int S, int stride, int pad, const int32_t *rowptr,
     const int32_t *colidx, const float *value, spconv_packed **out) {
     return spconv_pack_ex(C, H, W, M, R, S, stride, pad, rowptr, colidx, value, SPCONV_FORMAT_F32,
-                          1, nullptr, out);
+                          0, 1, nullptr, out);
 }
 
 __attribute__((visibility("default"))) int spconv_pack(
     int C, int H, int W, int M, int R, int S, int stride, int pad, const int32_t *rowptr,
     const int32_t *colidx, const float *value, void *stream, spconv_packed **out) {
     return spconv_pack_ex(C, H, W, M, R, S, stride, pad, rowptr, colidx, value, SPCONV_FORMAT_F32,
-                          0, stream, out);
+                          0, 0, stream, out);
 }
 
 __attribute__((visibility("default"))) int spconv_forward_ex(
@@ -846,6 +861,7 @@ __attribute__((visibility("default"))) int spconv_packed_info_get(const spconv_p
     info->in_stage_bytes = (int32_t)g.in_stage_bytes;
     info->dense_groups = g.dense_groups;
     info->format = g.format;
+    info->batch_hint = g.batch_hint;
     info->dense_mask_words = g.dense_mask_words;
     return SPCONV_OK;
 }

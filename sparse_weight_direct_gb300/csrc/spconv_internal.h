@@ -78,6 +78,7 @@ struct Geometry {
     int groups;       // output-channel groups (grid y)
     int num_slots;    // groups * warps * slots
     int format;       // sparse entries: 0 = {fp32, int32 offset}, 1 = 32-bit packed word
+    int batch_hint;   // batch size the plan targets (0 = unknown)
     int hdr_words;    // words of a sparse blob header (warps * slots + 1, to 4)
     int dense_groups; // leading groups whose blobs are dense-tap (0 if none)
     int dense_mask_words;  // words of a dense blob's slot masks (warps * chunk, to 4)

@@ -237,7 +237,7 @@ def test_packed32_limits():
     h = ctypes.c_void_p()
     rc = _lib.lib().spconv_pack_ex(1, 5, 5, 1, 3, 3, 1, 1, rowptr.ctypes.data_as(ctypes.c_void_p),
                                    colidx.ctypes.data_as(ctypes.c_void_p),
-                                   value.ctypes.data_as(ctypes.c_void_p), 9, 1, None,
+                                   value.ctypes.data_as(ctypes.c_void_p), 9, 0, 1, None,
                                    ctypes.byref(h))
     assert rc == _lib.SPCONV_ERR_INVALID_ARG
 

@@ -19,9 +19,9 @@ ATOL = 1e-7
 
 
 def run_gpu(x, rowptr, colidx, value, C, H, W, M, R, S, stride, pad, stream=None,
-            prefill=float("nan"), fmt="f32"):
+            prefill=float("nan"), fmt="f32", batch_hint=0):
     w = swd.pack(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=R, S=S, stride=stride, pad=pad,
-                 fmt=fmt)
+                 fmt=fmt, batch_hint=batch_hint)
     xd = torch.from_numpy(np.ascontiguousarray(x)).cuda()
     E = swd.out_extent(H, R, stride, pad)
     F = swd.out_extent(W, S, stride, pad)
@@ -45,10 +45,12 @@ def check(got, ref, mag, exact=False, what=""):
                              f"abs_sum={mag[tuple(i)]!r}")
 
 
-def layer_case(L, N=None):
+def layer_case(L, N=None, batch_hint=None):
     rowptr, colidx, value = workloads.make_weights(L)
     x = workloads.make_input(L, N)
-    got = run_gpu(x, rowptr, colidx, value, L.C, L.H, L.W, L.M, L.R, L.S, L.stride, L.pad)
+    hint = L.N if batch_hint is None else batch_hint
+    got = run_gpu(x, rowptr, colidx, value, L.C, L.H, L.W, L.M, L.R, L.S, L.stride, L.pad,
+                  batch_hint=hint)
     ref, mag = oracle.csr(x, rowptr, colidx, value, L.M, L.R, L.S, L.stride, L.pad)
     check(got, ref, mag, exact=L.integer, what=L.name)
     return got, ref, mag
@@ -57,8 +59,18 @@ def layer_case(L, N=None):
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", list(workloads.LAYERS))
 def test_layer_full_size(name):
-    """Every seeded layer at its full size (the benchmark's launch shape)."""
+    """Every seeded layer at its full size, planned for its batch as bench.py
+    plans it (the benchmark's launch configuration)."""
     layer_case(workloads.LAYERS[name])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["resnet3x3", "vgg3x3", "sweep99", "conv5x5"])
+@pytest.mark.parametrize("hint", [0, 1, 32])
+def test_plan_independent_of_batch_hint(name, hint):
+    """Any plan (batch hint unknown, too small or too large for the launch)
+    computes the same convolution."""
+    layer_case(workloads.LAYERS[name], N=min(workloads.LAYERS[name].N, 4), batch_hint=hint)
 
 
 @pytest.mark.gpu
@@ -232,7 +244,7 @@ def test_p1_sweep_sampled(name):
     rowptr, colidx, value = workloads.make_weights(L)
     x = workloads.make_input(L)
     w = swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
-                 stride=L.stride, pad=L.pad)
+                 stride=L.stride, pad=L.pad, batch_hint=L.N)
     xd = torch.from_numpy(x).cuda()
     out = torch.full((L.N, L.M, L.E, L.F), float("nan"), device="cuda")
     swd.forward(xd, w, out=out)
