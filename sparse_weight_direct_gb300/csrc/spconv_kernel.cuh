@@ -520,20 +520,28 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     cluster.sync();
     const int s_begin = kr * nslot / split, s_end = (kr + 1) * nslot / split;
     if (!failed && ox < p.F) {
-        for (int sl = s_begin + warp; sl < s_end; sl += kWarps) {
+        // (slot, output row) items spread over all warps; the ranks' partials
+        // of one item are loaded back to back, then added in rank order
+        const int items = (s_end - s_begin) * P;
+        for (int item = warp; item < items; item += kWarps) {
+            const int sl = s_begin + item / P, r = item % P;
             const int m = p.slot_oc[group * nslot + sl];
             if (m < 0) continue;
-            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
-            for (int r = 0; r < P; ++r) {
-                float sum = 0.f;
-                for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c])
-                    for (int j = 0; j < split; ++j) {
-                        const float *rp = cluster.map_shared_rank(part, j);
-                        sum += rp[(c * P + r) * 32 + lane];
-                    }
-                const int oy = oy0 + LR * r;
-                if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, sum);
+            float sum = 0.f;
+            for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c]) {
+                float v[kMaxSplit];
+#pragma unroll
+                for (int j = 0; j < kMaxSplit; ++j)
+                    v[j] = j < split ? cluster.map_shared_rank(part, j)[(c * P + r) * 32 + lane]
+                                     : 0.f;
+#pragma unroll
+                for (int j = 0; j < kMaxSplit; ++j)
+                    if (j < split) sum += v[j];
             }
+            const int oy = oy0 + LR * r;
+            if (oy < p.E)
+                p.y[((size_t)n * p.M + m) * p.E * p.F + (size_t)oy * p.F + ox] =
+                    finish(p, m, sum);
         }
     }
     cluster.sync();  // partials stay readable until every block is done
