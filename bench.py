@@ -40,8 +40,12 @@ UNIT = "µs/layer"
 FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 SM_COUNT_NOMINAL = 152
 FP32_LANES_PER_SM = 128
+# Everything that decides what one launch does: the kernel, its instances and
+# the planner that picks the tiling (a plan change changes the traffic too).
 KERNEL_SOURCES = [os.path.join(ROOT, "sparse_weight_direct_gb300", "csrc", f)
-                  for f in ("spconv_kernel.cuh", "spconv_fwd.cu")]
+                  for f in ("spconv_kernel.cuh", "spconv_fwd.cu", "spconv_fwd_q1.cu",
+                            "spconv_fwd_q2.cu", "spconv_fwd_q4.cu", "spconv_fwd_q8.cu",
+                            "spconv_ws.cu", "spconv_host.cpp", "spconv_internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
@@ -356,17 +360,17 @@ def run_ours(args, L):
         achieved = num["alg_bytes"] / (us_kernel * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": bw / 1e9, "unit": "GB/s",
                 "frac": achieved / (bw / 1e9), "peak_source": f"hbm_gbs ({peak_kind})"}
-    traffic = recorded_traffic(L.name)
+    traffic = recorded_traffic(L.name if args.fmt == "f32" else f"{L.name}:{args.fmt}")
     roof["traffic"] = traffic
     roof["algorithmic"] = num["alg_bytes"]
-    roof["kernel"] = "spconv_fwd_kernel"
+    roof["kernel"] = "spconv_ws_kernel" if args.fmt == "ws" else "spconv_fwd_kernel"
     roof["roofline_us"] = max(t_comp, t_comm) * 1e6
 
     line = {
         "metric": METRIC, "value": us_layer, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if args.fmt == "f32" else "f32 (fp16 weights)", "data": "synthetic",
+        "dtype": "f32 (fp16 weights)" if args.fmt == "packed32" else "f32", "data": "synthetic",
         "config": {**describe(L), "weight_format": args.fmt},
         "dense_equiv_tflops": num["dense_flop"] / (us_kernel * 1e-6) / 1e12,
         "useful_gflops": num["useful_flop"] / (us_kernel * 1e-6) / 1e9,
@@ -448,8 +452,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default=workloads.BENCH_DEFAULT,
                     choices=sorted(workloads.ALL_LAYERS))
-    ap.add_argument("--fmt", default="f32", choices=["f32", "packed32"],
-                    help="packed weight format (packed32: the first page's 32-bit words, FP16)")
+    ap.add_argument("--fmt", default="f32", choices=["f32", "packed32", "ws"],
+                    help="packed weight format (packed32: the first page's 32-bit words, "
+                         "FP16; ws: the weight-stationary mapping, one output channel per "
+                         "block)")
     ap.add_argument("--compare-dense", action="store_true",
                     help="also time PyTorch's dense conv2d (cuDNN) on the same layer")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -80,9 +80,16 @@ int spconv_pack(int C, int H, int W, int M, int R, int S, int stride, int pad,
 /* Packed weight formats of spconv_pack_ex. */
 typedef enum spconv_format {
     SPCONV_FORMAT_F32 = 0,      /* 8-byte entries: fp32 value + int32 precomputed offset    */
-    SPCONV_FORMAT_PACKED32 = 1  /* 4-byte words of the first page's Sec. 5.3 / Fig. 4:      */
+    SPCONV_FORMAT_PACKED32 = 1, /* 4-byte words of the first page's Sec. 5.3 / Fig. 4:      */
                                 /* [31:16] FP16 value, [15:8] input channel (within the     */
                                 /* chunk), [7:4] kernel column, [3:0] kernel row; R, S <= 16 */
+    SPCONV_FORMAT_WS = 2        /* weight-stationary mapping of Escoin (arXiv 1802.10280),  */
+                                /* Figs. 5-7: one output channel per thread block, its      */
+                                /* entries staged in shared memory, the input read in place */
+                                /* through the read-only cache.  8-byte entries {fp32 value, */
+                                /* uint32 word = off << 8 | r << 4 | s} with the stretched   */
+                                /* offset off = c*H*W + r*W + s; R, S <= 16 and             */
+                                /* C*H*W + R*W + S <= 2^24; forwards take N <= 65535         */
 } spconv_format;
 
 /*
@@ -96,7 +103,9 @@ typedef enum spconv_format {
  *               size); forwards accept any N either way.
  *   host_only   != 0: as spconv_pack_host (no device work, stream ignored)
  * Errors as spconv_pack; INVALID_ARG for an unknown format or a negative
- * batch_hint, UNSUPPORTED for PACKED32 with R or S > 16.
+ * batch_hint, UNSUPPORTED for PACKED32 or WS with R or S > 16 and for WS with
+ * C*H*W + R*W + S > 2^24.  spconv_forward(_ex) on a WS handle runs the
+ * weight-stationary kernel and returns UNSUPPORTED for N > 65535.
  */
 int spconv_pack_ex(int C, int H, int W, int M, int R, int S, int stride, int pad,
                    const int32_t *rowptr, const int32_t *colidx, const float *value, int format,
@@ -214,6 +223,11 @@ typedef struct spconv_packed_info {
     int32_t batch_hint;       /* batch size the plan targets (0 = unknown)     */
 } spconv_packed_info;
 
+/* For a SPCONV_FORMAT_WS handle: tile_rows, lane_rows, tile_cols, tiles_y and
+ * tiles_x describe one block's output tile (warps * lane_rows * tile_rows rows
+ * of tile_cols columns); chunk = entries per pipeline stage, num_chunks = the
+ * most stages of any row; max_warp_nnz / mean_warp_nnz = the longest / mean
+ * row (one row per block); the input-staging fields are 0. */
 int spconv_packed_info_get(const spconv_packed *p, spconv_packed_info *info);
 
 /* Which host-side array spconv_packed_copy_array copies. */
@@ -230,6 +244,12 @@ typedef enum spconv_array {
                                /* 16-byte units                                     */
     SPCONV_ARRAY_SLOT_OC = 2,  /* int32 [num_slots]: output channel of a head slot,  */
                                /* -1 for empty slots and later parts of split rows */
+                               /* SPCONV_FORMAT_WS instead: BLOBS = the entries of  */
+                               /* every row in column order, each row starting on an */
+                               /* even entry; BLOB_OFF = uint32 [2 * M] (first entry, */
+                               /* entry count) of row m; SLOT_OC = int32 [M] the row */
+                               /* of each block column (heaviest first); SLOT_NEXT   */
+                               /* and GROUP_FLAGS are empty                          */
     SPCONV_ARRAY_SLOT_NEXT = 3,/* int32 [num_slots]: group-local slot of the next   */
                                /* part of the same output channel, or -1            */
     SPCONV_ARRAY_GROUP_FLAGS = 4 /* int32 [groups]: bit 0 dense-tap blobs, bit 1    */

@@ -103,7 +103,7 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-FORMATS = {"f32": 0, "packed32": 1}
+FORMATS = {"f32": 0, "packed32": 1, "ws": 2}
 
 
 def _pack(rowptr, colidx, value, C, H, W, M, R, S, stride, pad, fmt, batch_hint, host_only,
@@ -124,9 +124,11 @@ def pack(rowptr, colidx, value, *, C: int, H: int, W: int, M: int, R: int, S: in
          stride: int = 1, pad: int = 0, stream=None, fmt: str = "f32",
          batch_hint: int = 0) -> PackedWeights:
     """CSR (host arrays) -> packed device layout on the current CUDA device.
-    fmt: "f32" (fp32 values, precomputed offsets) or "packed32" (the first
-    page's 32-bit words with FP16 values).  batch_hint: the batch size the
-    forwards will mostly use (0 = unknown); it only shapes the tiling plan."""
+    fmt: "f32" (fp32 values, precomputed offsets), "packed32" (the first page's
+    32-bit words with FP16 values) or "ws" (weight-stationary: one output channel
+    per block, input read in place; Escoin, Figs. 5-7).  batch_hint: the batch
+    size the forwards will mostly use (0 = unknown); it only shapes the tiling
+    plan."""
     return _pack(rowptr, colidx, value, C, H, W, M, R, S, stride, pad, fmt, batch_hint, False,
                  stream)
 

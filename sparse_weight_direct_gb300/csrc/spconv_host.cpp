@@ -386,20 +386,24 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
     return SPCONV_ERR_UNSUPPORTED;
 }
 
+// A column given twice in one row is malformed CSR.
+int check_duplicates(int M, const int32_t *rowptr, const int32_t *colidx) {
+    std::vector<int32_t> cols;
+    for (int m = 0; m < M; ++m) {
+        cols.assign(colidx + rowptr[m], colidx + rowptr[m + 1]);
+        std::sort(cols.begin(), cols.end());
+        if (std::adjacent_find(cols.begin(), cols.end()) != cols.end()) return SPCONV_ERR_BAD_CSR;
+    }
+    return SPCONV_OK;
+}
+
 // Builds the host arrays of a handle.  Returns a status.
 int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
                  const float *value) {
     spconv::Geometry &g = P.g;
     const int RS = g.R * g.S;
     // duplicate columns are rejected before anything else
-    {
-        std::vector<int32_t> cols;
-        for (int m = 0; m < g.M; ++m) {
-            cols.assign(colidx + rowptr[m], colidx + rowptr[m + 1]);
-            std::sort(cols.begin(), cols.end());
-            if (std::adjacent_find(cols.begin(), cols.end()) != cols.end()) return SPCONV_ERR_BAD_CSR;
-        }
-    }
+    if (int st = check_duplicates(g.M, rowptr, colidx)) return st;
     int bst = bin_channels(P, rowptr, colidx);
     if (bst) return bst;
     const std::vector<std::vector<int64_t>> &order = P.slot_entries;
@@ -507,16 +511,116 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
     return SPCONV_OK;
 }
 
+// ---- weight-stationary format (Escoin, arXiv 1802.10280, Figs. 5-7: one
+// output channel per thread block, its weights kept on chip, the input read
+// in place through the read-only cache, one output per thread position)
+
+constexpr int64_t kWsMaxOffset = (int64_t)1 << 24;  // stretched offsets fit 24 bits
+constexpr int kWsMaxPiece = 4096;                   // entries per stage (32 KB)
+
+// Tile of one block: 32 / LR columns, 8 warps x LR lane rows x P rows.
+int plan_ws(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, int stride, int pad,
+            const int32_t *rowptr) {
+    g.C = C; g.H = H; g.W = W; g.M = M; g.R = R; g.S = S; g.stride = stride; g.pad = pad;
+    g.E = out_extent(H, R, stride, pad);
+    g.F = out_extent(W, S, stride, pad);
+    g.lane_rows = g.F <= 16 ? 2 : 1;
+    const int rows_per_step = spconv::kWarps * g.lane_rows;
+    g.tile_w = spconv::kLanes / g.lane_rows;
+    g.tiles_x = (g.F + g.tile_w - 1) / g.tile_w;
+    // fewest tiles of at most 8 rows per lane, then the smallest instance P
+    // that covers the layer's rows with that many tiles
+    const int ty = (g.E + rows_per_step * 8 - 1) / (rows_per_step * 8);
+    const int need = (g.E + ty * rows_per_step - 1) / (ty * rows_per_step);
+    static const int kP[] = {1, 2, 4, 7, 8};
+    g.tile_rows = 8;
+    for (int cand : kP)
+        if (cand >= need) {
+            g.tile_rows = cand;
+            break;
+        }
+    if (!spconv::ws_variant_supported(g.tile_rows, g.lane_rows)) return SPCONV_ERR_UNSUPPORTED;
+    g.tile_h = rows_per_step * g.tile_rows;
+    g.tiles_y = (g.E + g.tile_h - 1) / g.tile_h;
+    if ((int64_t)g.tiles_y * g.tiles_x > 65535) return SPCONV_ERR_UNSUPPORTED;
+    int64_t longest = 0;
+    for (int m = 0; m < M; ++m) longest = std::max<int64_t>(longest, rowptr[m + 1] - rowptr[m]);
+    g.chunk = (int)std::min<int64_t>(kWsMaxPiece, std::max<int64_t>(2, round_up(longest, 2)));
+    g.num_chunks = (int)std::max<int64_t>(1, (longest + g.chunk - 1) / g.chunk);
+    g.warps = spconv::kWarps;
+    g.slots = 1;
+    g.groups = 0;
+    g.num_slots = M;
+    return SPCONV_OK;
+}
+
+// Row m's entries in column order, each {value, off << 8 | r << 4 | s} with
+// off = c*H*W + r*W + s (weight stretching against the input tensor itself);
+// every row starts on an even entry (16 bytes) and the array ends on one.
+int build_layout_ws(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
+                    const float *value) {
+    spconv::Geometry &g = P.g;
+    if (int st = check_duplicates(g.M, rowptr, colidx)) return st;
+    const int RS = g.R * g.S;
+    const int64_t HW = (int64_t)g.H * g.W;
+    std::vector<HostEntry> ent;
+    ent.reserve((size_t)P.nnz + 2 * (size_t)g.M + 2);
+    P.blob_off.assign(2 * (size_t)g.M, 0);
+    std::vector<int64_t> order;
+    for (int m = 0; m < g.M; ++m) {
+        const int64_t j0 = rowptr[m], j1 = rowptr[m + 1];
+        order.assign((size_t)(j1 - j0), 0);
+        std::iota(order.begin(), order.end(), j0);
+        std::sort(order.begin(), order.end(),
+                  [&](int64_t a, int64_t b) { return colidx[a] < colidx[b]; });
+        P.blob_off[2 * (size_t)m] = (uint32_t)ent.size();
+        P.blob_off[2 * (size_t)m + 1] = (uint32_t)(j1 - j0);
+        for (int64_t j : order) {
+            const int col = colidx[j];
+            const int c = col / RS, r = (col % RS) / g.S, s = col % g.S;
+            const int64_t off = c * HW + (int64_t)r * g.W + s;
+            HostEntry e;
+            e.value = value[j];
+            e.off = (int32_t)(((uint32_t)off << 8) | ((uint32_t)r << 4) | (uint32_t)s);
+            ent.push_back(e);
+        }
+        if (ent.size() & 1) ent.push_back(HostEntry{0.f, 0});
+    }
+    if (ent.empty()) ent.push_back(HostEntry{0.f, 0});
+    if (ent.size() & 1) ent.push_back(HostEntry{0.f, 0});
+    if (ent.size() >= ((size_t)1 << 32)) return SPCONV_ERR_UNSUPPORTED;
+    P.blobs.resize(ent.size() * sizeof(HostEntry));
+    std::memcpy(P.blobs.data(), ent.data(), P.blobs.size());
+    // heaviest rows first: the hardware hands out blocks in grid order
+    P.slot_oc.resize(g.M);
+    std::iota(P.slot_oc.begin(), P.slot_oc.end(), 0);
+    std::stable_sort(P.slot_oc.begin(), P.slot_oc.end(), [&](int a, int b) {
+        return rowptr[a + 1] - rowptr[a] > rowptr[b + 1] - rowptr[b];
+    });
+    P.slot_next.clear();
+    P.group_flags.clear();
+    int64_t longest = 0;
+    for (int m = 0; m < g.M; ++m) longest = std::max<int64_t>(longest, rowptr[m + 1] - rowptr[m]);
+    P.max_warp_nnz = longest;
+    P.mean_warp_nnz = g.M ? P.nnz / g.M : 0;
+    return SPCONV_OK;
+}
+
 int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
                 const int32_t *rowptr, const int32_t *colidx, const float *value, int format,
                 int batch_hint, spconv_packed **out) {
     if (!out) return SPCONV_ERR_INVALID_ARG;
-    if (format != SPCONV_FORMAT_F32 && format != SPCONV_FORMAT_PACKED32)
+    if (format != SPCONV_FORMAT_F32 && format != SPCONV_FORMAT_PACKED32 &&
+        format != SPCONV_FORMAT_WS)
         return SPCONV_ERR_INVALID_ARG;
     if (batch_hint < 0) return SPCONV_ERR_INVALID_ARG;
     int st = validate_shape(C, H, W, M, R, S, stride, pad);
     if (st) return st;
-    if (format == SPCONV_FORMAT_PACKED32 && (R > 16 || S > 16)) return SPCONV_ERR_UNSUPPORTED;
+    if ((format == SPCONV_FORMAT_PACKED32 || format == SPCONV_FORMAT_WS) && (R > 16 || S > 16))
+        return SPCONV_ERR_UNSUPPORTED;
+    if (format == SPCONV_FORMAT_WS &&
+        (int64_t)C * H * W + (int64_t)R * W + S > kWsMaxOffset)
+        return SPCONV_ERR_UNSUPPORTED;
     int64_t nnz = 0;
     st = validate_csr(M, (int64_t)C * R * S, rowptr, colidx, value, &nnz);
     if (st) return st;
@@ -526,8 +630,13 @@ int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
     P->nnz = nnz;
     P->g.format = format;
     P->g.batch_hint = batch_hint > 0 ? batch_hint : 0;
-    st = plan_tiles(P->g, C, H, W, M, R, S, stride, pad, nnz);
-    if (!st) st = build_layout(*P, rowptr, colidx, value);
+    if (format == SPCONV_FORMAT_WS) {
+        st = plan_ws(P->g, C, H, W, M, R, S, stride, pad, rowptr);
+        if (!st) st = build_layout_ws(*P, rowptr, colidx, value);
+    } else {
+        st = plan_tiles(P->g, C, H, W, M, R, S, stride, pad, nnz);
+        if (!st) st = build_layout(*P, rowptr, colidx, value);
+    }
     if (st) {
         delete P;
         return st;
@@ -556,18 +665,16 @@ int upload(spconv_packed *P, cudaStream_t stream) {
     ok = ok && (P->blobs.empty() ||
                 cudaMemcpyAsync(base, P->blobs.data(), P->blobs.size(), cudaMemcpyHostToDevice,
                                 stream) == cudaSuccess);
-    ok = ok && cudaMemcpyAsync(base + b_blobs, P->blob_off.data(),
-                               P->blob_off.size() * sizeof(uint32_t), cudaMemcpyHostToDevice,
-                               stream) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(base + b_blobs + b_off, P->slot_oc.data(),
-                               P->slot_oc.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
-                               stream) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(base + b_blobs + b_off + b_slot, P->slot_next.data(),
-                               P->slot_next.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
-                               stream) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(base + b_blobs + b_off + b_slot + b_next, P->group_flags.data(),
-                               P->group_flags.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
-                               stream) == cudaSuccess;
+    auto put = [&](size_t at, const void *src, size_t bytes) {
+        return bytes == 0 || cudaMemcpyAsync(base + at, src, bytes, cudaMemcpyHostToDevice,
+                                             stream) == cudaSuccess;
+    };
+    ok = ok && put(b_blobs, P->blob_off.data(), P->blob_off.size() * sizeof(uint32_t));
+    ok = ok && put(b_blobs + b_off, P->slot_oc.data(), P->slot_oc.size() * sizeof(int32_t));
+    ok = ok && put(b_blobs + b_off + b_slot, P->slot_next.data(),
+                   P->slot_next.size() * sizeof(int32_t));
+    ok = ok && put(b_blobs + b_off + b_slot + b_next, P->group_flags.data(),
+                   P->group_flags.size() * sizeof(int32_t));
     ok = ok && cudaStreamSynchronize(stream) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
@@ -733,6 +840,16 @@ __attribute__((visibility("default"))) int spconv_forward_ex(
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return SPCONV_ERR_CUDA;
     if (dev != packed->device) return SPCONV_ERR_MISMATCH;
+    if (g.format == SPCONV_FORMAT_WS) {
+        if (N > 65535) return SPCONV_ERR_UNSUPPORTED;  // images run along grid z
+        cudaError_t e = spconv::launch_forward_ws(g, N, input, output, bias, act, packed->d,
+                                                  static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return SPCONV_ERR_CUDA;
+        }
+        return SPCONV_OK;
+    }
     try {
         CUtensorMap tmp;
         const CUtensorMap *tmap = input_tmap(packed, input, N, tmp);
@@ -853,7 +970,8 @@ __attribute__((visibility("default"))) int spconv_packed_info_get(const spconv_p
     info->num_slots = g.num_slots;
     info->on_device = p->dev_block ? 1 : 0;
     info->device_bytes = (int64_t)p->dev_bytes;
-    info->smem_bytes = (int64_t)spconv::forward_smem_bytes(g, 1);
+    info->smem_bytes = (int64_t)(g.format == SPCONV_FORMAT_WS ? spconv::ws_smem_bytes(g)
+                                                               : spconv::forward_smem_bytes(g, 1));
     info->max_warp_nnz = p->max_warp_nnz;
     info->mean_warp_nnz = p->mean_warp_nnz;
     info->hdr_words = g.hdr_words;

@@ -71,13 +71,15 @@ struct Geometry {
     int phase_pitch;  // words of one stride-phase sub-row
     int row_pitch;    // words of one staged row
     int plane;        // words of one staged channel (in_rows * row_pitch)
-    int chunk;        // channels staged per pipeline stage
-    int num_chunks;
+    int chunk;        // channels staged per pipeline stage (weight-stationary
+                      // format: entries per stage)
+    int num_chunks;   // (weight-stationary format: most stages of any row)
     int slots;        // Q: output channels a warp carries at once
     int warps;        // warps per block
     int groups;       // output-channel groups (grid y)
     int num_slots;    // groups * warps * slots
-    int format;       // sparse entries: 0 = {fp32, int32 offset}, 1 = 32-bit packed word
+    int format;       // 0 = {fp32, int32 offset} entries, 1 = 32-bit packed words,
+                      // 2 = weight-stationary rows (one output channel per block)
     int batch_hint;   // batch size the plan targets (0 = unknown)
     int hdr_words;    // words of a sparse blob header (warps * slots + 1, to 4)
     int dense_groups; // leading groups whose blobs are dense-tap (0 if none)
@@ -119,5 +121,15 @@ size_t forward_smem_bytes(const Geometry &g, int split);
 cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast, const float *x,
                            float *y, const float *bias, int act, const DeviceArrays &d,
                            const CUtensorMap *tmap, cudaStream_t stream);
+
+// Weight-stationary format (one output channel per block, input read in
+// place): whether (P, LR) has an instance, the dynamic shared memory of a
+// launch, and the launcher (N <= 65535).  d.blobs holds the row entries,
+// d.blob_off the [2 * M] (first entry, count) pairs, d.slot_oc the row order.
+bool ws_variant_supported(int P, int LR);
+size_t ws_smem_bytes(const Geometry &g);
+cudaError_t launch_forward_ws(const Geometry &g, int N, const float *x, float *y,
+                              const float *bias, int act, const DeviceArrays &d,
+                              cudaStream_t stream);
 
 }  // namespace spconv

@@ -353,6 +353,29 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int k_end = (kr + 1) * p.num_chunks / split;
     const int iy0 = ty * (LR * P) * st - p.pad;
     const int ix0 = tx * LC * st - p.pad;
+    const int nmine = k_end - k_begin;
+    const int nslot = kWarps * Q;
+
+    // Loads that nothing computed here feeds, issued before any wait so that
+    // their latency overlaps the pipeline: the first blobs' offsets (issuing
+    // thread) and the output channel (+ chain link) of this warp's first
+    // output item.
+    uint32_t pre_off[3] = {0u, 0u, 0u};
+    if (threadIdx.x == 0 && nmine > 0) {
+        const uint32_t *bo = p.blob_off + group * p.num_chunks + k_begin;
+        pre_off[0] = bo[0];
+        pre_off[1] = bo[1];
+        if (nmine > 1) pre_off[2] = bo[2];
+    }
+    const int item0_slot =
+        split == 1 ? warp * Q : kr * nslot / split + warp / P;  // first item's slot
+    const bool item0_valid =
+        split == 1 ? true : warp < ((kr + 1) * nslot / split - kr * nslot / split) * P;
+    int pre_m = -1, pre_next = -1;
+    if (item0_valid) {
+        pre_m = p.slot_oc[group * nslot + item0_slot];
+        if (has_parts || split > 1) pre_next = p.slot_next[group * nslot + item0_slot];
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(&bar[0], 1);
@@ -371,8 +394,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         unsigned char *base = smem + (size_t)s * p.stage_bytes;
         const int c0 = k * p.chunk;
         if (issuer) {
-            const uint32_t o0 = p.blob_off[group * p.num_chunks + k];
-            const uint32_t o1 = p.blob_off[group * p.num_chunks + k + 1];
+            const int i = k - k_begin;
+            const uint32_t o0 = i < 2 ? pre_off[i] : p.blob_off[group * p.num_chunks + k];
+            const uint32_t o1 = i < 2 ? pre_off[i + 1] : p.blob_off[group * p.num_chunks + k + 1];
             const uint32_t blob_bytes = (o1 - o0) * 16u;
             asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
             mbar_expect_tx(&bar[s], blob_bytes + (p.use_tma ? (uint32_t)p.in_tma_bytes : 0u));
@@ -392,7 +416,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 #pragma unroll
         for (int r = 0; r < P; ++r) acc[q][r] = 0.f;
 
-    const int nmine = k_end - k_begin;
     bool failed = false;
     if (nmine > 0) issue(k_begin, 0, threadIdx.x == 0);
     if (nmine > 1) issue(k_begin + 1, 1, threadIdx.x == 0);
@@ -468,7 +491,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (lane == 0) atomicOr(p.err, 1u);
     }
 
-    const int nslot = kWarps * Q;
     const int slot0 = group * nslot + warp * Q;
     const int ox = tx * LC + lx;
     const int oy0 = ty * (LR * P) + ly;  // this lane's output rows: oy0 + LR * r
@@ -476,7 +498,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (failed || ox >= p.F) return;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
-            const int m = p.slot_oc[slot0 + q];
+            const int m = q == 0 ? pre_m : p.slot_oc[slot0 + q];
             if (m < 0) continue;
             float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
 #pragma unroll
@@ -503,12 +525,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (failed || ox >= p.F) return;
         for (int q = 0; q < Q; ++q) {
             const int sl = warp * Q + q;
-            const int m = p.slot_oc[group * nslot + sl];
+            const int m = q == 0 ? pre_m : p.slot_oc[group * nslot + sl];
             if (m < 0) continue;
+            const int next0 = q == 0 ? pre_next : p.slot_next[group * nslot + sl];
             float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
             for (int r = 0; r < P; ++r) {
-                float sum = 0.f;
-                for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c])
+                float sum = part[(sl * P + r) * 32 + lane];
+                for (int c = next0; c >= 0; c = p.slot_next[group * nslot + c])
                     sum += part[(c * P + r) * 32 + lane];
                 const int oy = oy0 + LR * r;
                 if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, sum);
@@ -525,10 +548,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         const int items = (s_end - s_begin) * P;
         for (int item = warp; item < items; item += kWarps) {
             const int sl = s_begin + item / P, r = item % P;
-            const int m = p.slot_oc[group * nslot + sl];
+            const bool first = item == warp;
+            const int m = first ? pre_m : p.slot_oc[group * nslot + sl];
             if (m < 0) continue;
             float sum = 0.f;
-            for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c]) {
+            for (int c = sl, next = first ? pre_next : p.slot_next[group * nslot + sl]; c >= 0;
+                 c = next, next = c >= 0 ? p.slot_next[group * nslot + c] : -1) {
                 float v[kMaxSplit];
 #pragma unroll
                 for (int j = 0; j < kMaxSplit; ++j)
