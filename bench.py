@@ -40,12 +40,18 @@ UNIT = "µs/layer"
 FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 SM_COUNT_NOMINAL = 152
 FP32_LANES_PER_SM = 128
-# Everything that decides what one launch does: the kernel, its instances and
-# the planner that picks the tiling (a plan change changes the traffic too).
-KERNEL_SOURCES = [os.path.join(ROOT, "sparse_weight_direct_gb300", "csrc", f)
-                  for f in ("spconv_kernel.cuh", "spconv_fwd.cu", "spconv_fwd_q1.cu",
-                            "spconv_fwd_q2.cu", "spconv_fwd_q4.cu", "spconv_fwd_q8.cu",
-                            "spconv_ws.cu", "spconv_host.cpp", "spconv_internal.h")]
+# Everything that decides what one launch of a kernel does: the kernel, its
+# instances and the planner that picks the tiling (a plan change changes the
+# traffic too).  One list per kernel, so a change to one leaves the other's
+# recorded traffic valid.
+_CSRC = os.path.join(ROOT, "sparse_weight_direct_gb300", "csrc")
+KERNEL_SOURCES = {
+    "spconv_fwd_kernel": [os.path.join(_CSRC, f) for f in (
+        "spconv_kernel.cuh", "spconv_fwd.cu", "spconv_fwd_q1.cu", "spconv_fwd_q2.cu",
+        "spconv_fwd_q4.cu", "spconv_fwd_q8.cu", "spconv_host.cpp", "spconv_internal.h")],
+    "spconv_ws_kernel": [os.path.join(_CSRC, f) for f in (
+        "spconv_kernel.cuh", "spconv_ws.cu", "spconv_host.cpp", "spconv_internal.h")],
+}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
@@ -63,20 +69,20 @@ def fp32_peak_flops(sm_count: int, sm_mhz: float) -> float:
     return sm_count * FP32_LANES_PER_SM * 2.0 * sm_mhz * 1e6
 
 
-def kernel_sha() -> str:
+def kernel_sha(kernel: str = "spconv_fwd_kernel") -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in KERNEL_SOURCES[kernel]:
         with open(p, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
 
 
-def recorded_traffic(config: str):
+def recorded_traffic(config: str, kernel: str = "spconv_fwd_kernel"):
     """DRAM bytes per launch from an ncu capture of this exact kernel source,
     or None (no capture, or the kernel changed since)."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    sha = kernel_sha()
+    sha = kernel_sha(kernel)
     with open(TRAFFIC_FILE) as fh:
         for line in fh:
             parts = line.split()
@@ -360,10 +366,11 @@ def run_ours(args, L):
         achieved = num["alg_bytes"] / (us_kernel * 1e-6) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": bw / 1e9, "unit": "GB/s",
                 "frac": achieved / (bw / 1e9), "peak_source": f"hbm_gbs ({peak_kind})"}
-    traffic = recorded_traffic(L.name if args.fmt == "f32" else f"{L.name}:{args.fmt}")
+    kname = "spconv_ws_kernel" if args.fmt == "ws" else "spconv_fwd_kernel"
+    traffic = recorded_traffic(L.name if args.fmt == "f32" else f"{L.name}:{args.fmt}", kname)
     roof["traffic"] = traffic
     roof["algorithmic"] = num["alg_bytes"]
-    roof["kernel"] = "spconv_ws_kernel" if args.fmt == "ws" else "spconv_fwd_kernel"
+    roof["kernel"] = kname
     roof["roofline_us"] = max(t_comp, t_comm) * 1e6
 
     line = {
