@@ -221,6 +221,9 @@ typedef struct spconv_packed_info {
     int32_t dense_mask_words; /* words of a dense blob's slot masks            */
     int32_t format;           /* spconv_format of the sparse entries           */
     int32_t batch_hint;       /* batch size the plan targets (0 = unknown)     */
+    int32_t blob_stride;      /* bytes between consecutive blobs when they are  */
+                              /* stored at a fixed stride (nearly equal sizes,  */
+                              /* each padded to the largest), else 0            */
 } spconv_packed_info;
 
 /* For a SPCONV_FORMAT_WS handle: tile_rows, lane_rows, tile_cols, tiles_y and
@@ -229,6 +232,26 @@ typedef struct spconv_packed_info {
  * most stages of any row; max_warp_nnz / mean_warp_nnz = the longest / mean
  * row (one row per block); the input-staging fields are 0. */
 int spconv_packed_info_get(const spconv_packed *p, spconv_packed_info *info);
+
+/* How spconv_forward would launch for a batch of N images (host logic only;
+ * no device work).  TMA staging also needs the input pointer's tensor map to
+ * encode, which this query does not try. */
+typedef struct spconv_launch_info {
+    int32_t kernel;          /* 0: tiled kernel, 1: weight-stationary kernel     */
+    int32_t grid_x, grid_y, grid_z;
+    int32_t block_threads;
+    int32_t cluster;         /* blocks per cluster splitting the channel chunks  */
+    int32_t push;            /* 1: the cluster reduces by remote stores into the */
+                             /* owning block (one cluster barrier), 0: by remote */
+                             /* reads (two barriers) or no cluster              */
+    int32_t group_fast;      /* 1: all channel groups of a tile run together     */
+    int32_t tma;             /* 1: input staged by TMA tensor copies             */
+    int64_t smem_bytes;      /* dynamic shared memory per block                  */
+} spconv_launch_info;
+
+/* Fills *info for a forward of N >= 1 images with handle p.  INVALID_ARG (NULL,
+ * N < 1), UNSUPPORTED (a grid spconv_forward would reject). */
+int spconv_launch_info_get(const spconv_packed *p, int N, spconv_launch_info *info);
 
 /* Which host-side array spconv_packed_copy_array copies. */
 typedef enum spconv_array {

@@ -53,6 +53,14 @@ class PackedWeights:
                    "spconv_packed_info_get")
         return {name: getattr(info, name) for name, _ in _lib.PackedInfo._fields_}
 
+    def launch_info(self, N: int) -> dict:
+        """How a forward of N images would launch (grid, cluster size, reduction
+        mode, shared memory, staging path, kernel); host logic only."""
+        info = _lib.LaunchInfo()
+        _lib.check(_lib.lib().spconv_launch_info_get(self.handle, int(N), ctypes.byref(info)),
+                   "spconv_launch_info_get")
+        return {name: getattr(info, name) for name, _ in _lib.LaunchInfo._fields_}
+
     def array(self, which: str) -> np.ndarray:
         """Copy of a packed host array: 'blobs' (raw bytes), 'blob_off'
         (uint32, 16-byte units), 'slot_oc', 'slot_next' or 'group_flags' (int32)."""

@@ -26,7 +26,7 @@ SPCONV_ERR_DEVICE = -7
 EXPORTS = ("spconv_pack", "spconv_pack_ex", "spconv_forward", "spconv_forward_ex", "spconv_packed_free",
            "spconv_status_string",
            "spconv_pack_host", "spconv_device_status", "spconv_selftest_wait",
-           "spconv_packed_info_get", "spconv_packed_copy_array")
+           "spconv_packed_info_get", "spconv_launch_info_get", "spconv_packed_copy_array")
 
 _lock = threading.Lock()
 _lib = None
@@ -51,7 +51,13 @@ class PackedInfo(ctypes.Structure):
         ("device_bytes", "smem_bytes", "max_warp_nnz", "mean_warp_nnz")] + [
         (n, ctypes.c_int32) for n in
         ("hdr_words", "blob_stage_bytes", "in_stage_bytes", "lane_rows", "dense_groups",
-         "dense_mask_words", "format", "batch_hint")]
+         "dense_mask_words", "format", "batch_hint", "blob_stride")]
+
+
+class LaunchInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("kernel", "grid_x", "grid_y", "grid_z", "block_threads", "cluster", "push",
+                 "group_fast", "tma")] + [("smem_bytes", ctypes.c_int64)]
 
 
 def lib() -> ctypes.CDLL:
@@ -83,6 +89,8 @@ def lib() -> ctypes.CDLL:
         L.spconv_status_string.restype = ctypes.c_char_p
         L.spconv_packed_info_get.argtypes = [p, ctypes.POINTER(PackedInfo)]
         L.spconv_packed_info_get.restype = i
+        L.spconv_launch_info_get.argtypes = [p, i, ctypes.POINTER(LaunchInfo)]
+        L.spconv_launch_info_get.restype = i
         L.spconv_packed_copy_array.argtypes = [p, i, p, ctypes.c_int64,
                                                ctypes.POINTER(ctypes.c_int64)]
         L.spconv_packed_copy_array.restype = i

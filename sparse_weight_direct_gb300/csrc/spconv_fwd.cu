@@ -80,9 +80,33 @@ int forward_variant_supported(int S, int stride, int P, int Q, int LR) {
     return pick(S, stride, P, Q, LR) ? 0 : -1;
 }
 
-size_t forward_smem_bytes(const Geometry &g, int split) {
+// Shared memory of the stage buffers a block with `split` cluster ranks uses.
+static size_t stages_bytes(const Geometry &g, int split) {
     const int per_block = (g.num_chunks + split - 1) / split;
-    size_t bytes = (size_t)(per_block > 1 ? 2 : 1) * stage_bytes(g);
+    return (size_t)(per_block > 1 ? 2 : 1) * stage_bytes(g);
+}
+
+// Receive buffer of the push-mode cluster reduction: [rank][owned slot][P][32].
+static size_t recv_bytes(const Geometry &g, int split) {
+    const int nslot = g.warps * g.slots;
+    return (size_t)split * ((nslot + split - 1) / split) * g.tile_rows * 32 * sizeof(float);
+}
+
+void forward_grid(const Geometry &g, int N, int split, bool group_fast, unsigned *gx,
+                  unsigned *gy) {
+    const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x * split;
+    *gx = (unsigned)(group_fast ? tiles * g.groups : tiles);
+    *gy = group_fast ? 1u : (unsigned)g.groups;
+}
+
+bool push_reduction(const Geometry &g, int split) {
+    return split > 1 && !g.split_rows &&
+           stages_bytes(g, split) + recv_bytes(g, split) + 128 <= (size_t)kern::kMaxDynamicSmem;
+}
+
+size_t forward_smem_bytes(const Geometry &g, int split) {
+    size_t bytes = stages_bytes(g, split);
+    if (push_reduction(g, split)) return bytes + recv_bytes(g, split) + 128;
     // room for the partial sums of split rows / a channel-split cluster
     const size_t part = (size_t)g.warps * g.slots * g.tile_rows * 32 * sizeof(float);
     if (part > bytes) bytes = part;
@@ -123,6 +147,9 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
     p.in_tma_bytes = g.chunk * g.plane * (int)sizeof(float);
     p.use_tma = tmap ? 1 : 0;
     p.fmt = g.format;
+    p.blob_stride16 = (uint32_t)g.blob_stride16;
+    p.push = push_reduction(g, split) ? 1 : 0;
+    p.recv_off = (int)stages_bytes(g, split);
     CUtensorMap dummy;
     if (!tmap) {
         for (int i = 0; i < 16; ++i) dummy.opaque[i] = 0;
@@ -132,11 +159,9 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
     cudaLaunchConfig_t cfg = {};
     p.groups = g.groups;
     p.group_fast = group_fast ? 1 : 0;
-    const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x * split;
-    if (p.group_fast)
-        cfg.gridDim = dim3((unsigned)(tiles * g.groups), 1, 1);
-    else
-        cfg.gridDim = dim3((unsigned)tiles, (unsigned)g.groups, 1);
+    unsigned gx = 0, gy = 0;
+    forward_grid(g, N, split, group_fast, &gx, &gy);
+    cfg.gridDim = dim3(gx, gy, 1);
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

@@ -311,7 +311,10 @@ int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx)
                 std::vector<int64_t> &mine = P.slot_entries[slot];
                 for (size_t t = k; t < idx.size(); t += ps.size()) mine.push_back(idx[t]);
             }
-            if (ps.size() > 1) P.group_flags[grp] |= 2;
+            if (ps.size() > 1) {
+                P.group_flags[grp] |= 2;
+                g.split_rows = 1;
+            }
         }
         for (int w = 0; w < g.warps; ++w) {
             mx = std::max(mx, load[w]);
@@ -422,21 +425,34 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
 
     // blobs, in (group, chunk) order
     const int nch = g.num_chunks;
-    P.blob_off.assign((size_t)g.groups * nch + 1, 0);
-    size_t total = 0;
+    const size_t nblobs = (size_t)g.groups * nch;
+    std::vector<size_t> bsize(nblobs);
+    size_t total = 0, largest = 0;
     for (int grp = 0; grp < g.groups; ++grp) {
         const int64_t *pre = &gpre[(size_t)grp * (g.C + 1)];
         for (int k = 0; k < nch; ++k) {
             const int c0 = k * g.chunk, c1 = std::min(g.C, c0 + g.chunk);
-            P.blob_off[(size_t)grp * nch + k] = (uint32_t)(total / 16);
-            if (P.group_flags[grp] & 1)
-                total += dense_blob_bytes(g, g.chunk);
-            else
-                total += (size_t)g.hdr_words * 4 +
-                         round_up((size_t)(pre[c1] - pre[c0]) * entry_bytes(g), 16);
+            size_t b = (P.group_flags[grp] & 1)
+                           ? dense_blob_bytes(g, g.chunk)
+                           : (size_t)g.hdr_words * 4 +
+                                 round_up((size_t)(pre[c1] - pre[c0]) * entry_bytes(g), 16);
+            bsize[(size_t)grp * nch + k] = b;
+            total += b;
+            largest = std::max(largest, b);
         }
     }
-    P.blob_off[(size_t)g.groups * nch] = (uint32_t)(total / 16);
+    // Nearly equal blobs are stored at a fixed stride (each padded to the
+    // largest): a block then finds its blob without first reading blob_off,
+    // one dependent global load less before its first stage can start.
+    g.blob_stride16 = (largest * nblobs <= total + total / 4) ? (int)(largest / 16) : 0;
+    P.blob_off.assign(nblobs + 1, 0);
+    size_t at = 0;
+    for (size_t b = 0; b < nblobs; ++b) {
+        P.blob_off[b] = (uint32_t)(at / 16);
+        at += g.blob_stride16 ? largest : bsize[b];
+    }
+    total = at;
+    P.blob_off[nblobs] = (uint32_t)(total / 16);
     if (total / 16 >= ((size_t)1 << 32)) return SPCONV_ERR_UNSUPPORTED;
     P.blobs.assign(total, 0);
     const int kk4 = (int)round_up((size_t)RS, 4);
@@ -981,6 +997,40 @@ __attribute__((visibility("default"))) int spconv_packed_info_get(const spconv_p
     info->format = g.format;
     info->batch_hint = g.batch_hint;
     info->dense_mask_words = g.dense_mask_words;
+    info->blob_stride = g.blob_stride16 * 16;
+    return SPCONV_OK;
+}
+
+__attribute__((visibility("default"))) int spconv_launch_info_get(const spconv_packed *p, int N,
+                                                                  spconv_launch_info *info) {
+    if (!p || !info || N < 1) return SPCONV_ERR_INVALID_ARG;
+    const spconv::Geometry &g = p->g;
+    std::memset(info, 0, sizeof(*info));
+    info->block_threads = spconv::kWarps * 32;
+    if (g.format == SPCONV_FORMAT_WS) {
+        if (N > 65535) return SPCONV_ERR_UNSUPPORTED;
+        info->kernel = 1;
+        info->grid_x = g.M;
+        info->grid_y = g.tiles_y * g.tiles_x;
+        info->grid_z = N;
+        info->cluster = 1;
+        info->smem_bytes = (int64_t)spconv::ws_smem_bytes(g);
+        return SPCONV_OK;
+    }
+    const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x * spconv::kMaxSplit * g.groups;
+    if (tiles > 0x7fffffffLL) return SPCONV_ERR_UNSUPPORTED;
+    const int split = choose_split(g, N);
+    const bool group_fast = choose_group_fast(g, N, p->nnz);
+    unsigned gx = 0, gy = 0;
+    spconv::forward_grid(g, N, split, group_fast, &gx, &gy);
+    info->grid_x = (int32_t)gx;
+    info->grid_y = (int32_t)gy;
+    info->grid_z = 1;
+    info->cluster = split;
+    info->push = spconv::push_reduction(g, split) ? 1 : 0;
+    info->group_fast = group_fast ? 1 : 0;
+    info->tma = tma_eligible(g) ? 1 : 0;
+    info->smem_bytes = (int64_t)spconv::forward_smem_bytes(g, split);
     return SPCONV_OK;
 }
 

@@ -83,7 +83,9 @@ struct Geometry {
     int batch_hint;   // batch size the plan targets (0 = unknown)
     int hdr_words;    // words of a sparse blob header (warps * slots + 1, to 4)
     int dense_groups; // leading groups whose blobs are dense-tap (0 if none)
+    int split_rows;   // 1 if any group has rows split into parts (bit 1 of its flags)
     int dense_mask_words;  // words of a dense blob's slot masks (warps * chunk, to 4)
+    int blob_stride16;        // blobs at a fixed stride (16-byte units), or 0: blob_off
     size_t in_stage_bytes;    // staged input of one chunk, rounded to 128 B
     size_t blob_stage_bytes;  // largest weight blob, rounded to 128 B
 };
@@ -111,6 +113,15 @@ cudaError_t launch_wait_selftest(unsigned int *flags, int arrive, cudaStream_t s
 
 // Dynamic shared memory a launch needs with `split` blocks per cluster.
 size_t forward_smem_bytes(const Geometry &g, int split);
+
+// Grid of a forward launch (x: cluster rank fastest, then tiles [and groups];
+// y: groups, or 1 when groups run fastest).
+void forward_grid(const Geometry &g, int N, int split, bool group_fast, unsigned *gx,
+                  unsigned *gy);
+
+// Whether a launch with `split` cluster ranks reduces by pushing partial sums
+// into the owning block (no split rows, and room beside the stage buffers).
+bool push_reduction(const Geometry &g, int split);
 
 // Enqueues the forward kernel.  tmap is a tiled tensor map of the input for
 // stride-1 layers whose row stride is a multiple of 16 bytes (nullptr:

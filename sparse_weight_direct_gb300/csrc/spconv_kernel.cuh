@@ -67,6 +67,9 @@ struct KParams {
     int use_tma;
     int fmt;  // sparse entries: 0 = {fp32 value, int32 offset}, 1 = 32-bit packed word
     int group_fast, groups;  // block order; number of groups
+    uint32_t blob_stride16;  // blobs at a fixed stride (16-byte units), or 0: blob_off
+    int push;                // cluster reduction by remote stores into the owner's buffer
+    int recv_off;            // byte offset of that receive buffer in shared memory
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     // thread) and the output channel (+ chain link) of this warp's first
     // output item.
     uint32_t pre_off[3] = {0u, 0u, 0u};
-    if (threadIdx.x == 0 && nmine > 0) {
+    if (threadIdx.x == 0 && nmine > 0 && p.blob_stride16 == 0) {
         const uint32_t *bo = p.blob_off + group * p.num_chunks + k_begin;
         pre_off[0] = bo[0];
         pre_off[1] = bo[1];
@@ -386,6 +389,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     }
     __syncthreads();
+    // Push-mode cluster reduction: this block announces that it is running;
+    // the matching wait comes before its first store into another block.
+    const bool push = split > 1 && p.push;
+    if (push) asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
 
     // Enqueue chunk k into stage s.  `issuer` (one thread) arms the stage's
     // mbarrier and issues the bulk copies; without TMA every thread also
@@ -394,10 +401,17 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         unsigned char *base = smem + (size_t)s * p.stage_bytes;
         const int c0 = k * p.chunk;
         if (issuer) {
-            const int i = k - k_begin;
-            const uint32_t o0 = i < 2 ? pre_off[i] : p.blob_off[group * p.num_chunks + k];
-            const uint32_t o1 = i < 2 ? pre_off[i + 1] : p.blob_off[group * p.num_chunks + k + 1];
-            const uint32_t blob_bytes = (o1 - o0) * 16u;
+            uint32_t o0, blob_bytes;
+            if (p.blob_stride16) {  // fixed-stride blobs: position from the indices alone
+                o0 = (uint32_t)(group * p.num_chunks + k) * p.blob_stride16;
+                blob_bytes = p.blob_stride16 * 16u;
+            } else {
+                const int i = k - k_begin;
+                o0 = i < 2 ? pre_off[i] : p.blob_off[group * p.num_chunks + k];
+                const uint32_t o1 =
+                    i < 2 ? pre_off[i + 1] : p.blob_off[group * p.num_chunks + k + 1];
+                blob_bytes = (o1 - o0) * 16u;
+            }
             asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
             mbar_expect_tx(&bar[s], blob_bytes + (p.use_tma ? (uint32_t)p.in_tma_bytes : 0u));
             bulk_load(base + p.in_stage_bytes, p.blobs + (size_t)o0 * 16u, blob_bytes, &bar[s]);
@@ -506,6 +520,55 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                 const int oy = oy0 + LR * r;
                 if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, acc[q][r]);
             }
+        }
+        return;
+    }
+
+    if (push) {
+        // ---- cluster reduction by pushing (groups without split rows).  Each
+        // block stores its partial sums straight into the receive buffer of
+        // the block that owns the slot (distributed shared memory, a region
+        // apart from the stage buffers, so an owner still computing is not
+        // disturbed); one cluster barrier publishes them; each owner adds its
+        // slots' partials in rank order -- the pull path's order, so the
+        // results are identical -- from its own shared memory, and needs no
+        // barrier after that because no other block reads it.
+        float *recv = reinterpret_cast<float *>(smem + p.recv_off);  // [rank][own][P][32]
+        const int own = (nslot + split - 1) / split;  // most slots a rank owns
+        cg::cluster_group cluster = cg::this_cluster();
+        asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");  // all blocks started
+        if (!failed) {
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int sl = warp * Q + q;
+                int o = split - 1;  // owner: the last rank whose range starts at or before sl
+                while (o > 0 && o * nslot / split > sl) --o;
+                float *dst = cluster.map_shared_rank(recv, o) +
+                             ((kr * own + (sl - o * nslot / split)) * P) * 32 + lane;
+#pragma unroll
+                for (int r = 0; r < P; ++r) dst[r * 32] = acc[q][r];
+            }
+        }
+        asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+        asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+        if (failed || ox >= p.F) return;
+        const int s_begin = kr * nslot / split, s_end = (kr + 1) * nslot / split;
+        const int items = (s_end - s_begin) * P;
+        for (int item = warp; item < items; item += kWarps) {
+            const int li = item / P, r = item % P;
+            const int m = item == warp ? pre_m : p.slot_oc[group * nslot + s_begin + li];
+            if (m < 0) continue;
+            float v[kMaxSplit];
+#pragma unroll
+            for (int j = 0; j < kMaxSplit; ++j)
+                v[j] = j < split ? recv[((j * own + li) * P + r) * 32 + lane] : 0.f;
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxSplit; ++j)
+                if (j < split) sum += v[j];
+            const int oy = oy0 + LR * r;
+            if (oy < p.E)
+                p.y[((size_t)n * p.M + m) * p.E * p.F + (size_t)oy * p.F + ox] = finish(p, m, sum);
         }
         return;
     }

@@ -109,7 +109,10 @@ def decode_layout(w):
             if info["format"] == 1:
                 # [31:16] fp16 value, [15:8] channel in chunk, [7:4] column, [3:0] row
                 words = blob[hw * 4:].view(np.uint32)
-                assert hdr[spg] <= words.size and words.size - hdr[spg] <= 3
+                assert hdr[spg] <= words.size
+                # padding past the last word: to 16 bytes, or to the fixed blob stride
+                assert info["blob_stride"] or words.size - hdr[spg] <= 3
+                assert not words[hdr[spg]:].any()
                 for ls in range(spg):
                     m = int(slot_oc[g * spg + ls])
                     seg = words[hdr[ls]:hdr[ls + 1]]
@@ -124,7 +127,10 @@ def decode_layout(w):
                         rows.setdefault(m, []).append(((c * R + r) * S + s, v))
                 continue
             ent = blob[hw * 4:].view([("value", "<f4"), ("off", "<i4")])
-            assert hdr[spg] <= ent.size and ent.size - hdr[spg] <= 1  # 16-byte padding
+            assert hdr[spg] <= ent.size
+            # padding past the last entry: to 16 bytes, or to the fixed blob stride
+            assert info["blob_stride"] or ent.size - hdr[spg] <= 1
+            assert not blob[hw * 4 + 8 * int(hdr[spg]):].any()
             for ls in range(spg):
                 m = int(slot_oc[g * spg + ls])
                 seg = ent[hdr[ls]:hdr[ls + 1]]
@@ -181,6 +187,74 @@ def test_packed_layout_decodes_to_csr(name, fmt):
     assert info["tiles_y"] * tile_h >= L.E
     assert info["tiles_x"] * info["tile_cols"] >= L.F
     assert info["smem_bytes"] <= 200 * 1024
+    w.close()
+
+
+@pytest.mark.parametrize("hint", [0, 1, "batch"])
+@pytest.mark.parametrize("name", ["tiny", "resnet3x3", "vgg3x3", "sweep50", "sweep90",
+                                  "sweep99", "conv5x5"])
+def test_fixed_stride_blobs(name, hint):
+    """Blobs of nearly equal size (padding each to the largest adds at most a
+    quarter) sit at a fixed stride, so a block finds its blob from its
+    (group, chunk) index alone; otherwise they are packed back to back."""
+    L = workloads.LAYERS[name]
+    rowptr, colidx, value = workloads.make_weights(L)
+    w = swd.pack_host(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
+                      stride=L.stride, pad=L.pad, batch_hint=L.N if hint == "batch" else hint)
+    info = w.info()
+    off = w.array("blob_off").astype(np.int64)
+    sizes = np.diff(off) * 16
+    stride = info["blob_stride"]
+    if stride:
+        assert np.all(sizes == stride) and stride % 16 == 0
+        assert stride <= info["blob_stage_bytes"]
+    else:
+        assert sizes.max() * sizes.size > 1.25 * sizes.sum()
+    if hint == "batch" and name in ("tiny", "resnet3x3", "vgg3x3"):
+        assert stride > 0  # the benchmark's plans of the Bernoulli layers: near-equal blobs
+    w.close()
+
+
+def test_launch_plans():
+    """The launch a forward would make (host logic): one-image layers split
+    their channel chunks over a cluster and reduce by pushing partial sums;
+    batched layers fill the GPU without a cluster; the weight-stationary
+    format launches one block per (output channel, tile, image)."""
+    def plan(name, N, **kw):
+        L = workloads.LAYERS[name]
+        rowptr, colidx, value = workloads.make_weights(L)
+        w = swd.pack_host(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
+                          stride=L.stride, pad=L.pad, **kw)
+        info, launch = w.info(), w.launch_info(N)
+        w.close()
+        return L, info, launch
+
+    L, info, pl = plan("resnet3x3", 1, batch_hint=1)
+    assert pl["kernel"] == 0 and pl["cluster"] == 8 and pl["push"] == 1
+    assert pl["grid_x"] * pl["grid_y"] == 8 * info["groups"] and pl["grid_z"] == 1
+    assert pl["block_threads"] == 256 and pl["tma"] == 0  # 56-byte rows: cp.async
+    assert pl["smem_bytes"] <= 200 * 1024
+    L, info, pl = plan("vgg3x3", 16, batch_hint=16)
+    assert pl["cluster"] == 1 and pl["push"] == 0 and pl["tma"] == 1
+    assert pl["grid_x"] * pl["grid_y"] == 16 * info["tiles_y"] * info["tiles_x"] * info["groups"]
+    L, info, pl = plan("vgg3x3", 16, fmt="ws")
+    assert pl["kernel"] == 1 and pl["cluster"] == 1
+    assert (pl["grid_x"], pl["grid_y"], pl["grid_z"]) == (L.M, info["tiles_y"] * info["tiles_x"],
+                                                          16)
+    # split rows keep a cluster on the reduction by remote reads
+    rng = np.random.default_rng(3)
+    C, M, CRS = 128, 64, 128 * 9
+    rows = [np.nonzero(rng.random(CRS) < (0.9 if m in (0, 40) else 0.1))[0] for m in range(M)]
+    rowptr = np.concatenate([[0], np.cumsum([r.size for r in rows])]).astype(np.int32)
+    colidx = np.concatenate(rows).astype(np.int32)
+    value = np.ones(colidx.size, np.float32)
+    w = swd.pack_host(rowptr, colidx, value, C=C, H=14, W=14, M=M, R=3, S=3, stride=1, pad=1,
+                      batch_hint=1)
+    assert (w.array("group_flags") & 2).any()
+    pl = w.launch_info(1)
+    assert pl["cluster"] > 1 and pl["push"] == 0
+    with pytest.raises(swd.SpconvError):
+        w.launch_info(0)
     w.close()
 
 

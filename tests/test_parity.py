@@ -274,3 +274,45 @@ def test_packed32_format(name, integer):
                   fmt="packed32")
     ref, mag = oracle.csr(x, rowptr, colidx, v16, L.M, L.R, L.S, L.stride, L.pad)
     check(got, ref, mag, exact=integer, what=name + " packed32")
+
+
+def _cluster_case(rng, heavy: bool, integer: bool):
+    """N=1, 128 channels in 8 chunks, 64 output channels: a small grid whose
+    chunks are split over a cluster.  heavy: rows 0 and 40 are 90 % dense and
+    get split into parts (which keeps the cluster on the reduction by reads)."""
+    C, H, W, M, K = 128, 14, 14, 64, 3
+    CRS = C * K * K
+    rows = [np.nonzero(rng.random(CRS) < (0.9 if heavy and m in (0, 40) else 0.1))[0]
+            for m in range(M)]
+    rowptr = np.concatenate([[0], np.cumsum([r.size for r in rows])]).astype(np.int32)
+    colidx = np.concatenate(rows).astype(np.int32)
+    if integer:
+        value = rng.choice(np.array([-3, -2, -1, 1, 2, 3], np.float32), size=colidx.size)
+    else:
+        value = rng.normal(0, 0.05, size=colidx.size).astype(np.float32)
+    x = workloads.random_input((1, C, H, W), rng, integer=integer)
+    return x, rowptr, colidx, value, C, H, W, M, K
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("integer", [False, True])
+@pytest.mark.parametrize("heavy", [False, True])
+def test_cluster_reduction_paths(heavy, integer):
+    """Both cluster reductions against the oracle: partial sums pushed into
+    the owning block (no split rows) and read from every rank (split rows)."""
+    rng = np.random.default_rng(17 + heavy * 2 + integer)
+    x, rowptr, colidx, value, C, H, W, M, K = _cluster_case(rng, heavy, integer)
+    w = swd.pack(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=K, S=K, stride=1, pad=1,
+                 batch_hint=1)
+    plan = w.launch_info(1)
+    assert plan["cluster"] > 1 and plan["push"] == (0 if heavy else 1)
+    assert bool((w.array("group_flags") & 2).any()) == heavy
+    xd = torch.from_numpy(x).cuda()
+    out = torch.full((1, M, H, W), float("nan"), device="cuda")
+    swd.forward(xd, w, out=out)
+    torch.cuda.synchronize()
+    assert w.device_status() == 0
+    w.close()
+    ref, mag = oracle.csr(x, rowptr, colidx, value, M, K, K, 1, 1)
+    check(out.cpu().numpy().astype(np.float64), ref, mag, exact=integer,
+          what=f"cluster heavy={heavy}")
