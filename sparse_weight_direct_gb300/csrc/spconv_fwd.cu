@@ -149,6 +149,7 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
     p.fmt = g.format;
     p.blob_stride16 = (uint32_t)g.blob_stride16;
     p.push = push_reduction(g, split) ? 1 : 0;
+    p.pairs = (g.stride == 1 && g.W % 2 == 0 && g.row_pitch % 2 == 0 && g.plane % 2 == 0) ? 1 : 0;
     p.recv_off = (int)stages_bytes(g, split);
     CUtensorMap dummy;
     if (!tmap) {

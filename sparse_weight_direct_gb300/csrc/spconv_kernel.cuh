@@ -69,6 +69,7 @@ struct KParams {
     int group_fast, groups;  // block order; number of groups
     uint32_t blob_stride16;  // blobs at a fixed stride (16-byte units), or 0: blob_off
     int push;                // cluster reduction by remote stores into the owner's buffer
+    int pairs;               // cp.async staging in 8-byte column pairs (stride 1, W even)
     int recv_off;            // byte offset of that receive buffer in shared memory
 };
 
@@ -143,6 +144,13 @@ static __device__ __forceinline__ void cp_async_4(float *smem_dst, const float *
                  "l"(gsrc), "r"(src_size)
                  : "memory");
 }
+static __device__ __forceinline__ void cp_async_8(float *smem_dst, const float *gsrc,
+                                                  int src_bytes) {
+    // 8-byte copy; the bytes past src_bytes (0, 4 or 8) are zero-filled
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
 static __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
@@ -188,6 +196,65 @@ static __device__ __forceinline__ void stage_input_cp_async(const KParams &p, fl
         col += dcol;
         if (col >= in_cols) {
             col -= in_cols;
+            ++row;
+        }
+    }
+}
+
+// The same staging with 8-byte copies, for stride 1 with an even input width
+// W: then global column x and its staged word x - ix0 + shift have the same
+// parity (row starts are even on both sides and ix0 = pad = shift mod 2), so
+// each aligned column pair is one copy.  Units u cover staged columns
+// 2u - a, 2u - a + 1 with a = pad & 1; the first unit (a = 1) and a unit that
+// would run past the staged row copy their one column with 4 bytes, so
+// nothing outside the staged row is written.  A pair whose second column is
+// past the image copies 4 bytes and zero-fills 4; one wholly outside copies
+// none (x is even, so a pair never starts left of the image and ends inside).
+static __device__ __forceinline__ void stage_input_cp_async_pairs(const KParams &p, float *buf,
+                                                                  int n, int c0, int cc, int iy0,
+                                                                  int ix0) {
+    const int in_cols = p.in_cols;
+    const int a = p.pad & 1;
+    const int units = (in_cols + a + 1) / 2;
+    const int plane_units = p.in_rows * units;
+    const size_t hw = (size_t)p.H * p.W;
+    const float *xc0 = p.x + ((size_t)n * p.C + c0) * hw;
+    const int T = blockDim.x;
+    int row = threadIdx.x / units, u = threadIdx.x - row * units;
+    const int drow = T / units, du = T - drow * units;
+    for (int e = threadIdx.x; e < plane_units; e += T) {
+        const int gy = iy0 + row;
+        const int j = 2 * u - a;  // first staged column of the unit
+        const bool row_ok = (unsigned)gy < (unsigned)p.H;
+        float *dst = buf + row * p.row_pitch + p.shift;
+        if (j < 0 || j + 1 >= in_cols) {  // one column
+            const int jj = j < 0 ? 0 : j;
+            const int gx = ix0 + jj;
+            const bool ok = row_ok && (unsigned)gx < (unsigned)p.W;
+            const float *src = ok ? xc0 + (size_t)gy * p.W + gx : p.x;
+            const size_t step = ok ? hw : 0;
+            float *d = dst + jj;
+            for (int cl = 0; cl < cc; ++cl) {
+                cp_async_4(d, src, ok);
+                d += p.plane;
+                src += step;
+            }
+        } else {
+            const int gx = ix0 + j;  // even
+            const int bytes = !row_ok || gx < 0 || gx >= p.W ? 0 : (gx + 1 < p.W ? 8 : 4);
+            const float *src = bytes ? xc0 + (size_t)gy * p.W + gx : p.x;
+            const size_t step = bytes ? hw : 0;
+            float *d = dst + j;
+            for (int cl = 0; cl < cc; ++cl) {
+                cp_async_8(d, src, bytes);
+                d += p.plane;
+                src += step;
+            }
+        }
+        row += drow;
+        u += du;
+        if (u >= units) {
+            u -= units;
             ++row;
         }
     }
@@ -320,6 +387,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar[2];
     __shared__ int stage_done[2];  // warps that have released a stage (TMA path)
+    __shared__ int issued[2];      // copy phases issued into each stage
     // stage buffers start on a 128-byte boundary (TMA destination)
     unsigned char *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     constexpr int LC = kLanes / LR;  // lanes per lane row = output columns of a tile
@@ -349,9 +417,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     b /= p.tiles_x;
     const int ty = b % p.tiles_y;
     const int n = b / p.tiles_y;
-    const int gflags = p.group_flags[group];
-    const bool dense = (gflags & 1) != 0;
-    const bool has_parts = (gflags & 2) != 0;
     const int k_begin = kr * p.num_chunks / split;
     const int k_end = (kr + 1) * p.num_chunks / split;
     const int iy0 = ty * (LR * P) * st - p.pad;
@@ -359,10 +424,27 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int nmine = k_end - k_begin;
     const int nslot = kWarps * Q;
 
+    // Barrier set-up first: its release fence would otherwise wait for the
+    // global loads below (a whole memory round trip before the first copy).
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        stage_done[0] = 0;
+        stage_done[1] = 0;
+        issued[0] = 0;
+        issued[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    }
+    __syncthreads();
+
     // Loads that nothing computed here feeds, issued before any wait so that
-    // their latency overlaps the pipeline: the first blobs' offsets (issuing
-    // thread) and the output channel (+ chain link) of this warp's first
-    // output item.
+    // their latency overlaps the pipeline: the group's flags, the first
+    // blobs' offsets (issuing thread) and the output channel (+ chain link)
+    // of this warp's first output item.
+    const int gflags = p.group_flags[group];
+    const bool dense = (gflags & 1) != 0;
+    const bool has_parts = (gflags & 2) != 0;
     uint32_t pre_off[3] = {0u, 0u, 0u};
     if (threadIdx.x == 0 && nmine > 0 && p.blob_stride16 == 0) {
         const uint32_t *bo = p.blob_off + group * p.num_chunks + k_begin;
@@ -377,18 +459,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     int pre_m = -1, pre_next = -1;
     if (item0_valid) {
         pre_m = p.slot_oc[group * nslot + item0_slot];
-        if (has_parts || split > 1) pre_next = p.slot_next[group * nslot + item0_slot];
+        pre_next = p.slot_next[group * nslot + item0_slot];
     }
-
-    if (threadIdx.x == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        stage_done[0] = 0;
-        stage_done[1] = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    }
-    __syncthreads();
     // Push-mode cluster reduction: this block announces that it is running;
     // the matching wait comes before its first store into another block.
     const bool push = split > 1 && p.push;
@@ -401,6 +473,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         unsigned char *base = smem + (size_t)s * p.stage_bytes;
         const int c0 = k * p.chunk;
         if (issuer) {
+            ++issued[s];  // one writer per stage at a time (the thread that frees it)
             uint32_t o0, blob_bytes;
             if (p.blob_stride16) {  // fixed-stride blobs: position from the indices alone
                 o0 = (uint32_t)(group * p.num_chunks + k) * p.blob_stride16;
@@ -418,8 +491,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             if (p.use_tma) tma_load_4d(base, &tmap, ix0 - p.shift, iy0, c0, n, &bar[s]);
         }
         if (!p.use_tma) {
-            stage_input_cp_async<ST_CT>(p, reinterpret_cast<float *>(base), n, c0,
-                                        min(p.chunk, p.C - c0), iy0, ix0);
+            if (ST_CT == 1 && p.pairs)
+                stage_input_cp_async_pairs(p, reinterpret_cast<float *>(base), n, c0,
+                                           min(p.chunk, p.C - c0), iy0, ix0);
+            else
+                stage_input_cp_async<ST_CT>(p, reinterpret_cast<float *>(base), n, c0,
+                                            min(p.chunk, p.C - c0), iy0, ix0);
             cp_async_commit();
         }
     };
@@ -499,10 +576,19 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             if (it + 2 < nmine) issue(k_begin + it + 2, s, threadIdx.x == 0);
         }
     }
-    if (p.use_tma) __syncthreads();  // every warp is out of the pipeline
+    // Every warp is out of the pipeline.  If any gave up waiting, the whole
+    // block writes no outputs; its copies still in flight (at most one phase
+    // per stage, since a stage is refilled only after it was consumed) are
+    // waited for, again with a limit, before shared memory can go away.
+    failed = __syncthreads_or(failed) != 0;
     if (failed) {
         if (!p.use_tma) cp_async_wait_all();
-        if (lane == 0) atomicOr(p.err, 1u);
+        if (threadIdx.x == 0) {
+            atomicOr(p.err, 1u);
+            for (int st2 = 0; st2 < 2; ++st2)
+                if (issued[st2] > 0) mbar_wait_bounded(&bar[st2], (uint32_t)((issued[st2] - 1) & 1));
+        }
+        __syncthreads();
     }
 
     const int slot0 = group * nslot + warp * Q;
