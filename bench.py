@@ -288,6 +288,7 @@ def run_ours(args, L):
                  stride=L.stride, pad=L.pad, stream=stream, fmt=args.fmt, batch_hint=L.N)
     pack_ms = (time.perf_counter() - t0) * 1e3
     info = w.info()
+    launch = w.launch_info(L.N)  # grid, cluster, reduction, shared memory of one launch
 
     x = torch.from_numpy(x_host).to(dev)
     y = torch.empty((L.N, L.M, L.E, L.F), device=dev, dtype=torch.float32)
@@ -387,9 +388,10 @@ def run_ours(args, L):
                           "sem": (statistics.stdev(per) / len(per) ** 0.5 * 1e3)
                           if len(per) > 1 else 0.0},
         "nnz": nnz, "pack_ms": pack_ms,
-        "tiling": {k: info[k] for k in ("tile_rows", "tiles_y", "tiles_x", "chunk",
-                                         "num_chunks", "slots_per_warp", "groups",
-                                         "smem_bytes")},
+        "tiling": {**{k: info[k] for k in ("tile_rows", "lane_rows", "tiles_y", "tiles_x",
+                                            "chunk", "num_chunks", "slots_per_warp", "groups",
+                                            "blob_stride")},
+                   "launch": launch},
         "roofline": roof,
         "e2e": {"value": whole_job_us_per_layer(e2e_ms * e2e_steps, e2e_steps, world),
                 "unit": UNIT,
