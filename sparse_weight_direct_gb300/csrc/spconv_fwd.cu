@@ -100,7 +100,7 @@ void forward_grid(const Geometry &g, int N, int split, bool group_fast, unsigned
 }
 
 bool push_reduction(const Geometry &g, int split) {
-    return split > 1 && !g.split_rows &&
+    return split > 1 && !g.split_rows && g.slots <= 2 &&  // compiled into Q <= 2 instances
            stages_bytes(g, split) + recv_bytes(g, split) + 128 <= (size_t)kern::kMaxDynamicSmem;
 }
 

@@ -610,53 +610,56 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         return;
     }
 
-    if (push) {
-        // ---- cluster reduction by pushing (groups without split rows).  Each
-        // block stores its partial sums straight into the receive buffer of
-        // the block that owns the slot (distributed shared memory, a region
-        // apart from the stage buffers, so an owner still computing is not
-        // disturbed); one cluster barrier publishes them; each owner adds its
-        // slots' partials in rank order -- the pull path's order, so the
-        // results are identical -- from its own shared memory, and needs no
-        // barrier after that because no other block reads it.
-        float *recv = reinterpret_cast<float *>(smem + p.recv_off);  // [rank][own][P][32]
-        const int own = (nslot + split - 1) / split;  // most slots a rank owns
-        cg::cluster_group cluster = cg::this_cluster();
-        asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");  // all blocks started
-        if (!failed) {
+    if constexpr (Q <= 2) {  // push mode is planned for narrow instances only
+        if (push) {
+            // ---- cluster reduction by pushing (groups without split rows).  Each
+            // block stores its partial sums straight into the receive buffer of
+            // the block that owns the slot (distributed shared memory, a region
+            // apart from the stage buffers, so an owner still computing is not
+            // disturbed); one cluster barrier publishes them; each owner adds its
+            // slots' partials in rank order -- the pull path's order, so the
+            // results are identical -- from its own shared memory, and needs no
+            // barrier after that because no other block reads it.
+            float *recv = reinterpret_cast<float *>(smem + p.recv_off);  // [rank][own][P][32]
+            const int own = (nslot + split - 1) / split;  // most slots a rank owns
+            cg::cluster_group cluster = cg::this_cluster();
+            asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");  // all blocks started
+            if (!failed) {
 #pragma unroll
-            for (int q = 0; q < Q; ++q) {
-                const int sl = warp * Q + q;
-                int o = split - 1;  // owner: the last rank whose range starts at or before sl
-                while (o > 0 && o * nslot / split > sl) --o;
-                float *dst = cluster.map_shared_rank(recv, o) +
-                             ((kr * own + (sl - o * nslot / split)) * P) * 32 + lane;
+                for (int q = 0; q < Q; ++q) {
+                    const int sl = warp * Q + q;
+                    int o = split - 1;  // owner: the last rank whose range starts at or before sl
+                    while (o > 0 && o * nslot / split > sl) --o;
+                    float *dst = cluster.map_shared_rank(recv, o) +
+                                 ((kr * own + (sl - o * nslot / split)) * P) * 32 + lane;
 #pragma unroll
-                for (int r = 0; r < P; ++r) dst[r * 32] = acc[q][r];
+                    for (int r = 0; r < P; ++r) dst[r * 32] = acc[q][r];
+                }
             }
-        }
-        asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-        asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-        if (failed || ox >= p.F) return;
-        const int s_begin = kr * nslot / split, s_end = (kr + 1) * nslot / split;
-        const int items = (s_end - s_begin) * P;
-        for (int item = warp; item < items; item += kWarps) {
-            const int li = item / P, r = item % P;
-            const int m = item == warp ? pre_m : p.slot_oc[group * nslot + s_begin + li];
-            if (m < 0) continue;
-            float v[kMaxSplit];
+            asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+            asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+            if (failed || ox >= p.F) return;
+            const int s_begin = kr * nslot / split, s_end = (kr + 1) * nslot / split;
+            const int items = (s_end - s_begin) * P;
+            for (int item = warp; item < items; item += kWarps) {
+                const int li = item / P, r = item % P;
+                const int m = item == warp ? pre_m : p.slot_oc[group * nslot + s_begin + li];
+                if (m < 0) continue;
+                float v[kMaxSplit];
 #pragma unroll
-            for (int j = 0; j < kMaxSplit; ++j)
-                v[j] = j < split ? recv[((j * own + li) * P + r) * 32 + lane] : 0.f;
-            float sum = 0.f;
+                for (int j = 0; j < kMaxSplit; ++j)
+                    v[j] = j < split ? recv[((j * own + li) * P + r) * 32 + lane] : 0.f;
+                float sum = 0.f;
 #pragma unroll
-            for (int j = 0; j < kMaxSplit; ++j)
-                if (j < split) sum += v[j];
-            const int oy = oy0 + LR * r;
-            if (oy < p.E)
-                p.y[((size_t)n * p.M + m) * p.E * p.F + (size_t)oy * p.F + ox] = finish(p, m, sum);
+                for (int j = 0; j < kMaxSplit; ++j)
+                    if (j < split) sum += v[j];
+                const int oy = oy0 + LR * r;
+                if (oy < p.E)
+                    p.y[((size_t)n * p.M + m) * p.E * p.F + (size_t)oy * p.F + ox] =
+                        finish(p, m, sum);
+            }
+            return;
         }
-        return;
     }
 
     // ---- partial sums through shared memory: parts of split rows (summed in
@@ -691,31 +694,51 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
     const int s_begin = kr * nslot / split, s_end = (kr + 1) * nslot / split;
-    if (!failed && ox < p.F) {
-        // (slot, output row) items spread over all warps; the ranks' partials
-        // of one item are loaded back to back, then added in rank order
-        const int items = (s_end - s_begin) * P;
-        for (int item = warp; item < items; item += kWarps) {
-            const int sl = s_begin + item / P, r = item % P;
-            const bool first = item == warp;
-            const int m = first ? pre_m : p.slot_oc[group * nslot + sl];
-            if (m < 0) continue;
-            float sum = 0.f;
-            for (int c = sl, next = first ? pre_next : p.slot_next[group * nslot + sl]; c >= 0;
-                 c = next, next = c >= 0 ? p.slot_next[group * nslot + c] : -1) {
-                float v[kMaxSplit];
+    if constexpr (Q <= 2) {
+        if (!failed && ox < p.F) {
+            // (slot, output row) items spread over all warps; the ranks' partials
+            // of one item are loaded back to back, then added in rank order
+            const int items = (s_end - s_begin) * P;
+            for (int item = warp; item < items; item += kWarps) {
+                const int sl = s_begin + item / P, r = item % P;
+                const bool first = item == warp;
+                const int m = first ? pre_m : p.slot_oc[group * nslot + sl];
+                if (m < 0) continue;
+                float sum = 0.f;
+                for (int c = sl, next = first ? pre_next : p.slot_next[group * nslot + sl]; c >= 0;
+                     c = next, next = c >= 0 ? p.slot_next[group * nslot + c] : -1) {
+                    float v[kMaxSplit];
 #pragma unroll
-                for (int j = 0; j < kMaxSplit; ++j)
-                    v[j] = j < split ? cluster.map_shared_rank(part, j)[(c * P + r) * 32 + lane]
-                                     : 0.f;
+                    for (int j = 0; j < kMaxSplit; ++j)
+                        v[j] = j < split ? cluster.map_shared_rank(part, j)[(c * P + r) * 32 + lane]
+                                         : 0.f;
 #pragma unroll
-                for (int j = 0; j < kMaxSplit; ++j)
-                    if (j < split) sum += v[j];
+                    for (int j = 0; j < kMaxSplit; ++j)
+                        if (j < split) sum += v[j];
+                }
+                const int oy = oy0 + LR * r;
+                if (oy < p.E)
+                    p.y[((size_t)n * p.M + m) * p.E * p.F + (size_t)oy * p.F + ox] =
+                        finish(p, m, sum);
             }
-            const int oy = oy0 + LR * r;
-            if (oy < p.E)
-                p.y[((size_t)n * p.M + m) * p.E * p.F + (size_t)oy * p.F + ox] =
-                    finish(p, m, sum);
+        }
+    } else {
+        // wide instances: one warp per slot, ranks and rows in sequence (compact
+        // code; these instances carry the register-heavy dense-tap path)
+        if (!failed && ox < p.F) {
+            for (int sl = s_begin + warp; sl < s_end; sl += kWarps) {
+                const int m = p.slot_oc[group * nslot + sl];
+                if (m < 0) continue;
+                float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
+                for (int r = 0; r < P; ++r) {
+                    float sum = 0.f;
+                    for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c])
+                        for (int j = 0; j < split; ++j)
+                            sum += cluster.map_shared_rank(part, j)[(c * P + r) * 32 + lane];
+                    const int oy = oy0 + LR * r;
+                    if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, sum);
+                }
+            }
         }
     }
     cluster.sync();  // partials stay readable until every block is done
