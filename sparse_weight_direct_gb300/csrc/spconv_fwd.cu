@@ -44,11 +44,11 @@ size_t stage_bytes(const Geometry &g) { return g.in_stage_bytes + g.blob_stage_b
 
 // The dynamic shared-memory limit is a per-function, per-device attribute:
 // raise it once to the largest size any plan uses, and remember that.
-cudaError_t raise_smem_limit(KernelFn fn) {
+cudaError_t raise_smem_limit(const void *fn) {
     constexpr int kMaxDev = 64;
     constexpr int kSlots = 256;
     static std::mutex lock;
-    static std::pair<KernelFn, int> done[kSlots];
+    static std::pair<const void *, int> done[kSlots];
     static int ndone = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -56,8 +56,8 @@ cudaError_t raise_smem_limit(KernelFn fn) {
     std::lock_guard<std::mutex> lk(lock);
     for (int i = 0; i < ndone; ++i)
         if (done[i].first == fn && done[i].second == dev) return cudaSuccess;
-    e = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kern::kMaxDynamicSmem);
     if (e != cudaSuccess) return e;
     if (ndone < kSlots && dev < kMaxDev) done[ndone++] = {fn, dev};
     return cudaSuccess;
@@ -121,7 +121,7 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
         return cudaErrorInvalidConfiguration;
     const size_t smem = forward_smem_bytes(g, split);
     if (smem > 48 * 1024) {
-        cudaError_t e = raise_smem_limit(fn);
+        cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(fn));
         if (e != cudaSuccess) return e;
     }
     KParams p;

@@ -49,6 +49,11 @@ namespace kern {
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
 constexpr int kMaxDynamicSmem = 200 * 1024;                   // upper bound of any plan
 
+// Raises a kernel's dynamic shared-memory limit to kMaxDynamicSmem, once per
+// kernel and device (later calls only look it up: no API call, so launches
+// can be captured into a CUDA graph).
+cudaError_t raise_smem_limit(const void *fn);
+
 struct KParams {
     const float *x;
     float *y;

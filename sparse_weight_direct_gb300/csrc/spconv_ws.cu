@@ -226,8 +226,8 @@ cudaError_t launch_forward_ws(const Geometry &g, int N, const float *x, float *y
         return cudaErrorInvalidConfiguration;
     const size_t smem = ws_smem_bytes(g);
     if (smem > 48 * 1024) {
-        cudaError_t e =
-            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (smem > (size_t)kern::kMaxDynamicSmem) return cudaErrorInvalidConfiguration;
+        cudaError_t e = kern::raise_smem_limit(reinterpret_cast<const void *>(fn));
         if (e != cudaSuccess) return e;
     }
     kern::WsParams p;
