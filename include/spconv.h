@@ -246,6 +246,10 @@ typedef struct spconv_launch_info {
                              /* reads (two barriers) or no cluster              */
     int32_t group_fast;      /* 1: all channel groups of a tile run together     */
     int32_t tma;             /* 1: input staged by TMA tensor copies             */
+    int32_t pdl;             /* 1: launched with programmatic stream             */
+                             /* serialization (start-up overlaps the previous    */
+                             /* kernel on the stream; input and output are only  */
+                             /* touched after that kernel has completed)         */
     int64_t smem_bytes;      /* dynamic shared memory per block                  */
 } spconv_launch_info;
 

@@ -57,7 +57,7 @@ class PackedInfo(ctypes.Structure):
 class LaunchInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("kernel", "grid_x", "grid_y", "grid_z", "block_threads", "cluster", "push",
-                 "group_fast", "tma")] + [("smem_bytes", ctypes.c_int64)]
+                 "group_fast", "tma", "pdl")] + [("smem_bytes", ctypes.c_int64)]
 
 
 def lib() -> ctypes.CDLL:

@@ -113,9 +113,9 @@ size_t forward_smem_bytes(const Geometry &g, int split) {
     return bytes + 128;  // room to align the stage buffers to 128 bytes
 }
 
-cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast, const float *x,
-                           float *y, const float *bias, int act, const DeviceArrays &d,
-                           const CUtensorMap *tmap, cudaStream_t stream) {
+cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast, bool pdl,
+                           const float *x, float *y, const float *bias, int act,
+                           const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream) {
     KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows);
     if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks)
         return cudaErrorInvalidConfiguration;
@@ -166,15 +166,25 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
     if (split > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)split;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)split;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    // Programmatic dependent launch: the kernel may start while the previous
+    // kernel on the stream finishes; it waits (griddepcontrol.wait) before it
+    // reads the input or writes the output.
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, fn, p, *tmap);
 }
 

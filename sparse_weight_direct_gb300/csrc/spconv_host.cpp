@@ -784,6 +784,17 @@ bool choose_group_fast(const spconv::Geometry &g, int N, int64_t nnz) {
 // Blocks per cluster along the channel chunks: none when the grid already
 // fills the GPU, else enough for about two blocks per SM (measured best on
 // the one-image ResNet-style layer).
+// Programmatic dependent launch hides a launch's start-up behind the previous
+// kernel's tail: worth most for the short one-wave launches of small layers
+// (one-image ResNet layer 8.6 -> 7.3 us back to back).  Measured to cost 4 %
+// on a multi-wave layer with dense-tap groups (lognormal sweep, 80 %), so
+// those launch without it.
+bool choose_pdl(const spconv::Geometry &g, int N, int split, bool group_fast) {
+    unsigned gx = 0, gy = 0;
+    spconv::forward_grid(g, N, split, group_fast, &gx, &gy);
+    return !(g.dense_groups > 0 && (int64_t)gx * gy > 2 * kSMs);
+}
+
 int choose_split(const spconv::Geometry &g, int N) {
     const int64_t blocks = (int64_t)N * g.tiles_y * g.tiles_x * g.groups;
     if (blocks >= kSMs) return 1;
@@ -871,8 +882,10 @@ __attribute__((visibility("default"))) int spconv_forward_ex(
         const CUtensorMap *tmap = input_tmap(packed, input, N, tmp);
         const int split = choose_split(g, N);
         const bool group_fast = choose_group_fast(g, N, packed->nnz);
-        cudaError_t e = spconv::launch_forward(g, N, split, group_fast, input, output, bias, act,
-                                               packed->d, tmap, static_cast<cudaStream_t>(stream));
+        const bool pdl = choose_pdl(g, N, split, group_fast);
+        cudaError_t e =
+            spconv::launch_forward(g, N, split, group_fast, pdl, input, output, bias, act,
+                                   packed->d, tmap, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) {
             cudaGetLastError();
             return SPCONV_ERR_CUDA;
@@ -1029,6 +1042,7 @@ __attribute__((visibility("default"))) int spconv_launch_info_get(const spconv_p
     info->cluster = split;
     info->push = spconv::push_reduction(g, split) ? 1 : 0;
     info->group_fast = group_fast ? 1 : 0;
+    info->pdl = choose_pdl(g, N, split, group_fast) ? 1 : 0;
     info->tma = tma_eligible(g) ? 1 : 0;
     info->smem_bytes = (int64_t)spconv::forward_smem_bytes(g, split);
     return SPCONV_OK;

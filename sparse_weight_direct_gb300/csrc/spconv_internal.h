@@ -129,9 +129,11 @@ bool push_reduction(const Geometry &g, int split);
 // tile run together (they then share the tile's input through L2).  Returns
 // cudaSuccess or the launch error.  bias (M floats or nullptr) and act
 // (0 identity, 1 ReLU) form the fused epilogue y = act(conv + bias).
-cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast, const float *x,
-                           float *y, const float *bias, int act, const DeviceArrays &d,
-                           const CUtensorMap *tmap, cudaStream_t stream);
+// pdl: launch with programmatic stream serialization (the kernel's prologue
+// may overlap the previous kernel on the stream).
+cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast, bool pdl,
+                           const float *x, float *y, const float *bias, int act,
+                           const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream);
 
 // Weight-stationary format (one output channel per block, input read in
 // place): whether (P, LR) has an instance, the dynamic shared memory of a

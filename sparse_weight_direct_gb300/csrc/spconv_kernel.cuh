@@ -474,10 +474,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     // Enqueue chunk k into stage s.  `issuer` (one thread) arms the stage's
     // mbarrier and issues the bulk copies; without TMA every thread also
     // stages its share of the input with cp.async.
-    auto issue = [&](int k, int s, bool issuer) {
+    // (weights: arm the stage's mbarrier for all its bytes and copy the blob;
+    // input: copy the input tile, which completes on the same mbarrier.)
+    auto issue = [&](int k, int s, bool issuer, bool weights, bool input) {
         unsigned char *base = smem + (size_t)s * p.stage_bytes;
         const int c0 = k * p.chunk;
-        if (issuer) {
+        if (issuer && weights) {
             ++issued[s];  // one writer per stage at a time (the thread that frees it)
             uint32_t o0, blob_bytes;
             if (p.blob_stride16) {  // fixed-stride blobs: position from the indices alone
@@ -493,9 +495,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
             mbar_expect_tx(&bar[s], blob_bytes + (p.use_tma ? (uint32_t)p.in_tma_bytes : 0u));
             bulk_load(base + p.in_stage_bytes, p.blobs + (size_t)o0 * 16u, blob_bytes, &bar[s]);
-            if (p.use_tma) tma_load_4d(base, &tmap, ix0 - p.shift, iy0, c0, n, &bar[s]);
         }
-        if (!p.use_tma) {
+        if (issuer && input && p.use_tma)
+            tma_load_4d(base, &tmap, ix0 - p.shift, iy0, c0, n, &bar[s]);
+        if (input && !p.use_tma) {
             if (ST_CT == 1 && p.pairs)
                 stage_input_cp_async_pairs(p, reinterpret_cast<float *>(base), n, c0,
                                            min(p.chunk, p.C - c0), iy0, ix0);
@@ -513,8 +516,16 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         for (int r = 0; r < P; ++r) acc[q][r] = 0.f;
 
     bool failed = false;
-    if (nmine > 0) issue(k_begin, 0, threadIdx.x == 0);
-    if (nmine > 1) issue(k_begin + 1, 1, threadIdx.x == 0);
+    // The weight blobs do not depend on earlier kernels: their copies start
+    // before the wait below, which (with programmatic dependent launch) lets
+    // this prologue overlap the previous kernel on the stream.  Past the wait
+    // that kernel has completed and its writes are visible, so the input may
+    // be read and the output written.
+    if (nmine > 0) issue(k_begin, 0, threadIdx.x == 0, true, false);
+    if (nmine > 1) issue(k_begin + 1, 1, threadIdx.x == 0, true, false);
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (nmine > 0) issue(k_begin, 0, threadIdx.x == 0, false, true);
+    if (nmine > 1) issue(k_begin + 1, 1, threadIdx.x == 0, false, true);
     for (int it = 0; it < nmine && !failed; ++it) {
         const int s = it & 1;
         if (!p.use_tma) {
@@ -572,15 +583,18 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                     if (old == kWarps - 1) {
                         stage_done[s] = 0;
                         __threadfence_block();
-                        issue(k_begin + it + 2, s, true);
+                        issue(k_begin + it + 2, s, true, true, true);
                     }
                 }
             }
         } else {
             __syncthreads();  // stage s is free again
-            if (it + 2 < nmine) issue(k_begin + it + 2, s, threadIdx.x == 0);
+            if (it + 2 < nmine) issue(k_begin + it + 2, s, threadIdx.x == 0, true, true);
         }
     }
+    // The next kernel on the stream may start launching (it waits for this
+    // grid to complete before touching memory that this grid uses).
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     // Every warp is out of the pipeline.  If any gave up waiting, the whole
     // block writes no outputs; its copies still in flight (at most one phase
     // per stage, since a stage is refilled only after it was consumed) are

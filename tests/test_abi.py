@@ -231,12 +231,16 @@ def test_launch_plans():
 
     L, info, pl = plan("resnet3x3", 1, batch_hint=1)
     assert pl["kernel"] == 0 and pl["cluster"] == 8 and pl["push"] == 1
+    assert pl["pdl"] == 1  # one wave: start-up overlaps the previous kernel
     assert pl["grid_x"] * pl["grid_y"] == 8 * info["groups"] and pl["grid_z"] == 1
     assert pl["block_threads"] == 256 and pl["tma"] == 0  # 56-byte rows: cp.async
     assert pl["smem_bytes"] <= 200 * 1024
     L, info, pl = plan("vgg3x3", 16, batch_hint=16)
-    assert pl["cluster"] == 1 and pl["push"] == 0 and pl["tma"] == 1
+    assert pl["cluster"] == 1 and pl["push"] == 0 and pl["tma"] == 1 and pl["pdl"] == 1
     assert pl["grid_x"] * pl["grid_y"] == 16 * info["tiles_y"] * info["tiles_x"] * info["groups"]
+    L, info, pl = plan("sweep80", 8, batch_hint=8)  # dense-tap groups, several waves
+    assert info["dense_groups"] > 0 and pl["grid_x"] * pl["grid_y"] > 2 * 152
+    assert pl["pdl"] == 0
     L, info, pl = plan("vgg3x3", 16, fmt="ws")
     assert pl["kernel"] == 1 and pl["cluster"] == 1
     assert (pl["grid_x"], pl["grid_y"], pl["grid_z"]) == (L.M, info["tiles_y"] * info["tiles_x"],

@@ -108,3 +108,43 @@ def test_forward_ex_rejects_unknown_activation():
                                       None)
     assert rc == _lib.SPCONV_ERR_MISMATCH  # host-only handle
     w.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("hw", [14, 16])  # 14: cp.async staging + cluster; 16: TMA staging
+def test_ping_pong_chain_back_to_back(hw):
+    """Ten layers launched back to back on one stream, alternating between two
+    buffers: each layer reads what the previous one wrote and overwrites what
+    the one before it read.  A kernel may start while the previous one
+    finishes (programmatic dependent launch) and must still see that order.
+    Each row has two nonzeros of +-1 (the centre tap of one permuted channel,
+    the corner tap of another), so values at most double per layer and stay
+    exact: the result must equal the oracle applied layer by layer."""
+    rng = np.random.default_rng(21 + hw)
+    N, C, H, W, K = 1, 64, hw, hw, 3
+    layers = []
+    for _ in range(10):
+        perm, perm2 = rng.permutation(C), rng.permutation(C)
+        rows = [sorted({(int(perm[m]) * K + 1) * K + 1, (int(perm2[m]) * K) * K}) for m in range(C)]
+        rowptr = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
+        colidx = np.concatenate(rows).astype(np.int32)
+        value = rng.choice(np.array([-1, 1], np.float32), size=colidx.size)
+        layers.append((rowptr, colidx, value))
+    x0 = rng.integers(0, 8, size=(N, C, H, W)).astype(np.float32)
+    ws = [swd.pack(rp, ci, v, C=C, H=H, W=W, M=C, R=K, S=K, stride=1, pad=1, batch_hint=1)
+          for rp, ci, v in layers]
+    a = torch.from_numpy(x0).cuda()
+    b = torch.empty_like(a)
+    torch.cuda.synchronize()
+    src, dst = a, b
+    for w in ws:
+        swd.forward(src, w, out=dst)
+        src, dst = dst, src
+    torch.cuda.synchronize()
+    got = src.cpu().numpy().astype(np.float64)
+    ref = x0.astype(np.float64)
+    for rp, ci, v in layers:
+        ref, _ = oracle.csr(ref, rp, ci, v, C, K, K, 1, 1)
+    assert np.array_equal(got, ref)
+    for w in ws:
+        w.close()
