@@ -287,7 +287,9 @@ static __device__ __forceinline__ void apply_entry(float (&acc)[P], const float 
         acc[r] = fmaf(v, s[r * (ROW_STEP ? ROW_STEP : row_step)], acc[r]);
 }
 
-template <int P, int ROW_STEP>
+// UNROLL: iterations (two entries each) unrolled; more shared loads in flight
+// per lane, where the registers allow it.
+template <int P, int ROW_STEP, int UNROLL>
 static __device__ __forceinline__ void run_segment(float (&acc)[P], const float *sb, const float2 *ent,
                                             int j, int j1, int row_step) {
     if ((j & 1) && j < j1) {  // head: bring j to a 16-byte boundary
@@ -295,6 +297,7 @@ static __device__ __forceinline__ void run_segment(float (&acc)[P], const float 
         apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
         ++j;
     }
+#pragma unroll UNROLL
     for (; j + 1 < j1; j += 2) {
         const float4 e = *reinterpret_cast<const float4 *>(ent + j);
         apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
@@ -559,7 +562,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             for (int q = 0; q < Q; ++q) {
                 const int j0 = (int)hdr[warp * Q + q];
                 const int j1 = (int)hdr[warp * Q + q + 1];
-                run_segment<P, ROW_STEP>(acc[q], sb, ent, j0, j1, row_step);
+                // Q = 8 instances are at the register cap: no unrolling there
+                run_segment<P, ROW_STEP, (Q >= 8 ? 1 : 4)>(acc[q], sb, ent, j0, j1, row_step);
             }
         } else if (!dense) {
             const uint32_t *ent = hdr + p.hdr_words;
