@@ -49,7 +49,8 @@ _CSRC = os.path.join(ROOT, "sparse_weight_direct_gb300", "csrc")
 KERNEL_SOURCES = {
     "spconv_fwd_kernel": [os.path.join(_CSRC, f) for f in (
         "spconv_kernel.cuh", "spconv_fwd.cu", "spconv_fwd_q1.cu", "spconv_fwd_q2.cu",
-        "spconv_fwd_q4.cu", "spconv_fwd_q8.cu", "spconv_host.cpp", "spconv_internal.h")],
+        "spconv_fwd_q4.cu", "spconv_fwd_q8.cu", "spconv_fwd_tm.cu", "spconv_host.cpp",
+        "spconv_internal.h")],
     "spconv_ws_kernel": [os.path.join(_CSRC, f) for f in (
         "spconv_kernel.cuh", "spconv_ws.cu", "spconv_host.cpp", "spconv_internal.h")],
 }
@@ -573,10 +574,10 @@ def main(argv=None):
                     help="graph: the K steps back to back from CUDA graphs over copies of the "
                          "data larger than L2 (throughput); flush: each step timed alone "
                          "after an L2 flush (latency, launch overhead included)")
-    ap.add_argument("--fmt", default="f32", choices=["f32", "packed32", "ws"],
+    ap.add_argument("--fmt", default="f32", choices=["f32", "packed32", "ws", "tmem"],
                     help="packed weight format (packed32: the first page's 32-bit words, "
                          "FP16; ws: the weight-stationary mapping, one output channel per "
-                         "block)")
+                         "block; tmem: the tensor-memory window path, 3x3 stride 1)")
     ap.add_argument("--compare-dense", action="store_true",
                     help="also time PyTorch's dense conv2d (cuDNN) on the same layer")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

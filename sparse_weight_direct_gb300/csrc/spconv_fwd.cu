@@ -30,7 +30,8 @@ __global__ void wait_selftest_kernel(unsigned int *flags, unsigned long long lim
     if (ok && threadIdx.x == 0) atomicOr(flags, 2u);
 }
 
-KernelFn pick(int S, int stride, int P, int Q, int LR) {
+KernelFn pick(int S, int stride, int P, int Q, int LR, bool tm = false) {
+    if (tm) return (S == 3 && stride == 1 && LR == 1) ? pick_tm(P, Q) : nullptr;
     switch (Q) {
         case 1: return pick_q1(S, stride, P, LR);
         case 2: return pick_q2(S, stride, P, LR);
@@ -76,8 +77,12 @@ bool dense_taps_supported(int R, int S, int stride, int LR, int Q) {
     return stride == 1 && R == S && (S == 3 || (S == 5 && LR == 1)) && Q <= 4;
 }
 
-int forward_variant_supported(int S, int stride, int P, int Q, int LR) {
-    return pick(S, stride, P, Q, LR) ? 0 : -1;
+int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm) {
+    return pick(S, stride, P, Q, LR, tm) ? 0 : -1;
+}
+
+bool tm_supported(int R, int S, int stride, int LR) {
+    return R == 3 && S == 3 && stride == 1 && LR == 1;
 }
 
 // Shared memory of the stage buffers a block with `split` cluster ranks uses.
@@ -110,14 +115,17 @@ size_t forward_smem_bytes(const Geometry &g, int split) {
     // room for the partial sums of split rows / a channel-split cluster
     const size_t part = (size_t)g.warps * g.slots * g.tile_rows * 32 * sizeof(float);
     if (part > bytes) bytes = part;
-    return bytes + 128;  // room to align the stage buffers to 128 bytes
+    bytes += 128;  // room to align the stage buffers to 128 bytes
+    if (g.format == 3 && bytes < kTmMinSmem) bytes = kTmMinSmem;
+    return bytes;
 }
 
 cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast, bool pdl,
                            const float *x, float *y, const float *bias, int act,
                            const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream) {
-    KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows);
-    if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks)
+    const bool tm = g.format == 3;
+    KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows, tm);
+    if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks || (tm && split != 1))
         return cudaErrorInvalidConfiguration;
     const size_t smem = forward_smem_bytes(g, split);
     if (smem > 48 * 1024) {
