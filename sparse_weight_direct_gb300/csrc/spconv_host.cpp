@@ -826,9 +826,6 @@ bool choose_group_fast(const spconv::Geometry &g, int N, int64_t nnz) {
     return restream_s * 4.0 > compute_s;
 }
 
-// Blocks per cluster along the channel chunks: none when the grid already
-// fills the GPU, else enough for about two blocks per SM (measured best on
-// the one-image ResNet-style layer).
 // Programmatic dependent launch hides a launch's start-up behind the previous
 // kernel's tail: worth most for the short one-wave launches of small layers
 // (one-image ResNet layer 8.6 -> 7.3 us back to back).  Measured to cost 4 %
@@ -840,6 +837,10 @@ bool choose_pdl(const spconv::Geometry &g, int N, int split, bool group_fast) {
     return !(g.dense_groups > 0 && (int64_t)gx * gy > 2 * kSMs);
 }
 
+// Blocks per cluster along the channel chunks: none when the grid already
+// fills the GPU (splitting it further measured slower on every batched layer)
+// or on the tensor-memory path, else enough for about two blocks per SM
+// (measured best on the one-image ResNet-style layer).
 int choose_split(const spconv::Geometry &g, int N) {
     const int64_t blocks = (int64_t)N * g.tiles_y * g.tiles_x * g.groups;
     if (blocks >= kSMs || g.format == SPCONV_FORMAT_TMEM) return 1;
