@@ -231,6 +231,8 @@ typedef struct spconv_packed_info {
     int32_t blob_stride;      /* bytes between consecutive blobs when they are  */
                               /* stored at a fixed stride (nearly equal sizes,  */
                               /* each padded to the largest), else 0            */
+    int32_t tap_pairs;        /* 1: sparse blobs also hold pair entries (see   */
+                              /* SPCONV_ARRAY_BLOBS)                           */
 } spconv_packed_info;
 
 /* For a SPCONV_FORMAT_WS handle: tile_rows, lane_rows, tile_cols, tiles_y and
@@ -272,8 +274,17 @@ typedef enum spconv_array {
                                /* uint32 entry indices (slot w*Q+q spans           */
                                /* [hdr[w*Q+q], hdr[w*Q+q+1])), then entries of     */
                                /* {float value, int32 offset} (F32) or 32-bit      */
-                               /* packed words (PACKED32).  TMEM: hdr_words words  */
-                               /* = warps + 1 first entries of each warp, then     */
+                               /* packed words (PACKED32).  With tap_pairs (F32,   */
+                               /* Q = 2 or 4 slots per warp, NP = Q(Q-1)/2): next  */
+                               /* come warps*NP + 1 words hp of pair ranges in     */
+                               /* 8-byte units -- warp w's pair p (slots q1 < q2,  */
+                               /* numbered in lexicographic order) spans           */
+                               /* [hp[w*NP+p], hp[w*NP+p+1]) -- and the pair       */
+                               /* entries are 16 bytes {float value of q1, float   */
+                               /* value of q2, int32 offset, 0}: a tap both slots  */
+                               /* use, from a 16-byte boundary.  TMEM: hdr_words   */
+                               /* words = warps + 1 first entries of each warp,    */
+                               /* then                                             */
                                /* [warp][chunk] words of 4-bit entry counts (bits  */
                                /* 4q..4q+3: slot q), padded to 4 words; entries    */
                                /* {float value, uint32 column (3r + s) * 8} per    */

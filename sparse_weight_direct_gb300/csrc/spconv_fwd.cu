@@ -30,8 +30,9 @@ __global__ void wait_selftest_kernel(unsigned int *flags, unsigned long long lim
     if (ok && threadIdx.x == 0) atomicOr(flags, 2u);
 }
 
-KernelFn pick(int S, int stride, int P, int Q, int LR, bool tm = false) {
+KernelFn pick(int S, int stride, int P, int Q, int LR, bool tm = false, bool pairs = false) {
     if (tm) return (S == 3 && stride == 1 && LR == 1) ? pick_tm(P, Q) : nullptr;
+    if (pairs) return pick_pairs(S, stride, P, Q, LR);
     switch (Q) {
         case 1: return pick_q1(S, stride, P, LR);
         case 2: return pick_q2(S, stride, P, LR);
@@ -77,8 +78,8 @@ bool dense_taps_supported(int R, int S, int stride, int LR, int Q) {
     return stride == 1 && R == S && (S == 3 || (S == 5 && LR == 1)) && Q <= 4;
 }
 
-int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm) {
-    return pick(S, stride, P, Q, LR, tm) ? 0 : -1;
+int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm, bool pairs) {
+    return pick(S, stride, P, Q, LR, tm, pairs) ? 0 : -1;
 }
 
 bool tm_supported(int R, int S, int stride, int LR) {
@@ -124,7 +125,7 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
                            const float *x, float *y, const float *bias, int act,
                            const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream) {
     const bool tm = g.format == 3;
-    KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows, tm);
+    KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows, tm, g.tap_pairs != 0);
     if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks || (tm && split != 1))
         return cudaErrorInvalidConfiguration;
     const size_t smem = forward_smem_bytes(g, split);

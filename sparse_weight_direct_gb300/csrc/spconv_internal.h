@@ -82,7 +82,10 @@ struct Geometry {
                       // 2 = weight-stationary rows (one output channel per block),
                       // 3 = {fp32, tensor-memory column} entries (tensor-memory path)
     int batch_hint;   // batch size the plan targets (0 = unknown)
-    int hdr_words;    // words of a sparse blob header (warps * slots + 1, to 4)
+    int hdr_words;    // words of a sparse blob header (warps * slots + 1, to 4; with
+                      // tap pairs + warps * slot pairs + 1)
+    int tap_pairs;    // 1: sparse blobs also hold pair entries -- a tap two slots of a
+                      // warp share, applied to both from one set of shared loads
     int dense_groups; // leading groups whose blobs are dense-tap (0 if none)
     int split_rows;   // 1 if any group has rows split into parts (bit 1 of its flags)
     int dense_mask_words;  // words of a dense blob's slot masks (warps * chunk, to 4)
@@ -101,8 +104,10 @@ struct DeviceArrays {
 };
 
 // Kernel variants compiled for sm_103a.  Returns 0 if (S, stride, P, Q, LR)
-// has an instance (tm: of the tensor-memory window path), else -1.
-int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm = false);
+// has an instance (tm: of the tensor-memory window path; pairs: with tap-pair
+// segments), else -1.
+int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm = false,
+                              bool pairs = false);
 
 // Whether a layer shape can take the tensor-memory window path (3 x 3,
 // stride 1, one lane row).

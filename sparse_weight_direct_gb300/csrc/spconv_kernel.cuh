@@ -309,6 +309,42 @@ static __device__ __forceinline__ void run_segment(float (&acc)[P], const float 
     }
 }
 
+// A pair entry: a tap that two of the warp's output channels share.  Its P
+// inputs are loaded once and feed both channels' accumulators.
+template <int P, int ROW_STEP>
+static __device__ __forceinline__ void apply_pair(float (&a)[P], float (&b)[P], const float *sb,
+                                                  float va, float vb, int off, int row_step) {
+    const float *s = sb + off;
+#pragma unroll
+    for (int r = 0; r < P; ++r) {
+        const float x = s[r * (ROW_STEP ? ROW_STEP : row_step)];
+        a[r] = fmaf(va, x, a[r]);
+        b[r] = fmaf(vb, x, b[r]);
+    }
+}
+
+// The warp's pair segments, one per slot pair (q1 < q2, lexicographic): hp
+// holds their ranges in 8-byte units, each pair entry 16 bytes {w1, w2,
+// offset, 0} starting on a 16-byte boundary.
+template <int P, int Q, int ROW_STEP>
+static __device__ __forceinline__ void run_pairs(float (&acc)[Q][P], const float *sb,
+                                                 const uint32_t *hp, const float4 *ent4,
+                                                 int row_step) {
+#pragma unroll
+    for (int q1 = 0; q1 < Q; ++q1)
+#pragma unroll
+        for (int q2 = q1 + 1; q2 < Q; ++q2) {
+            const int k = q1 * Q - q1 * (q1 + 1) / 2 + (q2 - q1 - 1);
+            const int j1 = (int)(hp[k + 1] >> 1);
+#pragma unroll 2
+            for (int j = (int)(hp[k] >> 1); j < j1; ++j) {
+                const float4 e = ent4[j];
+                apply_pair<P, ROW_STEP>(acc[q1], acc[q2], sb, e.x, e.y, __float_as_int(e.z),
+                                        row_step);
+            }
+        }
+}
+
 // Dense-tap accumulation of one chunk for a warp of dense output channels: the
 // channel's input window (LR*(P-1)+K rows x K columns around this lane's output
 // column) is loaded into registers once and every tap of every slot of the
@@ -523,12 +559,20 @@ static __device__ __forceinline__ void run_tm_chunk(float (&acc)[Q][P], const fl
 
 // P: output rows per lane; Q: output channels per warp; LR: lane rows (1, or 2
 // interleaved half-warps of 16 lanes for outputs at most 16 wide); S_CT/ST_CT:
-// kernel width and stride when known at compile time (0 = read from p); TM:
-// the tensor-memory window path (3 x 3, stride 1, one lane row).
-template <int P, int Q, int S_CT, int ST_CT, int LR, int TM = 0>
+// kernel width and stride when known at compile time (0 = read from p); MODE:
+// 0 the shared-memory path, kModeTmem the tensor-memory window path (3 x 3,
+// stride 1, one lane row), kModePairs the shared-memory path with tap-pair
+// segments (blobs of the tap-pair layout).  The pair loop lives in instances
+// of its own: compiled into the plain ones it slowed layers that never use it.
+constexpr int kModeTmem = 1;
+constexpr int kModePairs = 2;
+template <int P, int Q, int S_CT, int ST_CT, int LR, int MODE = 0>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     spconv_fwd_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap) {
+    constexpr bool TM = MODE == kModeTmem;
+    constexpr bool PAIRS = MODE == kModePairs;
     static_assert(!TM || (S_CT == 3 && ST_CT == 1 && LR == 1 && P <= 8), "tensor-memory path: 3x3, stride 1");
+    static_assert(!PAIRS || Q == 2 || Q == 4, "tap pairs: 2 or 4 output channels per warp");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar[2];
     __shared__ uint32_t tm_slot;   // tensor-memory address of the block's columns (TM)
@@ -727,6 +771,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                 // Q = 8 instances are at the register cap: no unrolling there
                 run_segment<P, ROW_STEP, (Q >= 8 ? 1 : 4)>(acc[q], sb, ent, j0, j1, row_step);
             }
+            if constexpr (PAIRS)
+                run_pairs<P, Q, ROW_STEP>(acc, sb, hdr + kWarps * Q + 1 + warp * (Q * (Q - 1) / 2),
+                                          reinterpret_cast<const float4 *>(ent), row_step);
         } else if (!dense) {
             const uint32_t *ent = hdr + p.hdr_words;
 #pragma unroll
@@ -946,6 +993,8 @@ KernelFn pick_q4(int S, int stride, int P, int LR);
 KernelFn pick_q8(int S, int stride, int P, int LR);
 // Tensor-memory window instances (3 x 3, stride 1, one lane row), Q in {4, 8}.
 KernelFn pick_tm(int P, int Q);
+// Tap-pair instances (Q = 4, one lane row; 3x3 and 5x5 stride 1, 11x11 stride 4).
+KernelFn pick_pairs(int S, int stride, int P, int Q, int LR);
 
 // Instantiates the kernels of one Q for the supported kernel widths, strides,
 // rows per lane and lane rows.

@@ -159,10 +159,40 @@ def decode_layout(w):
                         rows.setdefault(m, []).append(((c * R + r) * S + s, v))
                 continue
             ent = blob[hw * 4:].view([("value", "<f4"), ("off", "<i4")])
-            assert hdr[spg] <= ent.size
-            # padding past the last entry: to 16 bytes, or to the fixed blob stride
-            assert info["blob_stride"] or ent.size - hdr[spg] <= 1
-            assert not blob[hw * 4 + 8 * int(hdr[spg]):].any()
+            end = int(hdr[spg])
+            if info["tap_pairs"]:
+                # pair ranges after the single ranges; 16-byte pair entries
+                NP = Q * (Q - 1) // 2
+                assert Q in (2, 4) and hw == (spg + 1 + NW * NP + 1 + 3) // 4 * 4
+                hp = hdr[spg + 1:spg + 2 + NW * NP].astype(np.int64)
+                assert hp[0] == (end + 1) // 2 * 2 and np.all(np.diff(hp) >= 0)
+                assert np.all(hp % 2 == 0)
+                pair_of = [(a, b) for a in range(Q) for b in range(a + 1, Q)]
+                for w in range(NW):
+                    for pi, (q1, q2) in enumerate(pair_of):
+                        seg = blob[hw * 4 + 8 * hp[w * NP + pi]:hw * 4 + 8 * hp[w * NP + pi + 1]]
+                        pe = seg.view([("va", "<f4"), ("vb", "<f4"), ("off", "<i4"), ("z", "<i4")])
+                        assert not pe["z"].any()
+                        for q, key in ((q1, "va"), (q2, "vb")):
+                            m = int(slot_oc[(g * NW + w) * Q + q])
+                            assert m >= 0 or pe.size == 0
+                            for e in pe:
+                                off = int(e["off"])
+                                cl, rem = divmod(off, info["plane"])
+                                r, qq = divmod(rem, info["row_pitch"])
+                                if st == 1:
+                                    s = qq - info["shift"]
+                                else:
+                                    phase, qq2 = divmod(qq, info["phase_pitch"])
+                                    s = qq2 * st + phase
+                                c = k * info["chunk"] + cl
+                                rows.setdefault(m, []).append(((c * R + r) * S + s, float(e[key])))
+                end = int(hp[-1])
+            assert end <= ent.size
+            # padding past the last entry: to 16 bytes (with pairs, plus the 8 bytes
+            # reserved for their alignment), or to the fixed blob stride
+            assert info["blob_stride"] or ent.size - end <= (3 if info["tap_pairs"] else 1)
+            assert not blob[hw * 4 + 8 * end:].any()
             for ls in range(spg):
                 m = int(slot_oc[g * spg + ls])
                 seg = ent[hdr[ls]:hdr[ls + 1]]

@@ -316,3 +316,42 @@ def test_cluster_reduction_paths(heavy, integer):
     ref, mag = oracle.csr(x, rowptr, colidx, value, M, K, K, 1, 1)
     check(out.cpu().numpy().astype(np.float64), ref, mag, exact=integer,
           what=f"cluster heavy={heavy}")
+
+
+PAIR_CASES = [
+    # (N, C, H, W, M, R, S, stride, pad, density): plans with tap pairs (a fifth or
+    # more of the nonzeros share their tap with another output channel of the warp)
+    (4, 40, 30, 30, 128, 3, 3, 1, 1, 0.2),     # 3x3, ragged chunks, 30 of 32 columns
+    (4, 24, 27, 27, 128, 5, 5, 1, 2, 0.2),     # 5x5
+    (8, 3, 99, 99, 128, 11, 11, 4, 0, 0.2),    # 11x11 stride 4
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", PAIR_CASES, ids=[str(c) for c in PAIR_CASES])
+@pytest.mark.parametrize("integer", [False, True])
+@pytest.mark.parametrize("heavy", [False, True])
+def test_tap_pairs(case, integer, heavy):
+    """Layers planned with tap-pair entries (one set of shared loads feeding two
+    output channels of a warp), with uniform rows and with a few very dense
+    rows among them."""
+    N, C, H, W, M, R, S, st, pad, d = case
+    rng = np.random.default_rng(abs(hash(case)) % (2 ** 32) + 2 * integer + heavy)
+    CRS = C * R * S
+    rows = [np.nonzero(rng.random(CRS) < (0.95 if heavy and m % 17 == 3 else d))[0]
+            for m in range(M)]
+    rowptr = np.concatenate([[0], np.cumsum([r.size for r in rows])]).astype(np.int32)
+    colidx = np.concatenate(rows).astype(np.int32)
+    if integer:
+        value = rng.choice(np.array([-3, -2, -1, 1, 2, 3], np.float32), size=colidx.size)
+    else:
+        value = rng.normal(0, 0.05, size=colidx.size).astype(np.float32)
+    x = workloads.random_input((N, C, H, W), rng, integer=integer)
+    w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=R, S=S, stride=st, pad=pad,
+                      batch_hint=N)
+    info = w.info()
+    w.close()
+    assert info["tap_pairs"] == 1 and info["dense_groups"] == 0
+    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, R, S, st, pad, batch_hint=N)
+    ref, mag = oracle.csr(x, rowptr, colidx, value, M, R, S, st, pad)
+    check(got, ref, mag, exact=integer, what=f"pairs {case}")
