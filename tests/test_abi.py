@@ -419,3 +419,19 @@ def test_forward_rejects_host_only_handle_and_null():
     info = _lib.PackedInfo()
     assert L.spconv_packed_info_get(None, ctypes.byref(info)) == _lib.SPCONV_ERR_INVALID_ARG
     w.close()
+
+
+def test_launch_smem_within_limit_for_any_batch():
+    """Whatever batch size a plan was made for, a forward of any batch size asks
+    for at most the kernels' 200 KB of dynamic shared memory (the stages a block
+    runs depend on the chunks it gets, which depend on the launch's batch and
+    its cluster split)."""
+    for name, L in workloads.ALL_LAYERS.items():
+        rowptr, colidx, value = workloads.make_weights(L)
+        for hint in (0, 1, 4, 32, L.N):
+            w = swd.pack_host(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R,
+                              S=L.S, stride=L.stride, pad=L.pad, batch_hint=hint)
+            for n in (1, 2, 4, 16, 64, L.N):
+                li = w.launch_info(n)
+                assert li["smem_bytes"] <= 200 * 1024, (name, hint, n, li["smem_bytes"])
+            w.close()
