@@ -233,6 +233,11 @@ typedef struct spconv_packed_info {
                               /* each padded to the largest), else 0            */
     int32_t tap_pairs;        /* 1: sparse blobs also hold pair entries (see   */
                               /* SPCONV_ARRAY_BLOBS)                           */
+    int32_t plane_stage;      /* 1: the forward stages raw input planes (pitch */
+                              /* W after 16 zeroed words); F32 entry offsets   */
+                              /* are then (16 + c*H*W + (r-1)*W + (s-1)) << 4  */
+                              /* | flags: bit 0 s == 0, 1 s == 2, 2 r == 0,    */
+                              /* 3 r == 2                                      */
 } spconv_packed_info;
 
 /* For a SPCONV_FORMAT_WS handle: tile_rows, lane_rows, tile_cols, tiles_y and

@@ -51,7 +51,8 @@ class PackedInfo(ctypes.Structure):
         ("device_bytes", "smem_bytes", "max_warp_nnz", "mean_warp_nnz")] + [
         (n, ctypes.c_int32) for n in
         ("hdr_words", "blob_stage_bytes", "in_stage_bytes", "lane_rows", "dense_groups",
-         "dense_mask_words", "format", "batch_hint", "blob_stride", "tap_pairs")]
+         "dense_mask_words", "format", "batch_hint", "blob_stride", "tap_pairs",
+         "plane_stage")]
 
 
 class LaunchInfo(ctypes.Structure):

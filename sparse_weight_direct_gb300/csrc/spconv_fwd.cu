@@ -30,9 +30,11 @@ __global__ void wait_selftest_kernel(unsigned int *flags, unsigned long long lim
     if (ok && threadIdx.x == 0) atomicOr(flags, 2u);
 }
 
-KernelFn pick(int S, int stride, int P, int Q, int LR, bool tm = false, bool pairs = false) {
+KernelFn pick(int S, int stride, int P, int Q, int LR, bool tm = false, bool pairs = false,
+              bool plane = false) {
     if (tm) return (S == 3 && stride == 1 && LR == 1) ? pick_tm(P, Q) : nullptr;
     if (pairs) return pick_pairs(S, stride, P, Q, LR);
+    if (plane) return (S == 3 && stride == 1 && LR == 2) ? pick_plane(P, Q) : nullptr;
     switch (Q) {
         case 1: return pick_q1(S, stride, P, LR);
         case 2: return pick_q2(S, stride, P, LR);
@@ -78,8 +80,14 @@ bool dense_taps_supported(int R, int S, int stride, int LR, int Q) {
     return stride == 1 && R == S && (S == 3 || (S == 5 && LR == 1)) && Q <= 4;
 }
 
-int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm, bool pairs) {
-    return pick(S, stride, P, Q, LR, tm, pairs) ? 0 : -1;
+int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm, bool pairs,
+                              bool plane) {
+    return pick(S, stride, P, Q, LR, tm, pairs, plane) ? 0 : -1;
+}
+
+bool plane_stage_supported(int H, int W, int R, int S, int stride, int pad, int P, int LR, int Q) {
+    return R == 3 && S == 3 && stride == 1 && pad == 1 && LR == 2 && H == 2 * P && W >= 2 &&
+           W <= 16 && (W * 4) % 16 != 0 && (H * W) % 4 == 0 && pick(S, stride, P, Q, LR, false, false, true);
 }
 
 bool tm_supported(int R, int S, int stride, int LR) {
@@ -112,12 +120,18 @@ bool push_reduction(const Geometry &g, int split) {
 
 size_t forward_smem_bytes(const Geometry &g, int split) {
     size_t bytes = stages_bytes(g, split);
-    if (push_reduction(g, split)) return bytes + recv_bytes(g, split) + 128;
-    // room for the partial sums of split rows / a channel-split cluster
-    const size_t part = (size_t)g.warps * g.slots * g.tile_rows * 32 * sizeof(float);
-    if (part > bytes) bytes = part;
-    bytes += 128;  // room to align the stage buffers to 128 bytes
+    if (push_reduction(g, split)) {
+        bytes += recv_bytes(g, split) + 128;
+    } else {
+        // room for the partial sums of split rows / a channel-split cluster
+        const size_t part = (size_t)g.warps * g.slots * g.tile_rows * 32 * sizeof(float);
+        if (part > bytes) bytes = part;
+        bytes += 128;  // room to align the stage buffers to 128 bytes
+    }
     if (g.format == 3 && bytes < kTmMinSmem) bytes = kTmMinSmem;
+    // plane staging (one-image layers): at most two blocks per SM, as with the
+    // padded tile, so the cluster blocks spread over the SMs
+    if (g.plane_stage && bytes < 76 * 1024) bytes = 76 * 1024;
     return bytes;
 }
 
@@ -125,7 +139,8 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
                            const float *x, float *y, const float *bias, int act,
                            const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream) {
     const bool tm = g.format == 3;
-    KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows, tm, g.tap_pairs != 0);
+    KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows, tm, g.tap_pairs != 0,
+                       g.plane_stage != 0);
     if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks || (tm && split != 1))
         return cudaErrorInvalidConfiguration;
     const size_t smem = forward_smem_bytes(g, split);
@@ -160,6 +175,7 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
     p.push = push_reduction(g, split) ? 1 : 0;
     p.pairs = (g.stride == 1 && g.W % 2 == 0 && g.row_pitch % 2 == 0 && g.plane % 2 == 0) ? 1 : 0;
     p.recv_off = (int)stages_bytes(g, split);
+    p.plane_stage = g.plane_stage;
     CUtensorMap dummy;
     if (!tmap) {
         for (int i = 0; i < 16; ++i) dummy.opaque[i] = 0;

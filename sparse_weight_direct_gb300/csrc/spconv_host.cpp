@@ -179,6 +179,21 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     if (g.groups > 65535) return SPCONV_ERR_UNSUPPORTED;
     if (spconv::forward_variant_supported(S, stride, g.tile_rows, g.slots, g.lane_rows, tm) != 0)
         return SPCONV_ERR_UNSUPPORTED;
+    // Whole-image tiles of images whose rows TMA cannot address: one bulk copy
+    // of the chunk's raw planes (dense, pitch W) instead of per-element
+    // cp.async into a padded tile; the kernel applies the padding to the
+    // weights of the taps that leave the image.
+    g.plane_stage = 0;
+    if (g.format == SPCONV_FORMAT_F32 &&
+        spconv::plane_stage_supported(H, W, R, S, stride, pad, g.tile_rows, g.lane_rows, g.slots)) {
+        g.plane_stage = 1;
+        g.in_rows = H;
+        g.in_cols = W;
+        g.shift = 0;
+        g.phase_pitch = W;
+        g.row_pitch = W;
+        g.plane = H * W;
+    }
     return SPCONV_OK;
 }
 
@@ -197,7 +212,7 @@ int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx)
     const double crs = (double)g.C * g.R * g.S;
     auto nnz_of = [&](int m) { return (int64_t)rowptr[m + 1] - rowptr[m]; };
     std::vector<int> dense, sparse;
-    const bool can_dense = g.format != SPCONV_FORMAT_TMEM &&
+    const bool can_dense = g.format != SPCONV_FORMAT_TMEM && !g.plane_stage &&
                            spconv::dense_taps_supported(g.R, g.S, g.stride, g.lane_rows, g.slots);
     for (int m = 0; m < g.M; ++m)
         (can_dense && nnz_of(m) / crs >= kDenseRowMin ? dense : sparse).push_back(m);
@@ -361,7 +376,9 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
     // (the tensor-memory path runs without channel-split clusters)
     want_split = g.format == SPCONV_FORMAT_TMEM ? 1 : std::max(want_split, 1);
     int cap = std::min(C, 256);  // TMA box extent limit
-    if (want_split > 1 && C / want_split >= 32)
+    // Chunks small enough for the split (not below 32 channels; plane staging,
+    // whose stages are small, always: its layers are the one-image ones)
+    if (want_split > 1 && (C / want_split >= 32 || g.plane_stage))
         cap = std::min(cap, (C + want_split - 1) / want_split);
     // When the planned launch (known batch size) splits the chunks over a
     // cluster with one chunk per block, a single stage is enough: allow it up
@@ -375,7 +392,10 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
         // tensor-memory blobs: per-warp first entries + [warp][channel] counts
         if (tm) g.hdr_words = (int)round_up((size_t)g.warps * (chunk + 1) + 1, 4);
         const size_t hdr_bytes = (size_t)g.hdr_words * 4;
-        const size_t in_stage = round_up((size_t)chunk * g.plane * sizeof(float), 128);
+        const size_t in_stage = round_up(
+            ((size_t)chunk * g.plane +
+             (g.plane_stage ? spconv::kPlaneLead + spconv::kPlaneTail : 0)) * sizeof(float),
+            128);
         size_t blob_max = g.dense_groups ? dense_blob_bytes(g, chunk) : 0;
         for (int grp = g.dense_groups; grp < g.groups; ++grp) {
             const int64_t *pre = &gpre[(size_t)grp * (C + 1)];
@@ -422,7 +442,7 @@ int pair_index(int Q, int q1, int q2) { return q1 * Q - q1 * (q1 + 1) / 2 + (q2 
 void choose_tap_pairs(spconv::Geometry &g, const std::vector<int32_t> &group_flags,
                       const std::vector<std::vector<int64_t>> &order, const int32_t *colidx) {
     g.tap_pairs = 0;
-    if (g.format != SPCONV_FORMAT_F32 ||
+    if (g.format != SPCONV_FORMAT_F32 || g.plane_stage ||
         spconv::forward_variant_supported(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows,
                                           false, true) != 0)
         return;
@@ -680,11 +700,20 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
                     }
                     HostEntry h;
                     h.value = value[idx[t]];
-                    if (g.stride == 1)
+                    if (g.plane_stage) {
+                        // raw planes after the lead margin; bits 3:0 flag the
+                        // taps that can leave the image: bit 0 left column,
+                        // bit 1 right column, bit 2 top row, bit 3 bottom row
+                        const int32_t off = spconv::kPlaneLead + cl * g.plane + (r - 1) * g.W + (s - 1);
+                        const int32_t flags = (s == 0 ? 1 : 0) | (s == 2 ? 2 : 0) |
+                                              (r == 0 ? 4 : 0) | (r == 2 ? 8 : 0);
+                        h.off = (off << 4) | flags;
+                    } else if (g.stride == 1) {
                         h.off = cl * g.plane + r * g.row_pitch + s + g.shift;
-                    else
+                    } else {
                         h.off = cl * g.plane + r * g.row_pitch +
                                 (s % g.stride) * g.phase_pitch + s / g.stride;
+                    }
                     ent[e++] = h;
                 }
             }
@@ -1184,6 +1213,7 @@ __attribute__((visibility("default"))) int spconv_packed_info_get(const spconv_p
     info->dense_mask_words = g.dense_mask_words;
     info->blob_stride = g.blob_stride16 * 16;
     info->tap_pairs = g.tap_pairs;
+    info->plane_stage = g.plane_stage;
     return SPCONV_OK;
 }
 

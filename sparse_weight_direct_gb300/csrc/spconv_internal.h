@@ -86,6 +86,9 @@ struct Geometry {
                       // tap pairs + warps * slot pairs + 1)
     int tap_pairs;    // 1: sparse blobs also hold pair entries -- a tap two slots of a
                       // warp share, applied to both from one set of shared loads
+    int plane_stage;  // 1: the chunk's raw input planes are staged by one bulk copy
+                      // (whole-image tiles whose rows TMA cannot address) and the
+                      // padding is applied to the weights (see kPlaneLead)
     int dense_groups; // leading groups whose blobs are dense-tap (0 if none)
     int split_rows;   // 1 if any group has rows split into parts (bit 1 of its flags)
     int dense_mask_words;  // words of a dense blob's slot masks (warps * chunk, to 4)
@@ -107,11 +110,22 @@ struct DeviceArrays {
 // has an instance (tm: of the tensor-memory window path; pairs: with tap-pair
 // segments), else -1.
 int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm = false,
-                              bool pairs = false);
+                              bool pairs = false, bool plane = false);
 
 // Whether a layer shape can take the tensor-memory window path (3 x 3,
 // stride 1, one lane row).
 bool tm_supported(int R, int S, int stride, int LR);
+
+// Plane staging: zeroed words before and after the raw planes of a stage, so
+// that taps reaching past the first or last plane read finite values.
+constexpr int kPlaneLead = 16;
+constexpr int kPlaneTail = 48;
+
+// Whether a plan can stage raw planes: 3 x 3, pad 1, stride 1, two lane rows,
+// one tile covering the whole image (H = 2 P rows, W <= 16 columns), rows that
+// a TMA tensor map cannot address (4 W not a multiple of 16), and planes that
+// start on 16-byte boundaries (H W a multiple of 4).
+bool plane_stage_supported(int H, int W, int R, int S, int stride, int pad, int P, int LR, int Q);
 
 // Smallest dynamic shared memory of a tensor-memory launch: with more than
 // a third of an SM's shared memory per block at most two blocks share an SM,

@@ -76,6 +76,7 @@ struct KParams {
     int push;                // cluster reduction by remote stores into the owner's buffer
     int pairs;               // cp.async staging in 8-byte column pairs (stride 1, W even)
     int recv_off;            // byte offset of that receive buffer in shared memory
+    int plane_stage;         // raw planes staged by one bulk copy (kModePlane instances)
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -306,6 +307,50 @@ static __device__ __forceinline__ void run_segment(float (&acc)[P], const float 
     if (j < j1) {  // tail
         const float2 e = ent[j];
         apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
+    }
+}
+
+// Plane staging (whole-image tiles, 3 x 3, pad 1): the stage holds the raw
+// input planes, pitch W, after kPlaneLead zeroed words, so a tap's input is at
+// lane base + offset + p * row_step with no padding in shared memory.  The
+// padding is applied to the weight instead: an entry's low 4 bits flag the
+// sides its tap can leave the image by (bit 0 left column, 1 right column, 2
+// the row above, 3 the row below); lanebits holds the sides this lane's
+// outputs touch (its column is the first / last, its lane row holds the top
+// row at p = 0 / the bottom row at p = P - 1), and a tap that leaves the image
+// there reads a finite neighbour with weight zero.
+template <int P>
+static __device__ __forceinline__ void apply_entry_plane(float (&acc)[P], const float *sb, float v,
+                                                         uint32_t code, int row_step,
+                                                         uint32_t lanebits) {
+    const float *s = sb + (code >> 4);
+    const uint32_t hit = code & lanebits;
+    const float wc = (hit & 3u) ? 0.f : v;
+    const float w0 = (hit & 4u) ? 0.f : wc;
+    const float wl = (hit & 8u) ? 0.f : wc;
+#pragma unroll
+    for (int r = 0; r < P; ++r)
+        acc[r] = fmaf(r == 0 ? w0 : (r == P - 1 ? wl : wc), s[r * row_step], acc[r]);
+}
+
+template <int P, int UNROLL>
+static __device__ __forceinline__ void run_segment_plane(float (&acc)[P], const float *sb,
+                                                         const float2 *ent, int j, int j1,
+                                                         int row_step, uint32_t lanebits) {
+    if ((j & 1) && j < j1) {  // head: bring j to a 16-byte boundary
+        const float2 e = ent[j];
+        apply_entry_plane<P>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
+        ++j;
+    }
+#pragma unroll UNROLL
+    for (; j + 1 < j1; j += 2) {
+        const float4 e = *reinterpret_cast<const float4 *>(ent + j);
+        apply_entry_plane<P>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
+        apply_entry_plane<P>(acc, sb, e.z, __float_as_uint(e.w), row_step, lanebits);
+    }
+    if (j < j1) {  // tail
+        const float2 e = ent[j];
+        apply_entry_plane<P>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
     }
 }
 
@@ -566,11 +611,14 @@ static __device__ __forceinline__ void run_tm_chunk(float (&acc)[Q][P], const fl
 // of its own: compiled into the plain ones it slowed layers that never use it.
 constexpr int kModeTmem = 1;
 constexpr int kModePairs = 2;
+constexpr int kModePlane = 3;  // plane staging (see apply_entry_plane)
 template <int P, int Q, int S_CT, int ST_CT, int LR, int MODE = 0>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     spconv_fwd_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap) {
     constexpr bool TM = MODE == kModeTmem;
     constexpr bool PAIRS = MODE == kModePairs;
+    constexpr bool PLANE = MODE == kModePlane;
+    static_assert(!PLANE || (S_CT == 3 && ST_CT == 1 && LR == 2), "plane staging: 3x3, two lane rows");
     static_assert(!TM || (S_CT == 3 && ST_CT == 1 && LR == 1 && P <= 8), "tensor-memory path: 3x3, stride 1");
     static_assert(!PAIRS || Q == 2 || Q == 4, "tap pairs: 2 or 4 output channels per warp");
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -582,9 +630,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     unsigned char *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     constexpr int LC = kLanes / LR;  // lanes per lane row = output columns of a tile
     constexpr int ROW_STEP =
-        S_CT ? LR * (ST_CT == 1 ? row_pitch_s1(S_CT, LR)
-                                : ST_CT * ST_CT * phase_pitch_for(S_CT, ST_CT))
-             : 0;
+        (S_CT && !PLANE) ? LR * (ST_CT == 1 ? row_pitch_s1(S_CT, LR)
+                                            : ST_CT * ST_CT * phase_pitch_for(S_CT, ST_CT))
+                         : 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ly = lane / LC, lx = lane % LC;  // lane row / column of this thread
     const int st = ST_CT ? ST_CT : p.stride;
@@ -631,6 +679,16 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         issued[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    }
+    if constexpr (PLANE) {
+        // stage input regions start zeroed: the margins (and a last, partial
+        // chunk's tail) are read by taps that leave the image, with weight 0
+        const int nz = (nmine > 1 ? 2 : 1) * (p.stage_bytes / 16);
+        float4 *z = reinterpret_cast<float4 *>(smem);
+        for (int i = threadIdx.x; i < nz; i += blockDim.x) {
+            const int sidx = i / (p.stage_bytes / 16);
+            if ((i - sidx * (p.stage_bytes / 16)) * 16 < p.in_stage_bytes) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     if constexpr (TM) tm_fence_before();
     __syncthreads();
@@ -690,8 +748,22 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                 blob_bytes = (o1 - o0) * 16u;
             }
             asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-            mbar_expect_tx(&bar[s], blob_bytes + (p.use_tma ? (uint32_t)p.in_tma_bytes : 0u));
+            const uint32_t in_bytes =
+                PLANE ? (uint32_t)(min(p.chunk, p.C - c0) * p.H * p.W) * 4u
+                      : (p.use_tma ? (uint32_t)p.in_tma_bytes : 0u);
+            mbar_expect_tx(&bar[s], blob_bytes + in_bytes);
             bulk_load(base + p.in_stage_bytes, p.blobs + (size_t)o0 * 16u, blob_bytes, &bar[s]);
+        }
+        if constexpr (PLANE) {
+            // the chunk's planes are contiguous in the input (and start on a
+            // 16-byte boundary: H * W is a multiple of 4)
+            if (issuer && input) {
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                const size_t hw = (size_t)p.H * p.W;
+                bulk_load(base + kPlaneLead * sizeof(float), p.x + ((size_t)n * p.C + c0) * hw,
+                          (uint32_t)(min(p.chunk, p.C - c0) * hw * sizeof(float)), &bar[s]);
+            }
+            return;
         }
         if (issuer && input && p.use_tma)
             tma_load_4d(base, &tmap, ix0 - p.shift, iy0, c0, n, &bar[s]);
@@ -725,14 +797,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     if (nmine > 1) issue(k_begin + 1, 1, threadIdx.x == 0, false, true);
     for (int it = 0; it < nmine && !failed; ++it) {
         const int s = it & 1;
-        if (!p.use_tma) {
+        if (!p.use_tma && !PLANE) {
             if (it + 1 < nmine)
                 cp_async_wait_all_but_one();
             else
                 cp_async_wait_all();
         }
         const bool ok = mbar_wait_bounded(&bar[s], (uint32_t)((it >> 1) & 1));
-        if (p.use_tma) {
+        if (p.use_tma || PLANE) {
             // warps run independently (on the tensor-memory path, in pairs);
             // a warp that timed out stops, with its partner
             if constexpr (TM)
@@ -745,6 +817,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (failed) break;
         const unsigned char *base = smem + (size_t)s * p.stage_bytes;
         const float *sb = reinterpret_cast<const float *>(base) + ly * st * p.row_pitch + lx;
+        if constexpr (PLANE) {
+            // dense planes: lanes past the image's width read the spare banks
+            // 2W .. 31 (finite values, outputs discarded), so the 32 reads of a
+            // load stay in distinct banks
+            sb = reinterpret_cast<const float *>(base) +
+                 (lx < p.W ? ly * p.W + lx : 2 * p.W + ly * (LC - p.W) + (lx - p.W));
+        }
         const uint32_t *hdr = reinterpret_cast<const uint32_t *>(base + p.in_stage_bytes);
         if constexpr (TM) {
             const float2 *ent = reinterpret_cast<const float2 *>(hdr + p.hdr_words);
@@ -752,7 +831,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             run_tm_chunk<P, Q, row_pitch_s1(3, 1)>(acc, sb + p.shift, hdr, ent, warp, p.chunk,
                                                     min(p.chunk, p.C - k * p.chunk), p.plane,
                                                     tbase);
-        } else if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4) {
+        } else if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4 && !PLANE) {
             if (dense) {
                 const int k = k_begin + it;
                 run_dense_chunk<P, Q, S_CT, LR, row_pitch_s1(S_CT, LR)>(
@@ -768,8 +847,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             for (int q = 0; q < Q; ++q) {
                 const int j0 = (int)hdr[warp * Q + q];
                 const int j1 = (int)hdr[warp * Q + q + 1];
-                // Q = 8 instances are at the register cap: no unrolling there
-                run_segment<P, ROW_STEP, (Q >= 8 ? 1 : 4)>(acc[q], sb, ent, j0, j1, row_step);
+                if constexpr (PLANE) {
+                    const uint32_t lanebits = (lx == 0 ? 1u : 0u) | (lx == p.W - 1 ? 2u : 0u) |
+                                              (ly == 0 ? 4u : 0u) | (ly == LR - 1 ? 8u : 0u);
+                    run_segment_plane<P, 4>(acc[q], sb, ent, j0, j1, row_step, lanebits);
+                } else {
+                    // Q = 8 instances are at the register cap: no unrolling there
+                    run_segment<P, ROW_STEP, (Q >= 8 ? 1 : 4)>(acc[q], sb, ent, j0, j1, row_step);
+                }
             }
             if constexpr (PAIRS)
                 run_pairs<P, Q, ROW_STEP>(acc, sb, hdr + kWarps * Q + 1 + warp * (Q * (Q - 1) / 2),
@@ -783,7 +868,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                 run_segment_words<P, ROW_STEP, ST_CT>(acc[q], sb, ent, j0, j1, p, row_step);
             }
         }
-        if (p.use_tma) {
+        if (p.use_tma || PLANE) {
             // Release stage s without a block barrier: each warp counts itself
             // out; the warp that completes the count refills the stage (its
             // generic-proxy reads are ordered before the async-proxy copy by
@@ -821,7 +906,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (warp == 0) tm_dealloc(tm_slot);
     }
     if (failed) {
-        if (!p.use_tma) cp_async_wait_all();
+        if (!p.use_tma && !PLANE) cp_async_wait_all();
         if (threadIdx.x == 0) {
             atomicOr(p.err, 1u);
             for (int st2 = 0; st2 < 2; ++st2)
@@ -995,6 +1080,8 @@ KernelFn pick_q8(int S, int stride, int P, int LR);
 KernelFn pick_tm(int P, int Q);
 // Tap-pair instances (Q = 4, one lane row; 3x3 and 5x5 stride 1, 11x11 stride 4).
 KernelFn pick_pairs(int S, int stride, int P, int Q, int LR);
+// Plane-staging instances (3x3 stride 1, two lane rows, Q in {1, 2}).
+KernelFn pick_plane(int P, int Q);
 
 // Instantiates the kernels of one Q for the supported kernel widths, strides,
 // rows per lane and lane rows.

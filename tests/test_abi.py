@@ -201,11 +201,20 @@ def decode_layout(w):
                     continue
                 for e in seg:
                     off = int(e["off"])
-                    cl, rem = divmod(off, info["plane"])
-                    r, q = divmod(rem, info["row_pitch"])
-                    if st == 1:
+                    if info["plane_stage"]:
+                        # raw planes after 16 zeroed words; low bits flag the
+                        # sides the tap can leave the image by
+                        flags, off = off & 15, (off >> 4) - 16 + info["W"] + 1
+                        cl, rem = divmod(off, info["plane"])
+                        r, s = divmod(rem, info["W"])
+                        assert flags == (s == 0) | (s == 2) << 1 | (r == 0) << 2 | (r == 2) << 3
+                    elif st == 1:
+                        cl, rem = divmod(off, info["plane"])
+                        r, q = divmod(rem, info["row_pitch"])
                         s = q - info["shift"]
                     else:
+                        cl, rem = divmod(off, info["plane"])
+                        r, q = divmod(rem, info["row_pitch"])
                         phase, qq = divmod(q, info["phase_pitch"])
                         assert phase < st
                         s = qq * st + phase
@@ -247,8 +256,11 @@ def test_packed_layout_decodes_to_csr(name, fmt):
     # staged input tile covers every tap of every output of a tile
     tile_h = info["tile_rows"] * info["lane_rows"]
     assert info["tile_cols"] * info["lane_rows"] == 32
-    assert info["in_rows"] == (tile_h - 1) * L.stride + L.R
-    assert info["in_cols"] == (info["tile_cols"] - 1) * L.stride + L.S
+    if info["plane_stage"]:  # whole raw planes, the padding applied to the weights
+        assert info["in_rows"] == L.H == tile_h and info["in_cols"] == L.W <= info["tile_cols"]
+    else:
+        assert info["in_rows"] == (tile_h - 1) * L.stride + L.R
+        assert info["in_cols"] == (info["tile_cols"] - 1) * L.stride + L.S
     assert info["tiles_y"] * tile_h >= L.E
     assert info["tiles_x"] * info["tile_cols"] >= L.F
     assert info["smem_bytes"] <= 200 * 1024

@@ -355,3 +355,41 @@ def test_tap_pairs(case, integer, heavy):
     got = run_gpu(x, rowptr, colidx, value, C, H, W, M, R, S, st, pad, batch_hint=N)
     ref, mag = oracle.csr(x, rowptr, colidx, value, M, R, S, st, pad)
     check(got, ref, mag, exact=integer, what=f"pairs {case}")
+
+
+PLANE_CASES = [
+    # (N, C, H, W, M, density, heavy): whole-image tiles whose rows TMA cannot address,
+    # staged as raw planes with the padding applied to the weights
+    (1, 40, 14, 10, 24, 0.3, False),    # W = 10, ragged chunks
+    (2, 33, 16, 13, 20, 0.3, False),    # P = 8, odd width, odd channel count
+    (1, 64, 14, 6, 70, 0.2, False),     # W = 6, M not a multiple of the group size
+    (1, 20, 14, 2, 9, 0.5, False),      # W = 2: every lane but two reads spare banks
+    (1, 128, 14, 14, 64, 0.1, True),    # very dense rows split into parts
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", PLANE_CASES, ids=[str(c) for c in PLANE_CASES])
+@pytest.mark.parametrize("integer", [False, True])
+def test_plane_staging(case, integer):
+    N, C, H, W, M, d, heavy = case
+    rng = np.random.default_rng(abs(hash(case)) % (2 ** 32) + integer)
+    CRS = C * 9
+    rows = [np.nonzero(rng.random(CRS) < (0.9 if heavy and m % 20 == 0 else d))[0]
+            for m in range(M)]
+    rowptr = np.concatenate([[0], np.cumsum([r.size for r in rows])]).astype(np.int32)
+    colidx = np.concatenate(rows).astype(np.int32)
+    if integer:
+        value = rng.choice(np.array([-3, -2, -1, 1, 2, 3], np.float32), size=colidx.size)
+    else:
+        value = rng.normal(0, 0.05, size=colidx.size).astype(np.float32)
+    x = workloads.random_input((N, C, H, W), rng, integer=integer)
+    w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=3, S=3, stride=1, pad=1,
+                      batch_hint=N)
+    info = w.info()
+    assert info["plane_stage"] == 1
+    assert not heavy or (w.array("group_flags") & 2).any()
+    w.close()
+    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 3, 3, 1, 1, batch_hint=N)
+    ref, mag = oracle.csr(x, rowptr, colidx, value, M, 3, 3, 1, 1)
+    check(got, ref, mag, exact=integer, what=f"plane {case}")
