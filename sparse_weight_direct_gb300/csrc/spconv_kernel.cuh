@@ -16,7 +16,9 @@
 //     page: each input region is read once per block and reused by all of the
 //     block's output channels and rows), fetched by one TMA tensor copy with
 //     hardware zero fill for the padding, or by cp.async where the input row
-//     stride is not 16-byte aligned; and
+//     stride is not 16-byte aligned (whole-image 3x3 tiles of such inputs
+//     instead stage the raw planes with one bulk copy and apply the padding
+//     to the weights: kModePlane); and
 //   * the chunk's weight blob of the block's channel group (a header of per-warp
 //     entry ranges, then 8-byte (value, offset) entries), fetched by one bulk
 //     asynchronous copy.
