@@ -405,9 +405,7 @@ def run_ours(args, L):
             flush.zero_()
             if i >= 2:
                 es[i - 2].record(stream)
-            x.copy_(x_pin, non_blocking=True)
-            swd.forward(x, w, out=y, stream=stream)
-            y_pin.copy_(y, non_blocking=True)
+            swd.forward_host(x_pin, w, y_pin, x, y, stream=stream)  # copy in, forward, copy out
             if i >= 2:
                 ee[i - 2].record(stream)
         torch.cuda.synchronize(dev)

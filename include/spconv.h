@@ -21,7 +21,8 @@
  *    throws or prints; spconv_status_string() names a status.
  *  - Tensors are contiguous row-major: X is N x C x H x W, Y is N x M x E x F,
  *    both float32 in device memory of the device that was current when the
- *    handle was packed.
+ *    handle was packed (spconv_forward_host: in host memory, with device
+ *    workspaces).
  *  - "stream" is a cudaStream_t passed as void* (NULL = legacy default stream).
  *  - All shape arguments are int; sizes are validated before any device work.
  */
@@ -154,6 +155,37 @@ typedef enum spconv_act { SPCONV_ACT_NONE = 0, SPCONV_ACT_RELU = 1 } spconv_act;
 int spconv_forward_ex(int N, int C, int H, int W, int M, int R, int S, int stride, int pad,
                       const float *input, const spconv_packed *packed, const float *bias,
                       int act, float *output, void *stream);
+
+/*
+ * spconv_forward_host -- spconv_forward_ex with the activation and the result
+ * in host memory, enqueued on `stream` by one call; nothing is allocated.
+ * When CUDA maps both host buffers for the current device (page-locked memory
+ * from cudaHostAlloc / cudaHostRegister, each inside one allocation): a copy
+ * kernel reads input_host through its device mapping into dev_input, and the
+ * forward (launched behind it with programmatic dependent launch) writes Y
+ * straight into output_host through its mapping; dev_output is not touched.
+ * Otherwise: cudaMemcpyAsync of input_host into dev_input, the forward into
+ * dev_output, cudaMemcpyAsync of dev_output into output_host.
+ *   input_host   host pointer, N*C*H*W floats (NCHW); page-locked for the
+ *                work to be asynchronous (pageable memory takes the copy path,
+ *                where CUDA may copy before the call returns)
+ *   output_host  host pointer, N*M*E*F floats, 4-byte aligned, page-locked
+ *                likewise; must not overlap input_host
+ *   dev_input    device workspace, N*C*H*W floats, 16-byte aligned
+ *   dev_output   device workspace, N*M*E*F floats, 4-byte aligned, not
+ *                overlapping dev_input; its contents afterwards are unspecified
+ *   bias, act    as for spconv_forward_ex (bias is a device pointer or NULL)
+ * Asynchronous: output_host holds Y once the stream has passed the call's
+ * work; the caller keeps all four buffers alive until then.  Errors: those of
+ * spconv_forward_ex (with dev_input / dev_output in the roles of input /
+ * output), INVALID_ARG for a NULL, misaligned or overlapping host buffer, all
+ * returned before anything is enqueued; CUDA when a copy or a launch cannot be
+ * enqueued (work already enqueued is not undone).  N = 0 is a no-op.
+ */
+int spconv_forward_host(int N, int C, int H, int W, int M, int R, int S, int stride, int pad,
+                        const float *input_host, const spconv_packed *packed, const float *bias,
+                        int act, float *output_host, float *dev_input, float *dev_output,
+                        void *stream);
 
 /* Frees the handle and its device buffers.  NULL-safe.  The caller must make
  * sure no forward that uses the handle is still running. */

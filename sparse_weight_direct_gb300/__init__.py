@@ -21,7 +21,7 @@ import numpy as np
 from . import _lib
 from ._lib import SpconvError, status_string
 
-__all__ = ["pack", "pack_host", "forward", "PackedWeights", "SpconvError", "status_string",
+__all__ = ["pack", "pack_host", "forward", "forward_host", "PackedWeights", "SpconvError", "status_string",
            "out_extent", "library_path"]
 
 
@@ -200,3 +200,43 @@ def forward(x, packed: PackedWeights, out=None, stream=None, bias=None, relu: bo
                                       _stream_ptr(stream))
     _lib.check(rc, "spconv_forward_ex")
     return out
+
+
+def forward_host(x_host, packed: PackedWeights, out_host, x_dev, out_dev, stream=None, bias=None,
+                 relu: bool = False):
+    """Y = conv(x_host, packed) with the activation and the result in host
+    memory (spconv_forward_host): one call enqueues the copy of x_host into
+    the device workspace x_dev, the forward into out_dev and the copy of
+    out_dev into out_host, in that order on ``stream``.  x_host: (N, C, H, W)
+    and out_host: (N, M, E, F) contiguous float32 CPU tensors in page-locked
+    memory; x_dev / out_dev: CUDA tensors of the same shapes.  Asynchronous:
+    out_host holds Y once the stream has passed this work."""
+    import torch
+    sh = packed.shape
+    N = x_host.shape[0] if isinstance(x_host, torch.Tensor) and x_host.dim() == 4 else -1
+    E = out_extent(sh["H"], sh["R"], sh["stride"], sh["pad"])
+    F = out_extent(sh["W"], sh["S"], sh["stride"], sh["pad"])
+    in_shape = (N, sh["C"], sh["H"], sh["W"])
+    out_shape = (N, sh["M"], E, F)
+    for t, shape, cuda, what in ((x_host, in_shape, False, "x_host"),
+                                 (out_host, out_shape, False, "out_host"),
+                                 (x_dev, in_shape, True, "x_dev"),
+                                 (out_dev, out_shape, True, "out_dev")):
+        if not (isinstance(t, torch.Tensor) and t.dtype == torch.float32 and t.is_contiguous()
+                and t.is_cuda == cuda and tuple(t.shape) == shape):
+            raise SpconvError(_lib.SPCONV_ERR_INVALID_ARG,
+                              f"{what} must be a contiguous float32 {'CUDA' if cuda else 'CPU'} "
+                              f"tensor of shape {shape}")
+        if not cuda and not t.is_pinned():
+            raise SpconvError(_lib.SPCONV_ERR_INVALID_ARG, f"{what} must be in page-locked memory")
+    if bias is not None and not (bias.is_cuda and bias.dtype == torch.float32
+                                 and bias.is_contiguous() and bias.numel() == sh["M"]):
+        raise SpconvError(_lib.SPCONV_ERR_INVALID_ARG, "bias must be M contiguous float32 on the GPU")
+    rc = _lib.lib().spconv_forward_host(
+        N, sh["C"], sh["H"], sh["W"], sh["M"], sh["R"], sh["S"], sh["stride"], sh["pad"],
+        ctypes.c_void_p(x_host.data_ptr()), packed.handle,
+        ctypes.c_void_p(bias.data_ptr() if bias is not None else 0), 1 if relu else 0,
+        ctypes.c_void_p(out_host.data_ptr()), ctypes.c_void_p(x_dev.data_ptr()),
+        ctypes.c_void_p(out_dev.data_ptr()), _stream_ptr(stream))
+    _lib.check(rc, "spconv_forward_host")
+    return out_host

@@ -23,7 +23,8 @@ SPCONV_ERR_MISMATCH = -6
 SPCONV_ERR_DEVICE = -7
 
 # Every symbol include/spconv.h declares.
-EXPORTS = ("spconv_pack", "spconv_pack_ex", "spconv_forward", "spconv_forward_ex", "spconv_packed_free",
+EXPORTS = ("spconv_pack", "spconv_pack_ex", "spconv_forward", "spconv_forward_ex",
+           "spconv_forward_host", "spconv_packed_free",
            "spconv_status_string",
            "spconv_pack_host", "spconv_device_status", "spconv_selftest_wait",
            "spconv_packed_info_get", "spconv_launch_info_get", "spconv_packed_copy_array")
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.spconv_forward.restype = i
         L.spconv_forward_ex.argtypes = [i] * 9 + [p, p, p, i, p, p]
         L.spconv_forward_ex.restype = i
+        L.spconv_forward_host.argtypes = [i] * 9 + [p, p, p, i, p, p, p, p]
+        L.spconv_forward_host.restype = i
         L.spconv_packed_free.argtypes = [p]
         L.spconv_packed_free.restype = None
         L.spconv_status_string.argtypes = [i]

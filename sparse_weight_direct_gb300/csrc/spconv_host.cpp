@@ -916,6 +916,51 @@ bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
     return pa < pb + nb && pb < pa + na;
 }
 
+// ---- device mapping of page-locked host buffers (spconv_forward_host)
+
+using PointerAttrFn = CUresult (*)(void *, CUpointer_attribute, CUdeviceptr);
+
+PointerAttrFn pointer_attr_fn() {
+    static PointerAttrFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &p, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PointerAttrFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// The address through which kernels on the current device reach the host
+// buffer [host, host + bytes), or nullptr when there is none: the buffer must
+// be page-locked memory that CUDA maps for this device, and the allocation
+// CUDA reports for it must hold all `bytes`.  Anything else (pageable memory,
+// a range CUDA cannot confirm) gets nullptr, and the caller copies with
+// cudaMemcpyAsync instead.
+void *mapped_view(const void *host, size_t bytes) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer || !a.hostPointer) return nullptr;
+    PointerAttrFn get = pointer_attr_fn();
+    if (!get) return nullptr;
+    CUdeviceptr start = 0;
+    size_t size = 0;
+    const CUdeviceptr dp = (CUdeviceptr)(uintptr_t)a.devicePointer;
+    if (get(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, dp) != CUDA_SUCCESS ||
+        get(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, dp) != CUDA_SUCCESS)
+        return nullptr;
+    if (dp < start || dp - start > size || size - (dp - start) < bytes) return nullptr;
+    return a.devicePointer;
+}
+
 // ---- TMA tensor map of the input (stride-1 layers with 16-byte row stride)
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1009,6 +1054,69 @@ int choose_split(const spconv::Geometry &g, int N) {
     return std::max(1, std::min(s, g.num_chunks));
 }
 
+// Checks of a forward call, before anything is enqueued: the handle, the
+// shape, the device pointers' alignment and overlap, the current device.
+int check_forward(int N, int C, int H, int W, int M, int R, int S, int stride, int pad,
+                  const float *input, const spconv_packed *packed, const float *bias, int act,
+                  const float *output) {
+    if (!packed || N < 0) return SPCONV_ERR_INVALID_ARG;
+    if (act != SPCONV_ACT_NONE && act != SPCONV_ACT_RELU) return SPCONV_ERR_INVALID_ARG;
+    const spconv::Geometry &g = packed->g;
+    if (C != g.C || H != g.H || W != g.W || M != g.M || R != g.R || S != g.S ||
+        stride != g.stride || pad != g.pad)
+        return SPCONV_ERR_MISMATCH;
+    if (!packed->dev_block) return SPCONV_ERR_MISMATCH;
+    if (N == 0) return SPCONV_OK;
+    if (!input || !output) return SPCONV_ERR_INVALID_ARG;
+    if (((uintptr_t)input & 15) || ((uintptr_t)output & 3) || ((uintptr_t)bias & 3))
+        return SPCONV_ERR_INVALID_ARG;
+    const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x * spconv::kMaxSplit * g.groups;
+    if (tiles > 0x7fffffffLL) return SPCONV_ERR_UNSUPPORTED;
+    if (g.format == SPCONV_FORMAT_WS && N > 65535) return SPCONV_ERR_UNSUPPORTED;  // grid z
+    const size_t in_bytes = (size_t)N * C * H * W * sizeof(float);
+    const size_t out_bytes = (size_t)N * M * g.E * g.F * sizeof(float);
+    if (ranges_overlap(input, in_bytes, output, out_bytes)) return SPCONV_ERR_INVALID_ARG;
+    if (bias && ranges_overlap(bias, (size_t)M * sizeof(float), output, out_bytes))
+        return SPCONV_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SPCONV_ERR_CUDA;
+    if (dev != packed->device) return SPCONV_ERR_MISMATCH;
+    return SPCONV_OK;
+}
+
+// Launches a forward whose arguments check_forward accepted (N > 0).  after_copy:
+// the previous kernel on the stream is the copy of this forward's input, so the
+// forward is launched with programmatic dependent launch behind it.
+int enqueue_forward(int N, const float *input, const spconv_packed *packed, const float *bias,
+                    int act, float *output, cudaStream_t stream, bool after_copy = false) {
+    const spconv::Geometry &g = packed->g;
+    if (g.format == SPCONV_FORMAT_WS) {
+        cudaError_t e =
+            spconv::launch_forward_ws(g, N, input, output, bias, act, packed->d, stream);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return SPCONV_ERR_CUDA;
+        }
+        return SPCONV_OK;
+    }
+    try {
+        CUtensorMap tmp;
+        const CUtensorMap *tmap = input_tmap(packed, input, N, tmp);
+        const int split = choose_split(g, N);
+        const bool group_fast = choose_group_fast(g, N, packed->nnz);
+        const bool pdl = after_copy || choose_pdl(g, N, split, group_fast);
+        cudaError_t e = spconv::launch_forward(g, N, split, group_fast, pdl, input, output, bias,
+                                               act, packed->d, tmap, stream);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return SPCONV_ERR_CUDA;
+        }
+    } catch (...) {
+        return SPCONV_ERR_ALLOC;
+    }
+    return SPCONV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1053,52 +1161,48 @@ __attribute__((visibility("default"))) int spconv_pack(
 __attribute__((visibility("default"))) int spconv_forward_ex(
     int N, int C, int H, int W, int M, int R, int S, int stride, int pad, const float *input,
     const spconv_packed *packed, const float *bias, int act, float *output, void *stream) {
-    if (!packed || N < 0) return SPCONV_ERR_INVALID_ARG;
-    if (act != SPCONV_ACT_NONE && act != SPCONV_ACT_RELU) return SPCONV_ERR_INVALID_ARG;
-    const spconv::Geometry &g = packed->g;
-    if (C != g.C || H != g.H || W != g.W || M != g.M || R != g.R || S != g.S ||
-        stride != g.stride || pad != g.pad)
-        return SPCONV_ERR_MISMATCH;
-    if (!packed->dev_block) return SPCONV_ERR_MISMATCH;
-    if (N == 0) return SPCONV_OK;
-    if (!input || !output) return SPCONV_ERR_INVALID_ARG;
-    if (((uintptr_t)input & 15) || ((uintptr_t)output & 3) || ((uintptr_t)bias & 3))
-        return SPCONV_ERR_INVALID_ARG;
-    const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x * spconv::kMaxSplit * g.groups;
-    if (tiles > 0x7fffffffLL) return SPCONV_ERR_UNSUPPORTED;
-    const size_t in_bytes = (size_t)N * C * H * W * sizeof(float);
-    const size_t out_bytes = (size_t)N * M * g.E * g.F * sizeof(float);
-    if (ranges_overlap(input, in_bytes, output, out_bytes)) return SPCONV_ERR_INVALID_ARG;
-    if (bias && ranges_overlap(bias, (size_t)M * sizeof(float), output, out_bytes))
-        return SPCONV_ERR_INVALID_ARG;
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SPCONV_ERR_CUDA;
-    if (dev != packed->device) return SPCONV_ERR_MISMATCH;
-    if (g.format == SPCONV_FORMAT_WS) {
-        if (N > 65535) return SPCONV_ERR_UNSUPPORTED;  // images run along grid z
-        cudaError_t e = spconv::launch_forward_ws(g, N, input, output, bias, act, packed->d,
-                                                  static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) {
+    const int st = check_forward(N, C, H, W, M, R, S, stride, pad, input, packed, bias, act, output);
+    if (st != SPCONV_OK || N == 0) return st;
+    return enqueue_forward(N, input, packed, bias, act, output, static_cast<cudaStream_t>(stream));
+}
+
+__attribute__((visibility("default"))) int spconv_forward_host(
+    int N, int C, int H, int W, int M, int R, int S, int stride, int pad, const float *input_host,
+    const spconv_packed *packed, const float *bias, int act, float *output_host,
+    float *dev_input, float *dev_output, void *stream) {
+    int st = check_forward(N, C, H, W, M, R, S, stride, pad, dev_input, packed, bias, act,
+                           dev_output);
+    if (st != SPCONV_OK || N == 0) return st;
+    if (!input_host || !output_host || ((uintptr_t)output_host & 3)) return SPCONV_ERR_INVALID_ARG;
+    const size_t n_in = (size_t)N * C * H * W;
+    const size_t in_bytes = n_in * sizeof(float);
+    const size_t out_bytes = (size_t)N * M * packed->g.E * packed->g.F * sizeof(float);
+    if (ranges_overlap(input_host, in_bytes, output_host, out_bytes)) return SPCONV_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Page-locked buffers that CUDA maps for this device: the input is copied
+    // by the SMs and the forward writes Y straight into the host buffer (its
+    // write-back is plain stores, each output once).  Otherwise: copy engine
+    // in, forward into dev_output, copy engine out.
+    const float *in_view = static_cast<const float *>(mapped_view(input_host, in_bytes));
+    float *out_view = static_cast<float *>(mapped_view(output_host, out_bytes));
+    if (in_view && out_view) {
+        if (spconv::launch_copy_in(in_view, dev_input, n_in, s) != cudaSuccess) {
             cudaGetLastError();
             return SPCONV_ERR_CUDA;
         }
-        return SPCONV_OK;
+        return enqueue_forward(N, dev_input, packed, bias, act, out_view, s,
+                               packed->g.format != SPCONV_FORMAT_WS);
     }
-    try {
-        CUtensorMap tmp;
-        const CUtensorMap *tmap = input_tmap(packed, input, N, tmp);
-        const int split = choose_split(g, N);
-        const bool group_fast = choose_group_fast(g, N, packed->nnz);
-        const bool pdl = choose_pdl(g, N, split, group_fast);
-        cudaError_t e =
-            spconv::launch_forward(g, N, split, group_fast, pdl, input, output, bias, act,
-                                   packed->d, tmap, static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return SPCONV_ERR_CUDA;
-        }
-    } catch (...) {
-        return SPCONV_ERR_ALLOC;
+    if (cudaMemcpyAsync(dev_input, input_host, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        return SPCONV_ERR_CUDA;
+    }
+    st = enqueue_forward(N, dev_input, packed, bias, act, dev_output, s);
+    if (st != SPCONV_OK) return st;
+    if (cudaMemcpyAsync(output_host, dev_output, out_bytes, cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SPCONV_ERR_CUDA;
     }
     return SPCONV_OK;
 }

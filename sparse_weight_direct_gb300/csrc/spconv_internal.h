@@ -164,6 +164,11 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
                            const float *x, float *y, const float *bias, int act,
                            const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream);
 
+// dst[0, n) = src[0, n) on the SMs (src: the device mapping of a page-locked
+// host buffer, dst: device memory).  A forward launched next with pdl = true
+// overlaps its prologue with the copy and waits for it before reading dst.
+cudaError_t launch_copy_in(const float *src, float *dst, size_t n, cudaStream_t stream);
+
 // Weight-stationary format (one output channel per block, input read in
 // place): whether (P, LR) has an instance, the dynamic shared memory of a
 // launch, and the launcher (N <= 65535).  d.blobs holds the row entries,
