@@ -161,11 +161,13 @@ int spconv_forward_ex(int N, int C, int H, int W, int M, int R, int S, int strid
  * in host memory, enqueued on `stream` by one call; nothing is allocated.
  * When CUDA maps both host buffers for the current device (page-locked memory
  * from cudaHostAlloc / cudaHostRegister, each inside one allocation): a copy
- * kernel reads input_host through its device mapping into dev_input, and the
- * forward (launched behind it with programmatic dependent launch) writes Y
- * straight into output_host through its mapping; dev_output is not touched.
- * Otherwise: cudaMemcpyAsync of input_host into dev_input, the forward into
- * dev_output, cudaMemcpyAsync of dev_output into output_host.
+ * kernel reads input_host through its device mapping into dev_input; the
+ * forward (launched behind it with programmatic dependent launch) writes a Y
+ * of at most 1 MiB straight into output_host through its mapping (dev_output
+ * is not touched), a larger Y into dev_output, which a second copy kernel
+ * writes to output_host.  Otherwise: cudaMemcpyAsync of input_host into
+ * dev_input, the forward into dev_output, cudaMemcpyAsync of dev_output into
+ * output_host.
  *   input_host   host pointer, N*C*H*W floats (NCHW); page-locked for the
  *                work to be asynchronous (pageable memory takes the copy path,
  *                where CUDA may copy before the call returns)
@@ -270,6 +272,10 @@ typedef struct spconv_packed_info {
                               /* are then (16 + c*H*W + (r-1)*W + (s-1)) << 4  */
                               /* | flags: bit 0 s == 0, 1 s == 2, 2 r == 0,    */
                               /* 3 r == 2                                      */
+    int32_t col_blocks;       /* 1: column blocks -- a tile is lane_rows rows  */
+                              /* of tile_cols outputs, each lane holding       */
+                              /* tile_rows consecutive outputs of one row      */
+                              /* (entry offsets as for the padded tile)        */
 } spconv_packed_info;
 
 /* For a SPCONV_FORMAT_WS handle: tile_rows, lane_rows, tile_cols, tiles_y and

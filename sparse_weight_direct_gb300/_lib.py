@@ -53,7 +53,7 @@ class PackedInfo(ctypes.Structure):
         (n, ctypes.c_int32) for n in
         ("hdr_words", "blob_stage_bytes", "in_stage_bytes", "lane_rows", "dense_groups",
          "dense_mask_words", "format", "batch_hint", "blob_stride", "tap_pairs",
-         "plane_stage")]
+         "plane_stage", "col_blocks")]
 
 
 class LaunchInfo(ctypes.Structure):

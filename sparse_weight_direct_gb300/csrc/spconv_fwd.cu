@@ -31,7 +31,9 @@ __global__ void wait_selftest_kernel(unsigned int *flags, unsigned long long lim
 }
 
 KernelFn pick(int S, int stride, int P, int Q, int LR, bool tm = false, bool pairs = false,
-              bool plane = false) {
+              bool plane = false, bool cols = false) {
+    if (cols) return (S == 3 && stride == 1 && !tm && !pairs && !plane) ? pick_cols(P, Q, LR)
+                                                                        : nullptr;
     if (tm) return (S == 3 && stride == 1 && LR == 1) ? pick_tm(P, Q) : nullptr;
     if (pairs) return pick_pairs(S, stride, P, Q, LR);
     if (plane) return (S == 3 && stride == 1 && LR == 2) ? pick_plane(P, Q) : nullptr;
@@ -81,8 +83,8 @@ bool dense_taps_supported(int R, int S, int stride, int LR, int Q) {
 }
 
 int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm, bool pairs,
-                              bool plane) {
-    return pick(S, stride, P, Q, LR, tm, pairs, plane) ? 0 : -1;
+                              bool plane, bool cols) {
+    return pick(S, stride, P, Q, LR, tm, pairs, plane, cols) ? 0 : -1;
 }
 
 bool plane_stage_supported(int H, int W, int R, int S, int stride, int pad, int P, int LR, int Q) {
@@ -140,7 +142,7 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
                            const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream) {
     const bool tm = g.format == 3;
     KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows, tm, g.tap_pairs != 0,
-                       g.plane_stage != 0);
+                       g.plane_stage != 0, g.col_blocks != 0);
     if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks || (tm && split != 1))
         return cudaErrorInvalidConfiguration;
     const size_t smem = forward_smem_bytes(g, split);

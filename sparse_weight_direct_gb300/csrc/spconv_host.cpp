@@ -70,6 +70,9 @@ constexpr int kSMs = 152;                   // GB300 SM count, for the grid heur
 // times cheaper per FMA than a shared-memory load per FMA.
 constexpr double kDenseRowMin = 0.30;
 constexpr int64_t kMinPart = 32;  // smallest part a split row is cut into
+// spconv_forward_host: outputs up to this size are written by the forward
+// straight into the mapped host buffer, larger ones copied out after it.
+constexpr size_t kDirectOutBytes = 1 << 20;
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -136,6 +139,32 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
         g.phase_pitch = spconv::phase_pitch_for(S, stride);
         g.row_pitch = stride * g.phase_pitch;
     }
+    // Column blocks (3x3, stride 1): eight lane rows of four lanes, each lane
+    // holding seven consecutive outputs of its row, tile 8 x 28 -- where that
+    // covers fewer output positions than the column-per-lane tiles (widths a
+    // multiple of 28 but not of 32, e.g. 56 and 112, leave no lane idle).  The
+    // staged row pitch is 4 mod 8 words, so the 32 lanes' first inputs
+    // (ly * pitch + 7 lx) fall in distinct banks.
+    g.col_blocks = 0;
+    if (stride == 1 && R == 3 && S == 3 && g.format == SPCONV_FORMAT_F32 && g.lane_rows == 1) {
+        const int64_t area = (int64_t)g.tiles_y * g.tile_h * g.tiles_x * g.tile_w;
+        const int64_t area_cb = (int64_t)((g.E + 7) / 8) * 8 * ((g.F + 27) / 28) * 28;
+        if (area_cb * 100 < area * 97) {
+            g.col_blocks = 1;
+            g.lane_rows = 8;
+            g.tile_rows = 7;
+            g.tile_h = 8;
+            g.tile_w = 28;
+            g.tiles_y = (g.E + g.tile_h - 1) / g.tile_h;
+            g.tiles_x = (g.F + g.tile_w - 1) / g.tile_w;
+            g.in_rows = g.tile_h - 1 + R;
+            g.in_cols = g.tile_w - 1 + S;
+            int rp = (int)round_up((size_t)(g.shift + g.in_cols), 4);
+            if (rp % 8 == 0) rp += 4;
+            g.phase_pitch = rp;
+            g.row_pitch = rp;
+        }
+    }
     g.plane = g.in_rows * g.row_pitch;
     g.warps = spconv::kWarps;
     // output channels per warp: the largest Q in {4, 2, 1} whose one-image
@@ -177,7 +206,8 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     g.num_slots = g.groups * spconv::kWarps * g.slots;
     g.hdr_words = (int)round_up((size_t)spconv::kWarps * g.slots + 1, 4);
     if (g.groups > 65535) return SPCONV_ERR_UNSUPPORTED;
-    if (spconv::forward_variant_supported(S, stride, g.tile_rows, g.slots, g.lane_rows, tm) != 0)
+    if (spconv::forward_variant_supported(S, stride, g.tile_rows, g.slots, g.lane_rows, tm, false,
+                                          false, g.col_blocks != 0) != 0)
         return SPCONV_ERR_UNSUPPORTED;
     // Whole-image tiles of images whose rows TMA cannot address: one bulk copy
     // of the chunk's raw planes (dense, pitch W) instead of per-element
@@ -212,7 +242,7 @@ int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx)
     const double crs = (double)g.C * g.R * g.S;
     auto nnz_of = [&](int m) { return (int64_t)rowptr[m + 1] - rowptr[m]; };
     std::vector<int> dense, sparse;
-    const bool can_dense = g.format != SPCONV_FORMAT_TMEM && !g.plane_stage &&
+    const bool can_dense = g.format != SPCONV_FORMAT_TMEM && !g.plane_stage && !g.col_blocks &&
                            spconv::dense_taps_supported(g.R, g.S, g.stride, g.lane_rows, g.slots);
     for (int m = 0; m < g.M; ++m)
         (can_dense && nnz_of(m) / crs >= kDenseRowMin ? dense : sparse).push_back(m);
@@ -448,7 +478,7 @@ int pair_index(int Q, int q1, int q2) { return q1 * Q - q1 * (q1 + 1) / 2 + (q2 
 void choose_tap_pairs(spconv::Geometry &g, const std::vector<int32_t> &group_flags,
                       const std::vector<std::vector<int64_t>> &order, const int32_t *colidx) {
     g.tap_pairs = 0;
-    if (g.format != SPCONV_FORMAT_F32 || g.plane_stage ||
+    if (g.format != SPCONV_FORMAT_F32 || g.plane_stage || g.col_blocks ||
         spconv::forward_variant_supported(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows,
                                           false, true) != 0)
         return;
@@ -1180,18 +1210,28 @@ __attribute__((visibility("default"))) int spconv_forward_host(
     if (ranges_overlap(input_host, in_bytes, output_host, out_bytes)) return SPCONV_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // Page-locked buffers that CUDA maps for this device: the input is copied
-    // by the SMs and the forward writes Y straight into the host buffer (its
-    // write-back is plain stores, each output once).  Otherwise: copy engine
-    // in, forward into dev_output, copy engine out.
+    // by the SMs; a small Y is written by the forward straight into the host
+    // buffer (its write-back is plain stores, each output once), a large one
+    // goes to dev_output and is copied out by the SMs in 16-byte vectors (the
+    // forward's row segments make poorer writes over the host link).
+    // Otherwise: copy engine in, forward into dev_output, copy engine out.
     const float *in_view = static_cast<const float *>(mapped_view(input_host, in_bytes));
     float *out_view = static_cast<float *>(mapped_view(output_host, out_bytes));
     if (in_view && out_view) {
-        if (spconv::launch_copy_in(in_view, dev_input, n_in, s) != cudaSuccess) {
+        if (spconv::launch_copy(in_view, dev_input, n_in, s) != cudaSuccess) {
             cudaGetLastError();
             return SPCONV_ERR_CUDA;
         }
-        return enqueue_forward(N, dev_input, packed, bias, act, out_view, s,
-                               packed->g.format != SPCONV_FORMAT_WS);
+        const bool direct = out_bytes <= kDirectOutBytes;
+        st = enqueue_forward(N, dev_input, packed, bias, act, direct ? out_view : dev_output, s,
+                             packed->g.format != SPCONV_FORMAT_WS);
+        if (st != SPCONV_OK || direct) return st;
+        if (spconv::launch_copy(dev_output, out_view, out_bytes / sizeof(float), s) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return SPCONV_ERR_CUDA;
+        }
+        return SPCONV_OK;
     }
     if (cudaMemcpyAsync(dev_input, input_host, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
         cudaGetLastError();
@@ -1324,6 +1364,7 @@ __attribute__((visibility("default"))) int spconv_packed_info_get(const spconv_p
     info->blob_stride = g.blob_stride16 * 16;
     info->tap_pairs = g.tap_pairs;
     info->plane_stage = g.plane_stage;
+    info->col_blocks = g.col_blocks;
     return SPCONV_OK;
 }
 

@@ -89,6 +89,9 @@ struct Geometry {
     int plane_stage;  // 1: the chunk's raw input planes are staged by one bulk copy
                       // (whole-image tiles whose rows TMA cannot address) and the
                       // padding is applied to the weights (see kPlaneLead)
+    int col_blocks;   // 1: column blocks -- lane_rows lane rows of 32 / lane_rows
+                      // lanes, each lane holding tile_rows consecutive outputs of
+                      // its row (stride 1, widths a multiple of 28, not of 32)
     int dense_groups; // leading groups whose blobs are dense-tap (0 if none)
     int split_rows;   // 1 if any group has rows split into parts (bit 1 of its flags)
     int dense_mask_words;  // words of a dense blob's slot masks (warps * chunk, to 4)
@@ -108,9 +111,9 @@ struct DeviceArrays {
 
 // Kernel variants compiled for sm_103a.  Returns 0 if (S, stride, P, Q, LR)
 // has an instance (tm: of the tensor-memory window path; pairs: with tap-pair
-// segments), else -1.
+// segments; plane: with plane staging; cols: with column blocks), else -1.
 int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm = false,
-                              bool pairs = false, bool plane = false);
+                              bool pairs = false, bool plane = false, bool cols = false);
 
 // Whether a layer shape can take the tensor-memory window path (3 x 3,
 // stride 1, one lane row).
@@ -164,10 +167,11 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
                            const float *x, float *y, const float *bias, int act,
                            const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream);
 
-// dst[0, n) = src[0, n) on the SMs (src: the device mapping of a page-locked
-// host buffer, dst: device memory).  A forward launched next with pdl = true
-// overlaps its prologue with the copy and waits for it before reading dst.
-cudaError_t launch_copy_in(const float *src, float *dst, size_t n, cudaStream_t stream);
+// dst[0, n) = src[0, n) on the SMs (one side the device mapping of a
+// page-locked host buffer, the other device memory), after the previous work
+// on the stream.  A forward launched next with pdl = true overlaps its
+// prologue with the copy and waits for it before reading dst.
+cudaError_t launch_copy(const float *src, float *dst, size_t n, cudaStream_t stream);
 
 // Weight-stationary format (one output channel per block, input read in
 // place): whether (P, LR) has an instance, the dynamic shared memory of a

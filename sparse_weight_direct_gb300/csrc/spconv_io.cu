@@ -1,9 +1,9 @@
-// Copy of the activation from page-locked host memory into the device
-// workspace, run on the SMs through the host buffer's device mapping (used by
-// spconv_forward_host when CUDA maps the buffer).  Between a copy kernel and a
-// kernel this avoids the switch between the copy engine and the SMs, which
-// measured several microseconds per switch on one-image layers; the bandwidth
-// over the host link is the same either way.
+// Copies between page-locked host memory and the device workspaces, run on
+// the SMs through the host buffer's device mapping (used by
+// spconv_forward_host when CUDA maps the buffers).  Next to the forward kernel
+// this avoids the switch between the copy engine and the SMs, which measured
+// several microseconds per switch on one-image layers; the bandwidth over the
+// host link is the same either way.
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -17,10 +17,10 @@ namespace {
 constexpr int kCopyThreads = 256;
 constexpr int kCopyMaxBlocks = 4 * 152;
 
-// dst[i] = src[i] for i < n.  The forward launched after this kernel with
+// dst[i] = src[i] for i < n.  A kernel launched after this one with
 // programmatic dependent launch may start its prologue at once: it waits for
 // this grid to complete before it reads dst.
-__global__ void __launch_bounds__(kCopyThreads) copy_in_kernel(const float *__restrict__ src,
+__global__ void __launch_bounds__(kCopyThreads) copy_kernel(const float *__restrict__ src,
                                                                float *__restrict__ dst, size_t n,
                                                                int vec) {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -39,13 +39,13 @@ __global__ void __launch_bounds__(kCopyThreads) copy_in_kernel(const float *__re
 
 }  // namespace
 
-cudaError_t launch_copy_in(const float *src, float *dst, size_t n, cudaStream_t stream) {
+cudaError_t launch_copy(const float *src, float *dst, size_t n, cudaStream_t stream) {
     if (n == 0) return cudaSuccess;
     const int vec = (((uintptr_t)src | (uintptr_t)dst) & 15) == 0;
     const size_t per_block = (size_t)kCopyThreads * (vec ? 4 : 1);
     size_t blocks = (n + per_block - 1) / per_block;
     if (blocks > (size_t)kCopyMaxBlocks) blocks = kCopyMaxBlocks;
-    copy_in_kernel<<<(unsigned)blocks, kCopyThreads, 0, stream>>>(src, dst, n, vec);
+    copy_kernel<<<(unsigned)blocks, kCopyThreads, 0, stream>>>(src, dst, n, vec);
     return cudaGetLastError();
 }
 

@@ -614,12 +614,18 @@ static __device__ __forceinline__ void run_tm_chunk(float (&acc)[Q][P], const fl
 constexpr int kModeTmem = 1;
 constexpr int kModePairs = 2;
 constexpr int kModePlane = 3;  // plane staging (see apply_entry_plane)
+constexpr int kModeCols = 4;   // column blocks: a lane's P outputs run along a row
 template <int P, int Q, int S_CT, int ST_CT, int LR, int MODE = 0>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     spconv_fwd_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap) {
     constexpr bool TM = MODE == kModeTmem;
     constexpr bool PAIRS = MODE == kModePairs;
     constexpr bool PLANE = MODE == kModePlane;
+    // Column blocks (stride 1): lane (ly, lx) holds outputs (ly, lx*P + r) of
+    // an LR x (LC*P) tile, so widths that are multiples of LC*P but not of 32
+    // leave no lane idle; a tap's P inputs are consecutive words.
+    constexpr bool COLS = MODE == kModeCols;
+    static_assert(!COLS || ST_CT == 1, "column blocks: stride 1");
     static_assert(!PLANE || (S_CT == 3 && ST_CT == 1 && LR == 2), "plane staging: 3x3, two lane rows");
     static_assert(!TM || (S_CT == 3 && ST_CT == 1 && LR == 1 && P <= 8), "tensor-memory path: 3x3, stride 1");
     static_assert(!PAIRS || Q == 2 || Q == 4, "tap pairs: 2 or 4 output channels per warp");
@@ -632,13 +638,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     unsigned char *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     constexpr int LC = kLanes / LR;  // lanes per lane row = output columns of a tile
     constexpr int ROW_STEP =
-        (S_CT && !PLANE) ? LR * (ST_CT == 1 ? row_pitch_s1(S_CT, LR)
-                                            : ST_CT * ST_CT * phase_pitch_for(S_CT, ST_CT))
-                         : 0;
+        COLS ? 1
+             : (S_CT && !PLANE) ? LR * (ST_CT == 1 ? row_pitch_s1(S_CT, LR)
+                                                   : ST_CT * ST_CT * phase_pitch_for(S_CT, ST_CT))
+                                : 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ly = lane / LC, lx = lane % LC;  // lane row / column of this thread
     const int st = ST_CT ? ST_CT : p.stride;
-    const int row_step = LR * st * p.row_pitch;  // between this lane's output rows
+    const int row_step = COLS ? 1 : LR * st * p.row_pitch;  // between this lane's outputs
 
     // Block order (clusters run along x): channel-split rank fastest, then
     // either the tile (groups in grid y: the heaviest groups, dense ones,
@@ -659,8 +666,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int n = b / p.tiles_y;
     const int k_begin = kr * p.num_chunks / split;
     const int k_end = (kr + 1) * p.num_chunks / split;
-    const int iy0 = ty * (LR * P) * st - p.pad;
-    const int ix0 = tx * LC * st - p.pad;
+    const int iy0 = ty * (COLS ? LR : LR * P) * st - p.pad;
+    const int ix0 = tx * (COLS ? LC * P : LC) * st - p.pad;
     const int nmine = k_end - k_begin;
     const int nslot = kWarps * Q;
 
@@ -818,7 +825,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         }
         if (failed) break;
         const unsigned char *base = smem + (size_t)s * p.stage_bytes;
-        const float *sb = reinterpret_cast<const float *>(base) + ly * st * p.row_pitch + lx;
+        const float *sb = reinterpret_cast<const float *>(base) + ly * st * p.row_pitch +
+                          (COLS ? lx * P : lx);
         if constexpr (PLANE) {
             // dense planes: lanes past the image's width read the spare banks
             // 2W .. 31 (finite values, outputs discarded), so the 32 reads of a
@@ -833,7 +841,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             run_tm_chunk<P, Q, row_pitch_s1(3, 1)>(acc, sb + p.shift, hdr, ent, warp, p.chunk,
                                                     min(p.chunk, p.C - k * p.chunk), p.plane,
                                                     tbase);
-        } else if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4 && !PLANE) {
+        } else if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4 && !PLANE && !COLS) {
             if (dense) {
                 const int k = k_begin + it;
                 run_dense_chunk<P, Q, S_CT, LR, row_pitch_s1(S_CT, LR)>(
@@ -918,20 +926,55 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     }
 
     const int slot0 = group * nslot + warp * Q;
-    const int ox = tx * LC + lx;
-    const int oy0 = ty * (LR * P) + ly;  // this lane's output rows: oy0 + LR * r
+    // This lane's outputs r = 0 .. P-1: rows oy0 + LR * r of column ox, or
+    // (column blocks) columns ox + r of row oy0.
+    const int ox = COLS ? tx * (LC * P) + lx * P : tx * LC + lx;
+    const int oy0 = COLS ? ty * LR + ly : ty * (LR * P) + ly;
+    const bool lane_out = COLS ? oy0 < p.E : ox < p.F;  // the lane has outputs
+    auto out_ok = [&](int r) { return COLS ? ox + r < p.F : oy0 + LR * r < p.E; };
+    auto out_at = [&](int r) {  // offset of output r within its (n, m) plane
+        return COLS ? (size_t)oy0 * p.F + ox + r : (size_t)(oy0 + LR * r) * p.F + ox;
+    };
+    if constexpr (COLS) {
+        if (split == 1 && !has_parts) {
+            // Column blocks: lane (ly, lx) holds tile positions 7 lane + r
+            // (row-major LR x LC*P).  Each warp passes its slots through
+            // shared memory (free past the barrier above) so that a store
+            // instruction writes 32 consecutive positions of the tile, not
+            // 32 scattered ones.
+            if (failed) return;
+            float *tb = reinterpret_cast<float *>(smem) + (size_t)warp * Q * (P * 32);
+#pragma unroll
+            for (int q = 0; q < Q; ++q)
+#pragma unroll
+                for (int r = 0; r < P; ++r) tb[q * (P * 32) + lane * P + r] = acc[q][r];
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int m = q == 0 ? pre_m : p.slot_oc[slot0 + q];
+                if (m < 0) continue;
+                float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
+#pragma unroll
+                for (int i = 0; i < P; ++i) {
+                    const int t = i * 32 + lane;
+                    const int oy = ty * LR + t / (LC * P), oxt = tx * (LC * P) + t % (LC * P);
+                    if (oy < p.E && oxt < p.F)
+                        yo[(size_t)oy * p.F + oxt] = finish(p, m, tb[q * (P * 32) + t]);
+                }
+            }
+            return;
+        }
+    }
     if (split == 1 && !has_parts) {
-        if (failed || ox >= p.F) return;
+        if (failed || !lane_out) return;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
             const int m = q == 0 ? pre_m : p.slot_oc[slot0 + q];
             if (m < 0) continue;
-            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
+            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
 #pragma unroll
-            for (int r = 0; r < P; ++r) {
-                const int oy = oy0 + LR * r;
-                if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, acc[q][r]);
-            }
+            for (int r = 0; r < P; ++r)
+                if (out_ok(r)) yo[out_at(r)] = finish(p, m, acc[q][r]);
         }
         return;
     }
@@ -964,7 +1007,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             }
             asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
             asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-            if (failed || ox >= p.F) return;
+            if (failed || !lane_out) return;
             const int s_begin = kr * nslot / split, s_end = (kr + 1) * nslot / split;
             const int items = (s_end - s_begin) * P;
             for (int item = warp; item < items; item += kWarps) {
@@ -979,10 +1022,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 #pragma unroll
                 for (int j = 0; j < kMaxSplit; ++j)
                     if (j < split) sum += v[j];
-                const int oy = oy0 + LR * r;
-                if (oy < p.E)
-                    p.y[((size_t)n * p.M + m) * p.E * p.F + (size_t)oy * p.F + ox] =
-                        finish(p, m, sum);
+                if (out_ok(r))
+                    p.y[((size_t)n * p.M + m) * p.E * p.F + out_at(r)] = finish(p, m, sum);
             }
             return;
         }
@@ -1000,19 +1041,18 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         for (int r = 0; r < P; ++r) part[((warp * Q + q) * P + r) * 32 + lane] = acc[q][r];
     if (split == 1) {
         __syncthreads();
-        if (failed || ox >= p.F) return;
+        if (failed || !lane_out) return;
         for (int q = 0; q < Q; ++q) {
             const int sl = warp * Q + q;
             const int m = q == 0 ? pre_m : p.slot_oc[group * nslot + sl];
             if (m < 0) continue;
             const int next0 = q == 0 ? pre_next : p.slot_next[group * nslot + sl];
-            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
+            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
             for (int r = 0; r < P; ++r) {
                 float sum = part[(sl * P + r) * 32 + lane];
                 for (int c = next0; c >= 0; c = p.slot_next[group * nslot + c])
                     sum += part[(c * P + r) * 32 + lane];
-                const int oy = oy0 + LR * r;
-                if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, sum);
+                if (out_ok(r)) yo[out_at(r)] = finish(p, m, sum);
             }
         }
         return;
@@ -1021,7 +1061,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     cluster.sync();
     const int s_begin = kr * nslot / split, s_end = (kr + 1) * nslot / split;
     if constexpr (Q <= 2) {
-        if (!failed && ox < p.F) {
+        if (!failed && lane_out) {
             // (slot, output row) items spread over all warps; the ranks' partials
             // of one item are loaded back to back, then added in rank order
             const int items = (s_end - s_begin) * P;
@@ -1042,27 +1082,24 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                     for (int j = 0; j < kMaxSplit; ++j)
                         if (j < split) sum += v[j];
                 }
-                const int oy = oy0 + LR * r;
-                if (oy < p.E)
-                    p.y[((size_t)n * p.M + m) * p.E * p.F + (size_t)oy * p.F + ox] =
-                        finish(p, m, sum);
+                if (out_ok(r))
+                    p.y[((size_t)n * p.M + m) * p.E * p.F + out_at(r)] = finish(p, m, sum);
             }
         }
     } else {
         // wide instances: one warp per slot, ranks and rows in sequence (compact
         // code; these instances carry the register-heavy dense-tap path)
-        if (!failed && ox < p.F) {
+        if (!failed && lane_out) {
             for (int sl = s_begin + warp; sl < s_end; sl += kWarps) {
                 const int m = p.slot_oc[group * nslot + sl];
                 if (m < 0) continue;
-                float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F + ox;
+                float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
                 for (int r = 0; r < P; ++r) {
                     float sum = 0.f;
                     for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c])
                         for (int j = 0; j < split; ++j)
                             sum += cluster.map_shared_rank(part, j)[(c * P + r) * 32 + lane];
-                    const int oy = oy0 + LR * r;
-                    if (oy < p.E) yo[(size_t)oy * p.F] = finish(p, m, sum);
+                    if (out_ok(r)) yo[out_at(r)] = finish(p, m, sum);
                 }
             }
         }
@@ -1084,6 +1121,7 @@ KernelFn pick_tm(int P, int Q);
 KernelFn pick_pairs(int S, int stride, int P, int Q, int LR);
 // Plane-staging instances (3x3 stride 1, two lane rows, Q in {1, 2}).
 KernelFn pick_plane(int P, int Q);
+KernelFn pick_cols(int P, int Q, int LR);
 
 // Instantiates the kernels of one Q for the supported kernel widths, strides,
 // rows per lane and lane rows.

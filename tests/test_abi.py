@@ -254,8 +254,20 @@ def test_packed_layout_decodes_to_csr(name, fmt):
         got = [(c, v) for c, v in rows.get(m, []) if v != 0]
         assert got == want
     # staged input tile covers every tap of every output of a tile
-    tile_h = info["tile_rows"] * info["lane_rows"]
-    assert info["tile_cols"] * info["lane_rows"] == 32
+    if info["col_blocks"]:
+        # lane_rows rows of 32 / lane_rows lanes, each lane tile_rows
+        # consecutive outputs of its row; the lanes' first inputs
+        # (ly * row_pitch + lx * tile_rows) fall in 32 distinct banks
+        P, LR = info["tile_rows"], info["lane_rows"]
+        tile_h = LR
+        assert info["tile_cols"] == (32 // LR) * P and L.stride == 1
+        banks = {(ly * info["row_pitch"] + lx * P) % 32 for ly in range(LR)
+                 for lx in range(32 // LR)}
+        assert len(banks) == 32
+        assert info["row_pitch"] % 4 == 0 and info["row_pitch"] >= info["shift"] + info["in_cols"]
+    else:
+        tile_h = info["tile_rows"] * info["lane_rows"]
+        assert info["tile_cols"] * info["lane_rows"] == 32
     if info["plane_stage"]:  # whole raw planes, the padding applied to the weights
         assert info["in_rows"] == L.H == tile_h and info["in_cols"] == L.W <= info["tile_cols"]
     else:

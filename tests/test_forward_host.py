@@ -74,9 +74,13 @@ def test_forward_host_parity(name, integer):
     swd.forward_host(xh, w, yh, xd, yd, stream=s)
     s.synchronize()
     # page-locked buffers from torch are mapped on the device: the input went
-    # through the copy kernel and Y straight into the host buffer, so the
-    # device output workspace was never written
-    assert torch.isnan(yd).all()
+    # through the copy kernel; a Y of at most 1 MiB went straight into the host
+    # buffer (the device output workspace was never written), a larger one
+    # through the workspace
+    if yh.numel() * 4 <= 1 << 20:
+        assert torch.isnan(yd).all()
+    else:
+        np.testing.assert_array_equal(yd.cpu().numpy(), yh.numpy())
     got = yh.numpy().astype(np.float64)
     ref, mag = oracle.csr(x, rowptr, colidx, value, L.M, L.R, L.S, L.stride, L.pad)
     if integer:

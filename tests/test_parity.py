@@ -393,3 +393,46 @@ def test_plane_staging(case, integer):
     got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 3, 3, 1, 1, batch_hint=N)
     ref, mag = oracle.csr(x, rowptr, colidx, value, M, 3, 3, 1, 1)
     check(got, ref, mag, exact=integer, what=f"plane {case}")
+
+
+COLS_CASES = [
+    # (N, C, H, W, M, pad, density, heavy): 3x3 stride-1 layers whose output width is a
+    # multiple of 28 but not of 32, tiled in column blocks (8 x 28 tiles, each lane seven
+    # consecutive outputs of one row)
+    (2, 20, 56, 56, 40, 1, 0.1, False),      # two column tiles, one ragged chunk
+    (1, 9, 16, 28, 17, 1, 0.3, False),       # one column tile, M not a multiple of 8
+    (3, 9, 44, 84, 17, 1, 0.2, False),       # ragged rows (44), three column tiles
+    (1, 6, 58, 58, 12, 0, 0.3, False),       # pad 0 (no alignment shift), cp.async staging
+    (1, 7, 54, 54, 10, 2, 0.3, False),       # pad 2, cp.async staging
+    (2, 32, 112, 112, 16, 1, 0.1, False),    # 112 wide: four column tiles
+    (1, 128, 16, 56, 16, 1, 0.2, False),     # two-block clusters, push reduction
+    (1, 96, 24, 28, 24, 1, 0.1, False),      # push reduction, one column tile
+    (1, 128, 56, 56, 128, 1, 0.05, False),   # two-block clusters, four channels per warp
+    (1, 128, 56, 56, 64, 1, 0.1, True),      # very dense rows split into parts, clusters
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", COLS_CASES, ids=[str(c) for c in COLS_CASES])
+@pytest.mark.parametrize("integer", [False, True])
+def test_column_blocks(case, integer):
+    N, C, H, W, M, pad, d, heavy = case
+    rng = np.random.default_rng(abs(hash(case)) % (2 ** 32) + integer)
+    CRS = C * 9
+    rows = [np.nonzero(rng.random(CRS) < (0.9 if heavy and m % 20 == 0 else d))[0]
+            for m in range(M)]
+    rowptr = np.concatenate([[0], np.cumsum([r.size for r in rows])]).astype(np.int32)
+    colidx = np.concatenate(rows).astype(np.int32)
+    if integer:
+        value = rng.choice(np.array([-3, -2, -1, 1, 2, 3], np.float32), size=colidx.size)
+    else:
+        value = rng.normal(0, 0.05, size=colidx.size).astype(np.float32)
+    x = workloads.random_input((N, C, H, W), rng, integer=integer)
+    w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=3, S=3, stride=1, pad=pad,
+                      batch_hint=N)
+    assert w.info()["col_blocks"] == 1
+    assert not heavy or (w.array("group_flags") & 2).any()
+    w.close()
+    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 3, 3, 1, pad, batch_hint=N)
+    ref, mag = oracle.csr(x, rowptr, colidx, value, M, 3, 3, 1, pad)
+    check(got, ref, mag, exact=integer, what=f"column blocks {case}")
