@@ -65,6 +65,9 @@ int main(int argc, char **argv) {
     CHECK(info.nnz == nnz && info.E == E && info.F == F && info.on_device == 0, "info fields");
     CHECK(spconv_forward(N, C, H, W, M, R, S, stride, pad, NULL, hp, NULL, NULL) ==
               SPCONV_ERR_MISMATCH, "host-only handle rejected by forward");
+    CHECK(spconv_forward_host(N, C, H, W, M, R, S, stride, pad, NULL, hp, NULL, SPCONV_ACT_NONE,
+                              NULL, NULL, NULL, NULL) == SPCONV_ERR_MISMATCH,
+          "host-only handle rejected by forward_host");
     spconv_packed_free(hp);
     spconv_packed_free(NULL);
     CHECK(spconv_pack_host(0, H, W, M, R, S, stride, pad, rowptr, colidx, value, &hp) ==
@@ -103,6 +106,29 @@ int main(int argc, char **argv) {
         if (!(fabs((double)hy[i] - ref[i]) <= 1e-5 * mag[i] + 1e-7)) ++bad;
     printf("forward checked %zu outputs, %zu out of tolerance\n", ny, bad);
     CHECK(bad == 0, "parity");
+
+    /* host buffers: page-locked (device-mapped path) and pageable (copy path);
+     * the same kernel on the same data gives the same bits */
+    float *px = NULL, *py = NULL;
+    CHECK(cudaHostAlloc((void **)&px, nx * sizeof(float), cudaHostAllocDefault) == cudaSuccess,
+          "cudaHostAlloc x");
+    CHECK(cudaHostAlloc((void **)&py, ny * sizeof(float), cudaHostAllocDefault) == cudaSuccess,
+          "cudaHostAlloc y");
+    memcpy(px, hx, nx * sizeof(float));
+    float *gy = malloc(ny * sizeof(float));
+    for (int pass = 0; pass < 2; ++pass) {
+        float *in = pass == 0 ? px : hx, *out = pass == 0 ? py : gy;
+        for (size_t i = 0; i < ny; ++i) out[i] = -1.0f;
+        CHECK(spconv_forward_host(N, C, H, W, M, R, S, stride, pad, in, dp, NULL,
+                                  SPCONV_ACT_NONE, out, dx, dy, NULL) == SPCONV_OK,
+              "forward_host");
+        CHECK(cudaDeviceSynchronize() == cudaSuccess, "sync");
+        CHECK(memcmp(out, hy, ny * sizeof(float)) == 0, "forward_host equals forward");
+    }
+    printf("forward_host matched forward (page-locked and pageable buffers)\n");
+    cudaFreeHost(px);
+    cudaFreeHost(py);
+    free(gy);
     spconv_packed_free(dp);
     cudaFree(dx);
     cudaFree(dy);
