@@ -146,7 +146,8 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     // staged row pitch is 4 mod 8 words, so the 32 lanes' first inputs
     // (ly * pitch + 7 lx) fall in distinct banks.
     g.col_blocks = 0;
-    if (stride == 1 && R == 3 && S == 3 && g.format == SPCONV_FORMAT_F32 && g.lane_rows == 1) {
+    const bool tile_fmt = g.format == SPCONV_FORMAT_F32 || g.format == SPCONV_FORMAT_PACKED32;
+    if (stride == 1 && R == 3 && S == 3 && tile_fmt && g.lane_rows == 1) {
         const int64_t area = (int64_t)g.tiles_y * g.tile_h * g.tiles_x * g.tile_w;
         const int64_t area_cb = (int64_t)((g.E + 7) / 8) * 8 * ((g.F + 27) / 28) * 28;
         if (area_cb * 100 < area * 97) {
@@ -214,6 +215,8 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     // cp.async into a padded tile; the kernel applies the padding to the
     // weights of the taps that leave the image.
     g.plane_stage = 0;
+    // (F32 entries only: decoding a 32-bit word into a plane offset and side
+    // flags measured slower than the padded tile on the one-image layer)
     if (g.format == SPCONV_FORMAT_F32 &&
         spconv::plane_stage_supported(H, W, R, S, stride, pad, g.tile_rows, g.lane_rows, g.slots)) {
         g.plane_stage = 1;

@@ -415,7 +415,8 @@ COLS_CASES = [
 @pytest.mark.gpu
 @pytest.mark.parametrize("case", COLS_CASES, ids=[str(c) for c in COLS_CASES])
 @pytest.mark.parametrize("integer", [False, True])
-def test_column_blocks(case, integer):
+@pytest.mark.parametrize("fmt", ["f32", "packed32"])
+def test_column_blocks(case, integer, fmt):
     N, C, H, W, M, pad, d, heavy = case
     rng = np.random.default_rng(abs(hash(case)) % (2 ** 32) + integer)
     CRS = C * 9
@@ -427,12 +428,14 @@ def test_column_blocks(case, integer):
         value = rng.choice(np.array([-3, -2, -1, 1, 2, 3], np.float32), size=colidx.size)
     else:
         value = rng.normal(0, 0.05, size=colidx.size).astype(np.float32)
+    if fmt == "packed32":  # the 32-bit word holds FP16 values
+        value = value.astype(np.float16).astype(np.float32)
     x = workloads.random_input((N, C, H, W), rng, integer=integer)
     w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=3, S=3, stride=1, pad=pad,
-                      batch_hint=N)
+                      batch_hint=N, fmt=fmt)
     assert w.info()["col_blocks"] == 1
     assert not heavy or (w.array("group_flags") & 2).any()
     w.close()
-    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 3, 3, 1, pad, batch_hint=N)
+    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 3, 3, 1, pad, batch_hint=N, fmt=fmt)
     ref, mag = oracle.csr(x, rowptr, colidx, value, M, 3, 3, 1, pad)
     check(got, ref, mag, exact=integer, what=f"column blocks {case}")
