@@ -326,9 +326,20 @@ def test_launch_plans():
     assert pl["grid_x"] * pl["grid_y"] == 4 * info["groups"] <= 152 and pl["grid_z"] == 1
     assert pl["block_threads"] == 256 and pl["tma"] == 0
     assert pl["smem_bytes"] <= 200 * 1024
+    assert info["col_blocks"] == 0
     L, info, pl = plan("vgg3x3", 16, batch_hint=16)
     assert pl["cluster"] == 1 and pl["push"] == 0 and pl["tma"] == 1 and pl["pdl"] == 1
     assert pl["grid_x"] * pl["grid_y"] == 16 * info["tiles_y"] * info["tiles_x"] * info["groups"]
+    # 56 wide: column blocks, 8 x 28 tiles (two per row band), no idle lane
+    assert info["col_blocks"] == 1 and info["plane_stage"] == 0
+    assert (info["lane_rows"], info["tile_rows"], info["tile_cols"]) == (8, 7, 28)
+    assert (info["tiles_y"], info["tiles_x"], info["row_pitch"]) == (7, 2, 36)
+    L, info, pl = plan("vgg3x3", 16, batch_hint=16, fmt="packed32")
+    assert info["col_blocks"] == 1  # the 32-bit words decode to the same offsets
+    L, info, pl = plan("resnet3x3", 1, batch_hint=1, fmt="packed32")
+    assert info["plane_stage"] == 0 and info["col_blocks"] == 0  # padded tile
+    L, info, pl = plan("sweep90", 8, batch_hint=8)  # 28 wide: column-per-lane tiles
+    assert info["col_blocks"] == 0 and info["lane_rows"] == 1 and info["tile_cols"] == 32
     L, info, pl = plan("sweep80", 8, batch_hint=8)  # dense-tap groups, several waves
     assert info["dense_groups"] > 0 and pl["grid_x"] * pl["grid_y"] > 2 * 152
     assert pl["pdl"] == 0
