@@ -31,12 +31,12 @@ __global__ void wait_selftest_kernel(unsigned int *flags, unsigned long long lim
 }
 
 KernelFn pick(int S, int stride, int P, int Q, int LR, bool tm = false, bool pairs = false,
-              bool plane = false, bool cols = false) {
+              bool plane = false, bool cols = false, int W = 0) {
     if (cols) return (S == 3 && stride == 1 && !tm && !pairs && !plane) ? pick_cols(P, Q, LR)
                                                                         : nullptr;
     if (tm) return (S == 3 && stride == 1 && LR == 1) ? pick_tm(P, Q) : nullptr;
     if (pairs) return pick_pairs(S, stride, P, Q, LR);
-    if (plane) return (S == 3 && stride == 1 && LR == 2) ? pick_plane(P, Q) : nullptr;
+    if (plane) return (S == 3 && stride == 1 && LR == 2) ? pick_plane(P, Q, W) : nullptr;
     switch (Q) {
         case 1: return pick_q1(S, stride, P, LR);
         case 2: return pick_q2(S, stride, P, LR);
@@ -89,7 +89,8 @@ int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm, 
 
 bool plane_stage_supported(int H, int W, int R, int S, int stride, int pad, int P, int LR, int Q) {
     return R == 3 && S == 3 && stride == 1 && pad == 1 && LR == 2 && H == 2 * P && W >= 2 &&
-           W <= 16 && (W * 4) % 16 != 0 && (H * W) % 4 == 0 && pick(S, stride, P, Q, LR, false, false, true);
+           W <= 16 && (W * 4) % 16 != 0 && (H * W) % 4 == 0 &&
+           pick(S, stride, P, Q, LR, false, false, true, false, W);
 }
 
 bool tm_supported(int R, int S, int stride, int LR) {
@@ -142,7 +143,7 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
                            const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream) {
     const bool tm = g.format == 3;
     KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows, tm, g.tap_pairs != 0,
-                       g.plane_stage != 0, g.col_blocks != 0);
+                       g.plane_stage != 0, g.col_blocks != 0, g.W);
     if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks || (tm && split != 1))
         return cudaErrorInvalidConfiguration;
     const size_t smem = forward_smem_bytes(g, split);

@@ -320,8 +320,10 @@ static __device__ __forceinline__ void run_segment(float (&acc)[P], const float 
 // the row above, 3 the row below); lanebits holds the sides this lane's
 // outputs touch (its column is the first / last, its lane row holds the top
 // row at p = 0 / the bottom row at p = P - 1), and a tap that leaves the image
-// there reads a finite neighbour with weight zero.
-template <int P>
+// there reads a finite neighbour with weight zero.  RS: the step between the
+// lane's outputs (two rows, 2 W words) when the instance fixes it, so the P
+// loads take immediate offsets; 0 = row_step at run time.
+template <int P, int RS>
 static __device__ __forceinline__ void apply_entry_plane(float (&acc)[P], const float *sb, float v,
                                                          uint32_t code, int row_step,
                                                          uint32_t lanebits) {
@@ -332,27 +334,27 @@ static __device__ __forceinline__ void apply_entry_plane(float (&acc)[P], const 
     const float wl = (hit & 8u) ? 0.f : wc;
 #pragma unroll
     for (int r = 0; r < P; ++r)
-        acc[r] = fmaf(r == 0 ? w0 : (r == P - 1 ? wl : wc), s[r * row_step], acc[r]);
+        acc[r] = fmaf(r == 0 ? w0 : (r == P - 1 ? wl : wc), s[r * (RS ? RS : row_step)], acc[r]);
 }
 
-template <int P, int UNROLL>
+template <int P, int RS, int UNROLL>
 static __device__ __forceinline__ void run_segment_plane(float (&acc)[P], const float *sb,
                                                          const float2 *ent, int j, int j1,
                                                          int row_step, uint32_t lanebits) {
     if ((j & 1) && j < j1) {  // head: bring j to a 16-byte boundary
         const float2 e = ent[j];
-        apply_entry_plane<P>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
+        apply_entry_plane<P, RS>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
         ++j;
     }
 #pragma unroll UNROLL
     for (; j + 1 < j1; j += 2) {
         const float4 e = *reinterpret_cast<const float4 *>(ent + j);
-        apply_entry_plane<P>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
-        apply_entry_plane<P>(acc, sb, e.z, __float_as_uint(e.w), row_step, lanebits);
+        apply_entry_plane<P, RS>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
+        apply_entry_plane<P, RS>(acc, sb, e.z, __float_as_uint(e.w), row_step, lanebits);
     }
     if (j < j1) {  // tail
         const float2 e = ent[j];
-        apply_entry_plane<P>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
+        apply_entry_plane<P, RS>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
     }
 }
 
@@ -615,7 +617,7 @@ constexpr int kModeTmem = 1;
 constexpr int kModePairs = 2;
 constexpr int kModePlane = 3;  // plane staging (see apply_entry_plane)
 constexpr int kModeCols = 4;   // column blocks: a lane's P outputs run along a row
-template <int P, int Q, int S_CT, int ST_CT, int LR, int MODE = 0>
+template <int P, int Q, int S_CT, int ST_CT, int LR, int MODE = 0, int PLANE_RS = 0>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     spconv_fwd_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap) {
     constexpr bool TM = MODE == kModeTmem;
@@ -627,6 +629,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     constexpr bool COLS = MODE == kModeCols;
     static_assert(!COLS || ST_CT == 1, "column blocks: stride 1");
     static_assert(!PLANE || (S_CT == 3 && ST_CT == 1 && LR == 2), "plane staging: 3x3, two lane rows");
+    static_assert(PLANE || PLANE_RS == 0, "a fixed row step is a plane-staging instance");
     static_assert(!TM || (S_CT == 3 && ST_CT == 1 && LR == 1 && P <= 8), "tensor-memory path: 3x3, stride 1");
     static_assert(!PAIRS || Q == 2 || Q == 4, "tap pairs: 2 or 4 output channels per warp");
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -860,7 +863,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                 if constexpr (PLANE) {
                     const uint32_t lanebits = (lx == 0 ? 1u : 0u) | (lx == p.W - 1 ? 2u : 0u) |
                                               (ly == 0 ? 4u : 0u) | (ly == LR - 1 ? 8u : 0u);
-                    run_segment_plane<P, 4>(acc[q], sb, ent, j0, j1, row_step, lanebits);
+                    run_segment_plane<P, PLANE_RS, 4>(acc[q], sb, ent, j0, j1, row_step, lanebits);
                 } else {
                     // Q = 8 instances are at the register cap: no unrolling there
                     run_segment<P, ROW_STEP, (Q >= 8 ? 1 : 4)>(acc[q], sb, ent, j0, j1, row_step);
@@ -1119,8 +1122,9 @@ KernelFn pick_q8(int S, int stride, int P, int LR);
 KernelFn pick_tm(int P, int Q);
 // Tap-pair instances (Q = 4, one lane row; 3x3 and 5x5 stride 1, 11x11 stride 4).
 KernelFn pick_pairs(int S, int stride, int P, int Q, int LR);
-// Plane-staging instances (3x3 stride 1, two lane rows, Q in {1, 2}).
-KernelFn pick_plane(int P, int Q);
+// Plane-staging instances (3x3 stride 1, two lane rows, Q in {1, 2}); 14-wide
+// images (row step 28 words) have their own, with immediate load offsets.
+KernelFn pick_plane(int P, int Q, int W);
 KernelFn pick_cols(int P, int Q, int LR);
 
 // Instantiates the kernels of one Q for the supported kernel widths, strides,
