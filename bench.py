@@ -13,6 +13,10 @@ device synchronize; each step flushes L2 (a 256 MiB write, outside the timed
 events) and is timed with CUDA events on the launching stream.  Rank 0 prints
 one JSON line.  --impl reference times the CPU oracle (the only other
 implementation of this path) on the host cores on the same layer.
+
+End to end (`e2e`): the same layer through spconv_forward_host, one call per
+step with the input and the result in page-locked host memory (the copies to
+and from the GPU inside the timed events).
 """
 from __future__ import annotations
 
