@@ -472,3 +472,47 @@ def test_launch_smem_within_limit_for_any_batch():
                 li = w.launch_info(n)
                 assert li["smem_bytes"] <= 200 * 1024, (name, hint, n, li["smem_bytes"])
             w.close()
+
+
+SHAPE_CASES = [
+    # (N hint, C, H, W, M, pad, density, plan): ad-hoc 3x3 stride-1 shapes and the
+    # plan they take -- column blocks (56 / 84 / 112 wide), plane staging (14 wide
+    # or less, rows TMA cannot address) or the column-per-lane padded tile
+    (2, 20, 56, 56, 40, 1, 0.1, "cols"),
+    (3, 9, 44, 84, 17, 1, 0.2, "cols"),     # 44 rows: the last 8-row tile half used
+    (1, 6, 58, 58, 12, 0, 0.3, "cols"),
+    (1, 7, 54, 54, 10, 2, 0.3, "cols"),
+    (2, 12, 112, 112, 16, 1, 0.05, "cols"),
+    (1, 40, 14, 10, 24, 1, 0.3, "plane"),
+    (1, 64, 14, 14, 70, 1, 0.2, "plane"),
+    (2, 17, 28, 28, 33, 1, 0.15, "tile"),   # 28 x 28: same cover either way
+]
+
+
+@pytest.mark.parametrize("case", SHAPE_CASES, ids=[str(c) for c in SHAPE_CASES])
+@pytest.mark.parametrize("fmt", ["f32", "packed32"])
+def test_layout_decodes_for_ad_hoc_shapes(case, fmt):
+    """Whatever plan a shape takes (column blocks, plane staging, the plain
+    padded tile), every packed entry decodes back to its CSR nonzero and the
+    staged tile covers the output."""
+    N, C, H, W, M, pad, d, plan = case
+    rng = np.random.default_rng(sum(case[1:5]))
+    rowptr, colidx, value = workloads.random_csr(M, C * 9, d, rng)
+    if fmt == "packed32":
+        value = value.astype(np.float16).astype(np.float32)
+    w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=3, S=3, stride=1, pad=pad,
+                      fmt=fmt, batch_hint=N)
+    info, rows, _ = decode_layout(w)
+    for m in range(M):
+        lo, hi = rowptr[m], rowptr[m + 1]
+        want = sorted((c, v) for c, v in zip(colidx[lo:hi].tolist(),
+                                              value[lo:hi].astype(np.float64).tolist()) if v != 0)
+        assert [(c, v) for c, v in rows.get(m, []) if v != 0] == want
+    E, F = H + 2 * pad - 2, W + 2 * pad - 2
+    tile_h = info["lane_rows"] if info["col_blocks"] else info["tile_rows"] * info["lane_rows"]
+    assert info["tiles_y"] * tile_h >= E and info["tiles_x"] * info["tile_cols"] >= F
+    got = "cols" if info["col_blocks"] else "plane" if info["plane_stage"] else "tile"
+    # the 32-bit word format takes column blocks but not plane staging
+    assert got == ("tile" if plan == "plane" and fmt == "packed32" else plan)
+    assert info["smem_bytes"] <= 200 * 1024
+    w.close()
