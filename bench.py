@@ -53,7 +53,7 @@ _CSRC = os.path.join(ROOT, "sparse_weight_direct_gb300", "csrc")
 KERNEL_SOURCES = {
     "spconv_fwd_kernel": [os.path.join(_CSRC, f) for f in (
         "spconv_kernel.cuh", "spconv_fwd.cu", "spconv_fwd_q1.cu", "spconv_fwd_q2.cu",
-        "spconv_fwd_q4.cu", "spconv_fwd_q8.cu", "spconv_fwd_tm.cu", "spconv_fwd_pairs.cu",
+        "spconv_fwd_q4.cu", "spconv_fwd_q8.cu", "spconv_fwd_pairs.cu",
         "spconv_fwd_plane.cu", "spconv_fwd_cols.cu", "spconv_host.cpp",
         "spconv_internal.h")],
     "spconv_ws_kernel": [os.path.join(_CSRC, f) for f in (
@@ -590,10 +590,10 @@ def main(argv=None):
                     help="graph: the K steps back to back from CUDA graphs over copies of the "
                          "data larger than L2 (throughput); flush: each step timed alone "
                          "after an L2 flush (latency, launch overhead included)")
-    ap.add_argument("--fmt", default="f32", choices=["f32", "packed32", "ws", "tmem"],
+    ap.add_argument("--fmt", default="f32", choices=["f32", "packed32", "ws"],
                     help="packed weight format (packed32: the first page's 32-bit words, "
                          "FP16; ws: the weight-stationary mapping, one output channel per "
-                         "block; tmem: the tensor-memory window path, 3x3 stride 1)")
+                         "block)")
     ap.add_argument("--compare-dense", action="store_true",
                     help="also time PyTorch's dense conv2d (cuDNN) on the same layer")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -91,12 +91,6 @@ typedef enum spconv_format {
                                 /* uint32 word = off << 8 | r << 4 | s} with the stretched   */
                                 /* offset off = c*H*W + r*W + s; R, S <= 16 and             */
                                 /* C*H*W + R*W + S <= 2^24; forwards take N <= 65535         */
-    SPCONV_FORMAT_TMEM = 3      /* tensor-memory window path (sm_100-family tensor memory as */
-                                /* a per-lane store addressed by a warp-uniform column):     */
-                                /* 3x3, stride 1, outputs wider than 16 columns.  8-byte     */
-                                /* entries {fp32 value, uint32 tensor-memory column of the   */
-                                /* nonzero's tap}; every row of the layer on this path (no   */
-                                /* dense-tap groups) and no channel-split clusters           */
 } spconv_format;
 
 /*
@@ -111,8 +105,7 @@ typedef enum spconv_format {
  *   host_only   != 0: as spconv_pack_host (no device work, stream ignored)
  * Errors as spconv_pack; INVALID_ARG for an unknown format or a negative
  * batch_hint, UNSUPPORTED for PACKED32 or WS with R or S > 16, for WS with
- * C*H*W + R*W + S > 2^24, and for TMEM unless R = S = 3, stride = 1 and the
- * output is wider than 16 columns.  spconv_forward(_ex) on a WS handle runs
+ * C*H*W + R*W + S > 2^24.  spconv_forward(_ex) on a WS handle runs
  * the weight-stationary kernel and returns UNSUPPORTED for N > 65535.
  */
 int spconv_pack_ex(int C, int H, int W, int M, int R, int S, int stride, int pad,
@@ -289,8 +282,7 @@ int spconv_packed_info_get(const spconv_packed *p, spconv_packed_info *info);
  * no device work).  TMA staging also needs the input pointer's tensor map to
  * encode, which this query does not try. */
 typedef struct spconv_launch_info {
-    int32_t kernel;          /* 0: tiled kernel, 1: weight-stationary kernel,    */
-                             /* 2: tiled kernel on the tensor-memory path        */
+    int32_t kernel;          /* 0: tiled kernel, 1: weight-stationary kernel     */
     int32_t grid_x, grid_y, grid_z;
     int32_t block_threads;
     int32_t cluster;         /* blocks per cluster splitting the channel chunks  */
@@ -325,13 +317,7 @@ typedef enum spconv_array {
                                /* [hp[w*NP+p], hp[w*NP+p+1]) -- and the pair       */
                                /* entries are 16 bytes {float value of q1, float   */
                                /* value of q2, int32 offset, 0}: a tap both slots  */
-                               /* use, from a 16-byte boundary.  TMEM: hdr_words   */
-                               /* words = warps + 1 first entries of each warp,    */
-                               /* then                                             */
-                               /* [warp][chunk] words of 4-bit entry counts (bits  */
-                               /* 4q..4q+3: slot q), padded to 4 words; entries    */
-                               /* {float value, uint32 column (3r + s) * 8} per    */
-                               /* warp in (channel, slot) order.  Dense groups:    */
+                               /* use, from a 16-byte boundary.  Dense groups:     */
                                /* dense_mask_words uint32 slot masks [warp][chan], */
                                /* then floats [warp][chan][slot][R*S rounded to 4] */
     SPCONV_ARRAY_BLOB_OFF = 1, /* uint32 [groups * num_chunks + 1]: blob starts in  */

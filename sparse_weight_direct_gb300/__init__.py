@@ -111,7 +111,7 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-FORMATS = {"f32": 0, "packed32": 1, "ws": 2, "tmem": 3}
+FORMATS = {"f32": 0, "packed32": 1, "ws": 2}
 
 
 def _pack(rowptr, colidx, value, C, H, W, M, R, S, stride, pad, fmt, batch_hint, host_only,
@@ -133,12 +133,10 @@ def pack(rowptr, colidx, value, *, C: int, H: int, W: int, M: int, R: int, S: in
          batch_hint: int = 0) -> PackedWeights:
     """CSR (host arrays) -> packed device layout on the current CUDA device.
     fmt: "f32" (fp32 values, precomputed offsets), "packed32" (the first page's
-    32-bit words with FP16 values), "ws" (weight-stationary: one output channel
-    per block, input read in place; Escoin, Figs. 5-7) or "tmem" (3x3 stride-1
-    layers wider than 16 columns: each nonzero's inputs read from tensor memory
-    as one 8-column load).  batch_hint: the batch
-    size the forwards will mostly use (0 = unknown); it only shapes the tiling
-    plan."""
+    32-bit words with FP16 values) or "ws" (weight-stationary: one output
+    channel per block, input read in place; Escoin, Figs. 5-7).  batch_hint:
+    the batch size the forwards will mostly use (0 = unknown); it only shapes
+    the tiling plan."""
     return _pack(rowptr, colidx, value, C, H, W, M, R, S, stride, pad, fmt, batch_hint, False,
                  stream)
 

@@ -30,11 +30,9 @@ __global__ void wait_selftest_kernel(unsigned int *flags, unsigned long long lim
     if (ok && threadIdx.x == 0) atomicOr(flags, 2u);
 }
 
-KernelFn pick(int S, int stride, int P, int Q, int LR, bool tm = false, bool pairs = false,
-              bool plane = false, bool cols = false, int W = 0) {
-    if (cols) return (S == 3 && stride == 1 && !tm && !pairs && !plane) ? pick_cols(P, Q, LR)
-                                                                        : nullptr;
-    if (tm) return (S == 3 && stride == 1 && LR == 1) ? pick_tm(P, Q) : nullptr;
+KernelFn pick(int S, int stride, int P, int Q, int LR, bool pairs = false, bool plane = false,
+              bool cols = false, int W = 0) {
+    if (cols) return (S == 3 && stride == 1 && !pairs && !plane) ? pick_cols(P, Q, LR) : nullptr;
     if (pairs) return pick_pairs(S, stride, P, Q, LR);
     if (plane) return (S == 3 && stride == 1 && LR == 2) ? pick_plane(P, Q, W) : nullptr;
     switch (Q) {
@@ -82,19 +80,15 @@ bool dense_taps_supported(int R, int S, int stride, int LR, int Q) {
     return stride == 1 && R == S && (S == 3 || (S == 5 && LR == 1)) && Q <= 4;
 }
 
-int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm, bool pairs,
-                              bool plane, bool cols) {
-    return pick(S, stride, P, Q, LR, tm, pairs, plane, cols) ? 0 : -1;
+int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool pairs, bool plane,
+                              bool cols) {
+    return pick(S, stride, P, Q, LR, pairs, plane, cols) ? 0 : -1;
 }
 
 bool plane_stage_supported(int H, int W, int R, int S, int stride, int pad, int P, int LR, int Q) {
     return R == 3 && S == 3 && stride == 1 && pad == 1 && LR == 2 && H == 2 * P && W >= 2 &&
            W <= 16 && (W * 4) % 16 != 0 && (H * W) % 4 == 0 &&
-           pick(S, stride, P, Q, LR, false, false, true, false, W);
-}
-
-bool tm_supported(int R, int S, int stride, int LR) {
-    return R == 3 && S == 3 && stride == 1 && LR == 1;
+           pick(S, stride, P, Q, LR, false, true, false, W);
 }
 
 // Shared memory of the stage buffers a block with `split` cluster ranks uses.
@@ -131,7 +125,6 @@ size_t forward_smem_bytes(const Geometry &g, int split) {
         if (part > bytes) bytes = part;
         bytes += 128;  // room to align the stage buffers to 128 bytes
     }
-    if (g.format == 3 && bytes < kTmMinSmem) bytes = kTmMinSmem;
     // plane staging (one-image layers): at most two blocks per SM, as with the
     // padded tile, so the cluster blocks spread over the SMs
     if (g.plane_stage && bytes < 76 * 1024) bytes = 76 * 1024;
@@ -141,10 +134,9 @@ size_t forward_smem_bytes(const Geometry &g, int split) {
 cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast, bool pdl,
                            const float *x, float *y, const float *bias, int act,
                            const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream) {
-    const bool tm = g.format == 3;
-    KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows, tm, g.tap_pairs != 0,
+    KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows, g.tap_pairs != 0,
                        g.plane_stage != 0, g.col_blocks != 0, g.W);
-    if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks || (tm && split != 1))
+    if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks)
         return cudaErrorInvalidConfiguration;
     const size_t smem = forward_smem_bytes(g, split);
     if (smem > 48 * 1024) {

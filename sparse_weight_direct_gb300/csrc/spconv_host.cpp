@@ -195,20 +195,12 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
         const double compute_s = 2.0 * nnz * g.E * g.F / (0.18 * kSMs * 128 * 2 * 2.07e9);
         if (staging_s > compute_s) g.slots = 8;
     }
-    const bool tm = g.format == SPCONV_FORMAT_TMEM;
-    if (tm) {
-        // Tensor-memory path: each warp pair's window fill is shared by its
-        // 2 Q output channels, so Q = 8 unless that leaves fewer blocks than
-        // SMs (no channel-split clusters on this path).
-        if (!spconv::tm_supported(R, S, stride, g.lane_rows)) return SPCONV_ERR_UNSUPPORTED;
-        g.slots = spatial * groups_of(8) >= (int64_t)kSMs ? 8 : 4;
-    }
     g.groups = (M + spconv::kWarps * g.slots - 1) / (spconv::kWarps * g.slots);
     g.num_slots = g.groups * spconv::kWarps * g.slots;
     g.hdr_words = (int)round_up((size_t)spconv::kWarps * g.slots + 1, 4);
     if (g.groups > 65535) return SPCONV_ERR_UNSUPPORTED;
-    if (spconv::forward_variant_supported(S, stride, g.tile_rows, g.slots, g.lane_rows, tm, false,
-                                          false, g.col_blocks != 0) != 0)
+    if (spconv::forward_variant_supported(S, stride, g.tile_rows, g.slots, g.lane_rows, false, false,
+                                          g.col_blocks != 0) != 0)
         return SPCONV_ERR_UNSUPPORTED;
     // Whole-image tiles of images whose rows TMA cannot address: one bulk copy
     // of the chunk's raw planes (dense, pitch W) instead of per-element
@@ -245,7 +237,7 @@ int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx)
     const double crs = (double)g.C * g.R * g.S;
     auto nnz_of = [&](int m) { return (int64_t)rowptr[m + 1] - rowptr[m]; };
     std::vector<int> dense, sparse;
-    const bool can_dense = g.format != SPCONV_FORMAT_TMEM && !g.plane_stage && !g.col_blocks &&
+    const bool can_dense = !g.plane_stage && !g.col_blocks &&
                            spconv::dense_taps_supported(g.R, g.S, g.stride, g.lane_rows, g.slots);
     for (int m = 0; m < g.M; ++m)
         (can_dense && nnz_of(m) / crs >= kDenseRowMin ? dense : sparse).push_back(m);
@@ -406,8 +398,7 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
                          ? 1
                          : (int)std::min<int64_t>(spconv::kMaxSplit,
                                                   (2 * kSMs + base_blocks - 1) / base_blocks);
-    // (the tensor-memory path runs without channel-split clusters)
-    want_split = g.format == SPCONV_FORMAT_TMEM ? 1 : std::max(want_split, 1);
+    want_split = std::max(want_split, 1);
     // Plane-staged plans aim at one block per SM: their small stages hold twice
     // the channels, and the one-image ResNet-style layer measured 5.98 us with
     // 4-block clusters of 64-channel chunks (128 blocks) against 6.47 us with
@@ -425,11 +416,8 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
     // block per SM).
     const bool one_per_block =
         g.batch_hint > 0 && want_split > 1 && (int64_t)cap * want_split >= C;
-    const bool tm = g.format == SPCONV_FORMAT_TMEM;
     for (int chunk = cap; chunk >= 1; --chunk) {
         const int nch = (C + chunk - 1) / chunk;
-        // tensor-memory blobs: per-warp first entries + [warp][channel] counts
-        if (tm) g.hdr_words = (int)round_up((size_t)g.warps * (chunk + 1) + 1, 4);
         const size_t hdr_bytes = (size_t)g.hdr_words * 4;
         const size_t in_stage = round_up(
             ((size_t)chunk * g.plane +
@@ -483,7 +471,7 @@ void choose_tap_pairs(spconv::Geometry &g, const std::vector<int32_t> &group_fla
     g.tap_pairs = 0;
     if (g.format != SPCONV_FORMAT_F32 || g.plane_stage || g.col_blocks ||
         spconv::forward_variant_supported(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows,
-                                          false, true) != 0)
+                                          true) != 0)
         return;
     int64_t pairs = 0, total = 0;
     std::vector<int32_t> cols;
@@ -679,38 +667,6 @@ int build_layout(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx,
             }
             uint32_t *hdr = reinterpret_cast<uint32_t *>(blob);
             HostEntry *ent = reinterpret_cast<HostEntry *>(blob + (size_t)g.hdr_words * 4);
-            if (g.format == SPCONV_FORMAT_TMEM) {
-                // [warps + 1] first entries, [warp][chunk] 4-bit counts per slot;
-                // entries per warp in (channel, slot) order, each {value,
-                // tensor-memory column of its tap group (3 r + s) * 8}
-                uint32_t *counts = hdr + g.warps + 1;
-                uint32_t e = 0;
-                const int c0 = k * g.chunk;
-                for (int w = 0; w < g.warps; ++w) {
-                    hdr[w] = e;
-                    for (int c = c0; c < c_end; ++c) {
-                        uint32_t word = 0;
-                        for (int q = 0; q < g.slots; ++q) {
-                            const int slot = (grp * g.warps + w) * g.slots + q;
-                            const std::vector<int64_t> &idx = order[slot];
-                            size_t &t = cursor[slot];
-                            uint32_t n = 0;
-                            for (; t < idx.size() && colidx[idx[t]] / RS == c; ++t, ++n) {
-                                const int col = colidx[idx[t]];
-                                HostEntry h;
-                                h.value = value[idx[t]];
-                                h.off = ((col % RS) / g.S * 3 + col % g.S) * 8;
-                                ent[e++] = h;
-                            }
-                            if (n > 15) return SPCONV_ERR_UNSUPPORTED;  // 3 x 3: at most 9
-                            word |= n << (4 * q);
-                        }
-                        counts[w * g.chunk + (c - c0)] = word;
-                    }
-                }
-                hdr[g.warps] = e;
-                continue;
-            }
             uint32_t *word = reinterpret_cast<uint32_t *>(blob + (size_t)g.hdr_words * 4);
             if (g.tap_pairs) {
                 write_pair_blob(g, grp, k, c_end, order, colidx, value, cursor, hdr, ent);
@@ -866,7 +822,7 @@ int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
                 int batch_hint, spconv_packed **out) {
     if (!out) return SPCONV_ERR_INVALID_ARG;
     if (format != SPCONV_FORMAT_F32 && format != SPCONV_FORMAT_PACKED32 &&
-        format != SPCONV_FORMAT_WS && format != SPCONV_FORMAT_TMEM)
+        format != SPCONV_FORMAT_WS)
         return SPCONV_ERR_INVALID_ARG;
     if (batch_hint < 0) return SPCONV_ERR_INVALID_ARG;
     int st = validate_shape(C, H, W, M, R, S, stride, pad);
@@ -1077,12 +1033,12 @@ bool choose_pdl(const spconv::Geometry &g, int N, int split, bool group_fast) {
 }
 
 // Blocks per cluster along the channel chunks: none when the grid already
-// fills the GPU (splitting it further measured slower on every batched layer)
-// or on the tensor-memory path, else enough for about two blocks per SM
+// fills the GPU (splitting it further measured slower on every batched layer),
+// else enough for about two blocks per SM
 // (measured best on the one-image ResNet-style layer).
 int choose_split(const spconv::Geometry &g, int N) {
     const int64_t blocks = (int64_t)N * g.tiles_y * g.tiles_x * g.groups;
-    if (blocks >= kSMs || g.format == SPCONV_FORMAT_TMEM) return 1;
+    if (blocks >= kSMs) return 1;
     int s = (int)std::min<int64_t>(spconv::kMaxSplit, (2 * kSMs + blocks - 1) / blocks);
     return std::max(1, std::min(s, g.num_chunks));
 }
@@ -1393,7 +1349,7 @@ __attribute__((visibility("default"))) int spconv_launch_info_get(const spconv_p
     const bool group_fast = choose_group_fast(g, N, p->nnz);
     unsigned gx = 0, gy = 0;
     spconv::forward_grid(g, N, split, group_fast, &gx, &gy);
-    info->kernel = g.format == SPCONV_FORMAT_TMEM ? 2 : 0;
+    info->kernel = 0;
     info->grid_x = (int32_t)gx;
     info->grid_y = (int32_t)gy;
     info->grid_z = 1;

@@ -79,8 +79,7 @@ struct Geometry {
     int groups;       // output-channel groups (grid y)
     int num_slots;    // groups * warps * slots
     int format;       // 0 = {fp32, int32 offset} entries, 1 = 32-bit packed words,
-                      // 2 = weight-stationary rows (one output channel per block),
-                      // 3 = {fp32, tensor-memory column} entries (tensor-memory path)
+                      // 2 = weight-stationary rows (one output channel per block)
     int batch_hint;   // batch size the plan targets (0 = unknown)
     int hdr_words;    // words of a sparse blob header (warps * slots + 1, to 4; with
                       // tap pairs + warps * slot pairs + 1)
@@ -110,14 +109,10 @@ struct DeviceArrays {
 };
 
 // Kernel variants compiled for sm_103a.  Returns 0 if (S, stride, P, Q, LR)
-// has an instance (tm: of the tensor-memory window path; pairs: with tap-pair
-// segments; plane: with plane staging; cols: with column blocks), else -1.
-int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool tm = false,
-                              bool pairs = false, bool plane = false, bool cols = false);
-
-// Whether a layer shape can take the tensor-memory window path (3 x 3,
-// stride 1, one lane row).
-bool tm_supported(int R, int S, int stride, int LR);
+// has an instance (pairs: with tap-pair segments; plane: with plane staging;
+// cols: with column blocks), else -1.
+int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool pairs = false,
+                              bool plane = false, bool cols = false);
 
 // Plane staging: zeroed words before and after the raw planes of a stage, so
 // that taps reaching past the first or last plane read finite values.
@@ -129,11 +124,6 @@ constexpr int kPlaneTail = 48;
 // a TMA tensor map cannot address (4 W not a multiple of 16), and planes that
 // start on 16-byte boundaries (H W a multiple of 4).
 bool plane_stage_supported(int H, int W, int R, int S, int stride, int pad, int P, int LR, int Q);
-
-// Smallest dynamic shared memory of a tensor-memory launch: with more than
-// a third of an SM's shared memory per block at most two blocks share an SM,
-// so their tensor-memory allocations (256 columns each) always fit.
-constexpr size_t kTmMinSmem = 80 * 1024;
 
 // Whether a layer shape can use the dense-tap path (output channels with dense
 // rows get their K x K blocks applied from a register window).

@@ -471,156 +471,18 @@ static __device__ __forceinline__ void run_segment_words(float (&acc)[P], const 
     for (; j < j1; ++j) apply_word<P, ROW_STEP, ST_CT>(acc, sb, ent[j], p, row_step);  // tail
 }
 
-// ---------------------------------------------------------------- tensor-memory window path
-//
-// Shared memory delivers one 4-byte word per lane per FMA on the path above,
-// which caps it at a quarter of the fp32 rate.  This path reads the FMA's input
-// from tensor memory instead: per input channel, each lane's input window
-// ((P + 2) rows x 3 columns around its output column, 3 x 3 stride 1) is
-// loaded from the staged tile once and stored to the lane's row of tensor
-// memory as nine 8-column groups, group (r, s) holding the window rows r ..
-// r + 7 of column s.  A nonzero at tap (r, s) then needs one 8-column load at a
-// warp-uniform address (the group) and P FMAs -- the tap becomes an address,
-// not a register index, so no dispatch is needed.  Warp w reaches the lanes
-// 32 * (w % 4) .. + 31 of tensor memory, so warps w and w + 4 (the same output
-// columns, different output channels) share their window: they fill
-// alternate channels into two buffers and meet at a named barrier per channel.
-constexpr int kTmCols = 256;        // tensor-memory columns a block allocates
-constexpr int kTmChannelCols = 72;  // 9 taps x 8 columns per staged channel
-
-static __device__ __forceinline__ void tm_alloc(uint32_t *slot) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                     smem_u32(slot)),
-                 "r"(kTmCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
-}
-static __device__ __forceinline__ void tm_dealloc(uint32_t taddr) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr),
-                 "r"(kTmCols)
-                 : "memory");
-}
-static __device__ __forceinline__ void tm_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-}
-static __device__ __forceinline__ void tm_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-}
-static __device__ __forceinline__ void tm_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(
-                     taddr),
-                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
-                 "r"(v[7])
-                 : "memory");
-}
-static __device__ __forceinline__ void tm_ld8(uint32_t (&v)[8], uint32_t taddr) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
-                   "=r"(v[6]), "=r"(v[7])
-                 : "r"(taddr));
-}
-// Waits for this thread's tensor-memory loads; the loaded registers are
-// operands so that no use of them is scheduled before the wait.
-static __device__ __forceinline__ void tm_wait_ld(uint32_t (&v)[8]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
-                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
-                   "+r"(v[6]), "+r"(v[7])::"memory");
-}
-// Named barrier of the two warps sharing a quarter of tensor memory; this
-// warp's stores are complete and ordered before the partner's later loads.
-static __device__ __forceinline__ void tm_pair_sync(int id) {
-    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-    tm_fence_before();
-    asm volatile("bar.sync %0, 64;\n" ::"r"(id) : "memory");
-    tm_fence_after();
-}
-// Named-barrier vote of the pair: true if either warp passes true.
-static __device__ __forceinline__ bool tm_pair_any(int id, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, 64, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}\n"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id)
-        : "memory");
-    return r != 0;
-}
-
-// Stores one staged channel's windows: sbc points at this lane's staged
-// column (row 0) of the channel; group (r, s) at taddr + (3 r + s) * 8.
-template <int P, int RP>
-static __device__ __forceinline__ void tm_fill(const float *sbc, uint32_t taddr) {
-    // one kernel column at a time: (P + 2) window values live, not 3 (P + 2)
-#pragma unroll 1
-    for (int s = 0; s < 3; ++s) {
-        float w[P + 2];
-#pragma unroll
-        for (int i = 0; i < P + 2; ++i) w[i] = sbc[i * RP + s];
-#pragma unroll
-        for (int r = 0; r < 3; ++r) {
-            uint32_t v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __float_as_uint(w[r + (i < P ? i : P - 1)]);
-            tm_st8(taddr + (uint32_t)((r * 3 + s) * 8), v);
-        }
-    }
-}
-
-// One chunk on the tensor-memory path.  The blob header holds each warp's
-// first entry (kWarps + 1 words), then per (warp, channel) a word of 4-bit
-// counts, one per slot; the entries of a warp follow in (channel, slot)
-// order, each {value, column of its tap group}.
-template <int P, int Q, int RP>
-static __device__ __forceinline__ void run_tm_chunk(float (&acc)[Q][P], const float *sbl,
-                                                    const uint32_t *hdr, const float2 *ent,
-                                                    int warp, int chunk, int cc, int plane,
-                                                    uint32_t tbase) {
-    const int pair = 1 + (warp & 3), h = warp >> 2;
-    const uint32_t *cnt = hdr + (kWarps + 1) + warp * chunk;
-    int j = (int)hdr[warp];
-    if (h == 0) tm_fill<P, RP>(sbl, tbase);
-    tm_pair_sync(pair);
-    for (int cl = 0; cl < cc; ++cl) {
-        // the next channel goes into the other buffer, which both warps
-        // finished reading before the last barrier
-        if (cl + 1 < cc && h == ((cl + 1) & 1))
-            tm_fill<P, RP>(sbl + (cl + 1) * plane,
-                           tbase + (uint32_t)(((cl + 1) & 1) * kTmChannelCols));
-        const uint32_t counts = cnt[cl];
-        const uint32_t tb = tbase + (uint32_t)((cl & 1) * kTmChannelCols);
-#pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const int nq = (int)((counts >> (4 * q)) & 15u);
-            for (int t = 0; t < nq; ++t, ++j) {
-                const float2 e = ent[j];
-                uint32_t x[8];
-                tm_ld8(x, tb + __float_as_uint(e.y));
-                tm_wait_ld(x);
-#pragma unroll
-                for (int r = 0; r < P; ++r) acc[q][r] = fmaf(e.x, __uint_as_float(x[r]), acc[q][r]);
-            }
-        }
-        tm_pair_sync(pair);
-    }
-}
-
 // P: output rows per lane; Q: output channels per warp; LR: lane rows (1, or 2
 // interleaved half-warps of 16 lanes for outputs at most 16 wide); S_CT/ST_CT:
 // kernel width and stride when known at compile time (0 = read from p); MODE:
-// 0 the shared-memory path, kModeTmem the tensor-memory window path (3 x 3,
-// stride 1, one lane row), kModePairs the shared-memory path with tap-pair
+// 0 the shared-memory path, kModePairs the shared-memory path with tap-pair
 // segments (blobs of the tap-pair layout).  The pair loop lives in instances
 // of its own: compiled into the plain ones it slowed layers that never use it.
-constexpr int kModeTmem = 1;
 constexpr int kModePairs = 2;
 constexpr int kModePlane = 3;  // plane staging (see apply_entry_plane)
 constexpr int kModeCols = 4;   // column blocks: a lane's P outputs run along a row
 template <int P, int Q, int S_CT, int ST_CT, int LR, int MODE = 0, int PLANE_RS = 0>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     spconv_fwd_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap) {
-    constexpr bool TM = MODE == kModeTmem;
     constexpr bool PAIRS = MODE == kModePairs;
     constexpr bool PLANE = MODE == kModePlane;
     // Column blocks (stride 1): lane (ly, lx) holds outputs (ly, lx*P + r) of
@@ -630,11 +492,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     static_assert(!COLS || ST_CT == 1, "column blocks: stride 1");
     static_assert(!PLANE || (S_CT == 3 && ST_CT == 1 && LR == 2), "plane staging: 3x3, two lane rows");
     static_assert(PLANE || PLANE_RS == 0, "a fixed row step is a plane-staging instance");
-    static_assert(!TM || (S_CT == 3 && ST_CT == 1 && LR == 1 && P <= 8), "tensor-memory path: 3x3, stride 1");
     static_assert(!PAIRS || Q == 2 || Q == 4, "tap pairs: 2 or 4 output channels per warp");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar[2];
-    __shared__ uint32_t tm_slot;   // tensor-memory address of the block's columns (TM)
     __shared__ int stage_done[2];  // warps that have released a stage (TMA path)
     __shared__ int issued[2];      // copy phases issued into each stage
     // stage buffers start on a 128-byte boundary (TMA destination)
@@ -674,12 +534,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int nmine = k_end - k_begin;
     const int nslot = kWarps * Q;
 
-    // Tensor memory: one warp allocates the block's columns (at most two
-    // blocks share an SM, so 2 x kTmCols always fit and the allocation never
-    // waits on another block of this kernel).
-    if constexpr (TM) {
-        if (warp == 0) tm_alloc(&tm_slot);
-    }
     // Barrier set-up first: its release fence would otherwise wait for the
     // global loads below (a whole memory round trip before the first copy).
     if (threadIdx.x == 0) {
@@ -702,13 +556,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             if ((i - sidx * (p.stage_bytes / 16)) * 16 < p.in_stage_bytes) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    if constexpr (TM) tm_fence_before();
     __syncthreads();
-    uint32_t tbase = 0;  // this warp's quarter (lanes) of the block's tensor memory
-    if constexpr (TM) {
-        tm_fence_after();
-        tbase = tm_slot + ((uint32_t)((warp & 3) * 32) << 16);
-    }
 
     // Loads that nothing computed here feeds, issued before any wait so that
     // their latency overlaps the pipeline: the group's flags, the first
@@ -817,12 +665,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         }
         const bool ok = mbar_wait_bounded(&bar[s], (uint32_t)((it >> 1) & 1));
         if (p.use_tma || PLANE) {
-            // warps run independently (on the tensor-memory path, in pairs);
-            // a warp that timed out stops, with its partner
-            if constexpr (TM)
-                failed = tm_pair_any(1 + (warp & 3), !ok);
-            else
-                failed = !ok;
+            // warps run independently; a warp that timed out stops
+            failed = !ok;
         } else {
             failed = __syncthreads_or(!ok) != 0;  // cp.async data of all threads
         }
@@ -838,13 +682,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                  (lx < p.W ? ly * p.W + lx : 2 * p.W + ly * (LC - p.W) + (lx - p.W));
         }
         const uint32_t *hdr = reinterpret_cast<const uint32_t *>(base + p.in_stage_bytes);
-        if constexpr (TM) {
-            const float2 *ent = reinterpret_cast<const float2 *>(hdr + p.hdr_words);
-            const int k = k_begin + it;
-            run_tm_chunk<P, Q, row_pitch_s1(3, 1)>(acc, sb + p.shift, hdr, ent, warp, p.chunk,
-                                                    min(p.chunk, p.C - k * p.chunk), p.plane,
-                                                    tbase);
-        } else if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4 && !PLANE && !COLS) {
+        if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4 && !PLANE && !COLS) {
             if (dense) {
                 const int k = k_begin + it;
                 run_dense_chunk<P, Q, S_CT, LR, row_pitch_s1(S_CT, LR)>(
@@ -852,9 +690,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                     warp, p.chunk, min(p.chunk, p.C - k * p.chunk), p.plane);
             }
         }
-        if (TM) {
-            // done above
-        } else if (!dense && p.fmt == 0) {
+        if (!dense && p.fmt == 0) {
             const float2 *ent = reinterpret_cast<const float2 *>(hdr + p.hdr_words);
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
@@ -910,14 +746,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     // block writes no outputs; its copies still in flight (at most one phase
     // per stage, since a stage is refilled only after it was consumed) are
     // waited for, again with a limit, before shared memory can go away.
-    if constexpr (TM) tm_fence_before();
     failed = __syncthreads_or(failed) != 0;
-    if constexpr (TM) {
-        // every tensor-memory access of the block is complete (loads are
-        // waited for, stores before each pair barrier)
-        tm_fence_after();
-        if (warp == 0) tm_dealloc(tm_slot);
-    }
     if (failed) {
         if (!p.use_tma && !PLANE) cp_async_wait_all();
         if (threadIdx.x == 0) {
@@ -1118,8 +947,6 @@ KernelFn pick_q1(int S, int stride, int P, int LR);
 KernelFn pick_q2(int S, int stride, int P, int LR);
 KernelFn pick_q4(int S, int stride, int P, int LR);
 KernelFn pick_q8(int S, int stride, int P, int LR);
-// Tensor-memory window instances (3 x 3, stride 1, one lane row), Q in {4, 8}.
-KernelFn pick_tm(int P, int Q);
 // Tap-pair instances (Q = 4, one lane row; 3x3 and 5x5 stride 1, 11x11 stride 4).
 KernelFn pick_pairs(int S, int stride, int P, int Q, int LR);
 // Plane-staging instances (3x3 stride 1, two lane rows, Q in {1, 2}); 14-wide

@@ -105,38 +105,6 @@ def decode_layout(w):
                                 rows.setdefault(m, []).append((c * RS + int(t), float(blk[t])))
                 continue
             hdr = blob[:hw * 4].view(np.uint32)
-            if info["format"] == 3:
-                # tensor-memory blobs: [warps + 1] first entries, [warp][chunk]
-                # 4-bit counts per slot, entries {value, (3 r + s) * 8} per warp
-                # in (channel, slot) order
-                assert hw == (NW * (chunk + 1) + 1 + 3) // 4 * 4
-                first = hdr[:NW + 1].astype(np.int64)
-                assert first[0] == 0 and np.all(np.diff(first) >= 0)
-                counts = hdr[NW + 1:NW + 1 + NW * chunk].reshape(NW, chunk)
-                ent = blob[hw * 4:].view([("value", "<f4"), ("col", "<u4")])
-                assert first[NW] <= ent.size
-                assert not blob[hw * 4 + 8 * int(first[NW]):].any()
-                cc = min(chunk, info["C"] - k * chunk)
-                assert not counts[:, cc:].any()
-                for w in range(NW):
-                    j = int(first[w])
-                    for cl in range(cc):
-                        for q in range(Q):
-                            n = int(counts[w, cl]) >> (4 * q) & 15
-                            m = int(slot_oc[(g * NW + w) * Q + q])
-                            assert m >= 0 or n == 0
-                            taps = []
-                            for e in ent[j:j + n]:
-                                col = int(e["col"])
-                                assert col % 8 == 0 and col < 72
-                                r, s_ = divmod(col // 8, 3)
-                                taps.append(col)
-                                c = k * chunk + cl
-                                rows.setdefault(m, []).append(((c * R + r) * S + s_, float(e["value"])))
-                            assert taps == sorted(set(taps))  # tap order, no repeats
-                            j += n
-                    assert j == first[w + 1]
-                continue
             assert hdr[0] == 0 and np.all(np.diff(hdr[:spg + 1].astype(np.int64)) >= 0)
             if info["format"] == 1:
                 # [31:16] fp16 value, [15:8] channel in chunk, [7:4] column, [3:0] row
@@ -227,12 +195,8 @@ def decode_layout(w):
     return info, rows, slot_oc
 
 
-TMEM_LAYERS = ["vgg3x3", "sweep50", "sweep90", "sweep99"]
-
-
 @pytest.mark.parametrize("fmt,name", [(f, n) for f in ("f32", "packed32") for n in (
-    "tiny", "tiny_int", "resnet3x3", "vgg3x3", "sweep90", "sweep99", "alex11x11", "conv5x5")]
-    + [("tmem", n) for n in TMEM_LAYERS])
+    "tiny", "tiny_int", "resnet3x3", "vgg3x3", "sweep90", "sweep99", "alex11x11", "conv5x5")])
 def test_packed_layout_decodes_to_csr(name, fmt):
     L = workloads.LAYERS[name]
     rowptr, colidx, value = workloads.make_weights(L)
