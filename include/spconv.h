@@ -205,7 +205,11 @@ int spconv_pack_host(int C, int H, int W, int M, int R, int S, int stride, int p
  * error word and returns SPCONV_OK if it was clear, SPCONV_ERR_DEVICE if not
  * (then *flags, if not NULL, receives the bits: 1 = a pipeline wait in the
  * forward kernel ran out its time limit and the kernel returned without
- * writing its outputs).  Errors: INVALID_ARG (NULL or host-only handle), CUDA.
+ * writing its outputs; 2 = after such a timeout, the wait for the block's
+ * copies still in flight ran out as well, so an asynchronous copy may have
+ * landed in shared memory after the block left: treat the CUDA context as
+ * suspect and reset it before further use).  Errors: INVALID_ARG (NULL or
+ * host-only handle), CUDA.
  */
 int spconv_device_status(const spconv_packed *p, void *stream, int32_t *flags);
 

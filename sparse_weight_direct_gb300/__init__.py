@@ -81,7 +81,9 @@ class PackedWeights:
 
     def device_status(self, stream=None) -> int:
         """Synchronise the stream and read/clear the device error flags
-        (0 = clean; bit 0 = a pipeline wait of the forward kernel timed out)."""
+        (0 = clean; bit 0 = a pipeline wait of the forward kernel timed out;
+        bit 1 = the wait for the block's copies in flight after that timeout
+        ran out too: the context is then suspect and should be reset)."""
         flags = ctypes.c_int32(0)
         rc = _lib.lib().spconv_device_status(self.handle, _stream_ptr(stream), ctypes.byref(flags))
         if rc not in (_lib.SPCONV_OK, _lib.SPCONV_ERR_DEVICE):

@@ -1073,11 +1073,12 @@ int check_forward(int N, int C, int H, int W, int M, int R, int S, int stride, i
     return SPCONV_OK;
 }
 
-// Launches a forward whose arguments check_forward accepted (N > 0).  after_copy:
-// the previous kernel on the stream is the copy of this forward's input, so the
-// forward is launched with programmatic dependent launch behind it.
+// Launches a forward whose arguments check_forward accepted (N > 0).  The
+// launch mode (programmatic dependent launch or not) is choose_pdl's, also
+// behind the host-buffer forward's copy kernel: the forward waits for the
+// previous kernel either way before it reads its input.
 int enqueue_forward(int N, const float *input, const spconv_packed *packed, const float *bias,
-                    int act, float *output, cudaStream_t stream, bool after_copy = false) {
+                    int act, float *output, cudaStream_t stream) {
     const spconv::Geometry &g = packed->g;
     if (g.format == SPCONV_FORMAT_WS) {
         cudaError_t e =
@@ -1093,7 +1094,7 @@ int enqueue_forward(int N, const float *input, const spconv_packed *packed, cons
         const CUtensorMap *tmap = input_tmap(packed, input, N, tmp);
         const int split = choose_split(g, N);
         const bool group_fast = choose_group_fast(g, N, packed->nnz);
-        const bool pdl = after_copy || choose_pdl(g, N, split, group_fast);
+        const bool pdl = choose_pdl(g, N, split, group_fast);
         cudaError_t e = spconv::launch_forward(g, N, split, group_fast, pdl, input, output, bias,
                                                act, packed->d, tmap, stream);
         if (e != cudaSuccess) {
@@ -1182,8 +1183,7 @@ __attribute__((visibility("default"))) int spconv_forward_host(
             return SPCONV_ERR_CUDA;
         }
         const bool direct = out_bytes <= kDirectOutBytes;
-        st = enqueue_forward(N, dev_input, packed, bias, act, direct ? out_view : dev_output, s,
-                             packed->g.format != SPCONV_FORMAT_WS);
+        st = enqueue_forward(N, dev_input, packed, bias, act, direct ? out_view : dev_output, s);
         if (st != SPCONV_OK || direct) return st;
         if (spconv::launch_copy(dev_output, out_view, out_bytes / sizeof(float), s) !=
             cudaSuccess) {

@@ -105,7 +105,8 @@ struct DeviceArrays {
     const int *slot_oc;          // [num_slots]: head slot -> output channel, else -1
     const int *slot_next;        // [num_slots]: next part (group-local slot) or -1
     const int *group_flags;      // [groups]: bit 0 dense-tap blobs, bit 1 split rows
-    unsigned int *err;           // device error flags (bit 0: pipeline wait timed out)
+    unsigned int *err;           // device error flags (bit 0: pipeline wait timed out;
+                                 // bit 1: the drain of in-flight copies timed out too)
 };
 
 // Kernel variants compiled for sm_103a.  Returns 0 if (S, stride, P, Q, LR)

@@ -555,6 +555,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             const int sidx = i / (p.stage_bytes / 16);
             if ((i - sidx * (p.stage_bytes / 16)) * 16 < p.in_stage_bytes) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        // the bulk copies (async proxy) later overwrite part of these bytes:
+        // each thread orders its own generic-proxy zero stores before them
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     }
     __syncthreads();
 
@@ -745,14 +748,18 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     // Every warp is out of the pipeline.  If any gave up waiting, the whole
     // block writes no outputs; its copies still in flight (at most one phase
     // per stage, since a stage is refilled only after it was consumed) are
-    // waited for, again with a limit, before shared memory can go away.
+    // waited for, again with a limit, before shared memory can go away.  A
+    // drain that runs out too is recorded apart (bit 1): a copy may then still
+    // be writing into shared memory that the SM's next block will own.
     failed = __syncthreads_or(failed) != 0;
     if (failed) {
         if (!p.use_tma && !PLANE) cp_async_wait_all();
         if (threadIdx.x == 0) {
             atomicOr(p.err, 1u);
             for (int st2 = 0; st2 < 2; ++st2)
-                if (issued[st2] > 0) mbar_wait_bounded(&bar[st2], (uint32_t)((issued[st2] - 1) & 1));
+                if (issued[st2] > 0 &&
+                    !mbar_wait_bounded(&bar[st2], (uint32_t)((issued[st2] - 1) & 1)))
+                    atomicOr(p.err, 2u);
         }
         __syncthreads();
     }

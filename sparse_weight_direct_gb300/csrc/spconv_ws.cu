@@ -176,10 +176,12 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (failed) {
         // Let the copies still in flight (pieces k and k + 1, if issued) land
         // before the block's shared memory goes away, again with a limit.
+        // A drain that runs out too is recorded apart (bit 1): a copy may then
+        // still be writing into shared memory that the SM's next block will own.
         if (threadIdx.x == 0) {
             atomicOr(p.err, 1u);
             for (int j = k; j < min(k + 2, npieces); ++j)
-                mbar_wait_bounded(&bar[j & 1], (uint32_t)((j >> 1) & 1));
+                if (!mbar_wait_bounded(&bar[j & 1], (uint32_t)((j >> 1) & 1))) atomicOr(p.err, 2u);
         }
         return;
     }

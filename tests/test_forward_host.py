@@ -71,6 +71,8 @@ def test_forward_host_parity(name, integer):
     yd = torch.empty(yh.shape, device="cuda")
     s = torch.cuda.Stream()
     yd.fill_(float("nan"))
+    # the fill runs on the current stream, the forward on s: order them
+    s.wait_stream(torch.cuda.current_stream())
     swd.forward_host(xh, w, yh, xd, yd, stream=s)
     s.synchronize()
     # page-locked buffers from torch are mapped on the device: the input went
