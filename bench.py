@@ -1,22 +1,31 @@
 """Benchmark of the sparse-weight direct convolution forward on GB300.
 
-One step = one forward of one seeded synthetic layer (default: the ResNet-style
-3x3 layer, N=1, C=M=256, 14x14, 90 % unstructured sparsity) through the C ABI
+One step = one forward of one seeded synthetic layer (default: the 90 %
+layer of the sparsity sweep, N=8, C=M=512, 28x28, 3x3, lognormal per-row
+density -- the largest one-GPU layer in the 90-99 % range) through the C ABI
 (spconv_forward), inputs resident in HBM.  The packing (spconv_pack) runs once
 per weight set before timing, as in deployment, and is reported separately.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
-                    [--impl ours|reference]
+                    [--impl ours|reference] [--no-layers]
 
-Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
-device synchronize; each step flushes L2 (a 256 MiB write, outside the timed
-events) and is timed with CUDA events on the launching stream.  Rank 0 prints
-one JSON line.  --impl reference times the CPU oracle (the only other
-implementation of this path) on the host cores on the same layer.
+Timing (default, --timing graph): W untimed warm-up steps, then the K steps
+replayed back to back from CUDA graphs, each on its own copy of input,
+weights and output, the copies together larger than twice the L2; CUDA events
+on the launching stream around the region, a barrier and a device
+synchronize on both sides, max over ranks.  --timing flush times each step
+alone after a 256 MiB L2 flush instead.  Rank 0 prints one JSON line.
 
-End to end (`e2e`): the same layer through spconv_forward_host, one call per
-step with the input and the result in page-locked host memory (the copies to
-and from the GPU inside the timed events).
+`layers`: every other seeded layer (ResNet-, VGG-, AlexNet-style, the rest of
+the sweep) timed the same back-to-back way after the headline, each with its
+µs/layer, roofline and in-core fractions and recorded DRAM traffic.
+
+End to end (`e2e`): the headline layer through spconv_forward_host, one call
+per step with the input and the result in page-locked host memory (the copies
+to and from the GPU inside the timed events).
+
+--impl reference times the CPU oracle (the only other implementation of this
+path) on the host cores on the same layer; its `config` is the same dict.
 """
 from __future__ import annotations
 
@@ -185,11 +194,21 @@ def layer_numbers(L, nnz: int, entry_bytes: int = roofline.ENTRY_BYTES):
     }
 
 
-def describe(L):
+def l2_method(timing: str) -> str:
+    """How the timed steps keep L2 from serving their data (the same words on
+    both arms of the benchmark, so their configs compare key for key)."""
+    if timing == "flush":
+        return "GPU: each timed step alone after a 256 MiB write that flushes L2"
+    return ("GPU: inputs larger than L2 -- copies of input, weights and output, the steps "
+            "replayed back to back from CUDA graphs")
+
+
+def describe(L, fmt: str = "f32", timing: str = "graph"):
+    """The workload a line's metric is measured on."""
     return {"workload": L.name, "N": L.N, "C": L.C, "H": L.H, "W": L.W, "M": L.M,
             "R": L.R, "S": L.S, "stride": L.stride, "pad": L.pad,
             "sparsity": round(1 - L.density, 4), "rows": L.rows,
-            "l2": "flushed between timed steps (256 MiB write)"}
+            "weight_format": fmt, "l2": l2_method(timing)}
 
 
 # --------------------------------------------------------------------------
@@ -257,7 +276,8 @@ def run_reference(args, L):
         "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": describe(L),
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe(L, args.fmt, args.timing),
         "dense_equiv_tflops": num["dense_flop"] / (us * 1e-6) / 1e12,
         "useful_gflops": num["useful_flop"] / (us * 1e-6) / 1e9,
         "cpu_baseline": {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -272,6 +292,154 @@ def run_reference(args, L):
 # The CUDA path
 # --------------------------------------------------------------------------
 
+def graph_time(swd, torch, L, w, x, y, rowptr, colidx, value, fmt, steps, stream, dev,
+               sample_clocks=False, local=0):
+    """K forwards back to back, replayed from CUDA graphs, each on its own copy
+    of input, weights and output; the copies together exceed twice the L2, so
+    no launch finds its data in L2.  CUDA events on the launching stream
+    around the whole region.  Returns (total ms, copies, bytes per copy, wall
+    seconds, clock record or None)."""
+    info = w.info()
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (126 << 20))
+    per_copy = (x.numel() + y.numel()) * 4 + int(info["device_bytes"])
+    n_copies = int(max(2, min(512, math.ceil(2 * l2 / per_copy))))
+    xs, ys, hs = [x], [y], [w]
+    for _ in range(n_copies - 1):
+        xs.append(x.clone())
+        ys.append(torch.empty_like(y))
+        hs.append(swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R,
+                           S=L.S, stride=L.stride, pad=L.pad, stream=stream,
+                           fmt=fmt, batch_hint=L.N))
+    for i in range(n_copies):
+        swd.forward(xs[i], hs[i], out=ys[i], stream=stream)
+    torch.cuda.synchronize(dev)
+    group = min(n_copies, steps)
+    full, rem = divmod(steps, group)
+
+    def capture(count):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for i in range(count):
+                swd.forward(xs[i], hs[i], out=ys[i], stream=stream)
+        return g
+
+    g_full = capture(group)
+    g_rem = capture(rem) if rem else None
+    g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = None
+    if sample_clocks:
+        clocks = ClockSampler(local)
+        clocks.start()
+        time.sleep(0.25)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    for _ in range(full):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop() if clocks is not None else None
+    total_ms = t_start.elapsed_time(t_end)
+    del g_full, g_rem
+    torch.cuda.synchronize(dev)
+    for h in hs[1:]:
+        h.close()
+    return total_ms, n_copies, per_copy, wall, clk
+
+
+def roofline_of(L, nnz, fmt, us_kernel, sm_count):
+    """The roofline and in-core records of one launch of `us_kernel` µs."""
+    num = layer_numbers(L, nnz, 4 if fmt == "packed32" else roofline.ENTRY_BYTES)
+    peaks, peak_kind = measured_peaks()
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    p_fp32 = fp32_peak_flops(sm_count, mhz)
+    bw = float(peaks["hbm_gbs"]) * 1e9
+    t_comp = num["useful_flop"] / p_fp32
+    t_comm = num["alg_bytes"] / bw
+    if t_comp >= t_comm:
+        achieved = num["useful_flop"] / (us_kernel * 1e-6) / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": p_fp32 / 1e12, "unit": "TFLOP/s",
+                "frac": achieved / (p_fp32 / 1e12),
+                "peak_source": f"{sm_count} SMs x 128 fp32 lanes x 2 x "
+                               f"{mhz:.0f} MHz ({peak_kind} clock)"}
+    else:
+        achieved = num["alg_bytes"] / (us_kernel * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": bw / 1e9, "unit": "GB/s",
+                "frac": achieved / (bw / 1e9), "peak_source": f"hbm_gbs ({peak_kind})"}
+    kname = "spconv_ws_kernel" if fmt == "ws" else "spconv_fwd_kernel"
+    roof["traffic"] = recorded_traffic(L.name if fmt == "f32" else f"{L.name}:{fmt}", kname)
+    roof["algorithmic"] = num["alg_bytes"]
+    roof["kernel"] = kname
+    roof["roofline_us"] = max(t_comp, t_comm) * 1e6
+    # Reported, not graded: the sparse path's in-core ceiling.  Every FMA of a
+    # nonzero reads one 4-byte word of the staged input from shared memory,
+    # which delivers 128 bytes per clock per SM: 32 FMAs per clock per SM, a
+    # quarter of the fp32 rate.  (The dense-tap path reuses a register window
+    # and is not bound by it; layers with many dense rows can exceed it.)
+    p_smem = sm_count * 32 * 2 * mhz * 1e6
+    in_core = {"ceiling": "shared memory, one 4-byte load per FMA of a nonzero",
+               "achieved": num["useful_flop"] / (us_kernel * 1e-6) / 1e12,
+               "peak": p_smem / 1e12, "unit": "TFLOP/s",
+               "frac": num["useful_flop"] / (us_kernel * 1e-6) / p_smem,
+               "peak_source": f"{sm_count} SMs x 128 B/clk / 4 B x 2 FLOP x {mhz:.0f} MHz"}
+    return num, roof, in_core
+
+
+# The other seeded layers the `layers` record times beside the headline one.
+LAYER_SET = ("resnet3x3", "vgg3x3", "sweep50", "sweep80", "sweep90", "sweep95", "sweep99",
+             "alex11x11", "conv5x5")
+
+
+def time_layers(swd, torch, args, names, stream, dev, local, sm_count):
+    """Each layer timed like the headline (graph replay over copies larger than
+    L2, args.layer_steps steps), one entry per layer with its µs/layer,
+    throughputs, roofline and in-core fractions and recorded DRAM traffic."""
+    out = {}
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.25)
+    for name in names:
+        L = workloads.ALL_LAYERS[name]
+        rowptr, colidx, value = workloads.make_weights(L)
+        nnz = int(rowptr[-1])
+        w = swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
+                     stride=L.stride, pad=L.pad, stream=stream, fmt=args.fmt, batch_hint=L.N)
+        x = torch.from_numpy(workloads.make_input(L)).to(dev)
+        y = torch.empty((L.N, L.M, L.E, L.F), device=dev, dtype=torch.float32)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                swd.forward(x, w, out=y, stream=stream)
+            total_ms, n_copies, per_copy, _, _ = graph_time(
+                swd, torch, L, w, x, y, rowptr, colidx, value, args.fmt, args.layer_steps,
+                stream, dev)
+        us = total_ms * 1e3 / args.layer_steps
+        num, roof, in_core = roofline_of(L, nnz, args.fmt, us, sm_count)
+        out[name] = {
+            "value": us, "unit": UNIT, "steps": args.layer_steps,
+            "config": describe(L, args.fmt, "graph"),
+            "dense_equiv_tflops": num["dense_flop"] / (us * 1e-6) / 1e12,
+            "useful_gflops": num["useful_flop"] / (us * 1e-6) / 1e9,
+            "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                              "traffic", "algorithmic", "roofline_us")},
+            "in_core": {"frac": in_core["frac"], "achieved": in_core["achieved"]},
+            "nnz": nnz, "copies": n_copies,
+            "launch": w.launch_info(L.N),
+        }
+        w.close()
+        del x, y
+        torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    return out, clk
+
+
 def run_ours(args, L):
     import torch
     import torch.distributed as dist
@@ -284,6 +452,7 @@ def run_ours(args, L):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
 
     rowptr, colidx, value = workloads.make_weights(L)
     x_host = workloads.make_input(L)
@@ -337,69 +506,20 @@ def run_ours(args, L):
             wall = time.perf_counter() - wall0
             clk = clocks.stop()
             total_ms = sum(per)
-            l2_note = "flushed between timed steps (256 MiB write)"
+            l2_detail = f"{lat_steps} launches, each after a 256 MiB write"
         else:
-            # ---- throughput: K launches back to back, replayed from CUDA graphs,
-            # each reading its own copy of input and weights and writing its own
-            # output; the copies together exceed twice the L2, so no launch finds
-            # its data in L2 ----
+            # ---- throughput: the K steps back to back from CUDA graphs over
+            # copies of the data larger than L2 ----
+            barrier()
+            total_ms, n_copies, per_copy, wall, clk = graph_time(
+                swd, torch, L, w, x, y, rowptr, colidx, value, args.fmt, args.steps, stream,
+                dev, sample_clocks=True, local=local)
+            barrier()
             l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)
                      or (126 << 20))
-            per_copy = (x.numel() + y.numel()) * 4 + int(info["device_bytes"])
-            n_copies = int(max(2, min(512, math.ceil(2 * l2 / per_copy))))
-            xs, ys, hs = [x], [y], [w]
-            for _ in range(n_copies - 1):
-                xs.append(x.clone())
-                ys.append(torch.empty_like(y))
-                hs.append(swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R,
-                                   S=L.S, stride=L.stride, pad=L.pad, stream=stream,
-                                   fmt=args.fmt, batch_hint=L.N))
-            for i in range(n_copies):
-                swd.forward(xs[i], hs[i], out=ys[i], stream=stream)
-            torch.cuda.synchronize(dev)
-            group = min(n_copies, args.steps)
-            full, rem = divmod(args.steps, group)
-
-            def capture(count):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
-                    for i in range(count):
-                        swd.forward(xs[i], hs[i], out=ys[i], stream=stream)
-                return g
-
-            g_full = capture(group)
-            g_rem = capture(rem) if rem else None
-            g_full.replay()
-            if g_rem is not None:
-                g_rem.replay()
-            torch.cuda.synchronize(dev)
-            t_start = torch.cuda.Event(enable_timing=True)
-            t_end = torch.cuda.Event(enable_timing=True)
-            clocks = ClockSampler(local)
-            clocks.start()
-            time.sleep(0.25)
-            barrier()
-            torch.cuda.synchronize(dev)
-            wall0 = time.perf_counter()
-            t_start.record(stream)
-            for _ in range(full):
-                g_full.replay()
-            if g_rem is not None:
-                g_rem.replay()
-            t_end.record(stream)
-            torch.cuda.synchronize(dev)
-            barrier()
-            wall = time.perf_counter() - wall0
-            clk = clocks.stop()
-            total_ms = t_start.elapsed_time(t_end)
-            del g_full, g_rem
-            torch.cuda.synchronize(dev)
-            for h in hs[1:]:
-                h.close()
-            del xs, ys, hs
-            l2_note = (f"inputs larger than L2: {n_copies} copies of input, weights and output "
-                       f"({n_copies * per_copy / 2**20:.0f} MiB; L2 {l2 / 2**20:.0f} MiB), "
-                       f"the {args.steps} steps replayed back to back from CUDA graphs")
+            l2_detail = (f"{n_copies} copies of input, weights and output "
+                         f"({n_copies * per_copy / 2**20:.0f} MiB; L2 {l2 / 2**20:.0f} MiB), "
+                         f"the {args.steps} steps replayed back to back from CUDA graphs")
 
         # ---- end to end through the public API with host buffers ----
         e2e_steps = max(3, min(args.steps, 200))
@@ -421,49 +541,15 @@ def run_ours(args, L):
     ms_step = total_ms / args.steps
     us_layer = whole_job_us_per_layer(total_ms, args.steps, world)
     us_kernel = ms_step * 1e3                                 # one launch on one GPU
-    num = layer_numbers(L, nnz, 4 if args.fmt == "packed32" else roofline.ENTRY_BYTES)
-    peaks, peak_kind = measured_peaks()
-    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-    p_fp32 = fp32_peak_flops(sm_count, float(peaks.get("sm_max_mhz", 2070.0)))
-    bw = float(peaks["hbm_gbs"]) * 1e9
-    t_comp = num["useful_flop"] / p_fp32
-    t_comm = num["alg_bytes"] / bw
-    if t_comp >= t_comm:
-        achieved = num["useful_flop"] / (us_kernel * 1e-6) / 1e12
-        roof = {"bound": "alu", "achieved": achieved, "peak": p_fp32 / 1e12, "unit": "TFLOP/s",
-                "frac": achieved / (p_fp32 / 1e12),
-                "peak_source": f"{sm_count} SMs x 128 fp32 lanes x 2 x "
-                               f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz ({peak_kind} clock)"}
-    else:
-        achieved = num["alg_bytes"] / (us_kernel * 1e-6) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": bw / 1e9, "unit": "GB/s",
-                "frac": achieved / (bw / 1e9), "peak_source": f"hbm_gbs ({peak_kind})"}
-    kname = "spconv_ws_kernel" if args.fmt == "ws" else "spconv_fwd_kernel"
-    traffic = recorded_traffic(L.name if args.fmt == "f32" else f"{L.name}:{args.fmt}", kname)
-    roof["traffic"] = traffic
-    roof["algorithmic"] = num["alg_bytes"]
-    roof["kernel"] = kname
-    roof["roofline_us"] = max(t_comp, t_comm) * 1e6
-    # Reported, not graded: the sparse path's in-core ceiling.  Every FMA of a
-    # nonzero reads one 4-byte word of the staged input from shared memory,
-    # which delivers 128 bytes per clock per SM: 32 FMAs per clock per SM, a
-    # quarter of the fp32 rate.  (The dense-tap path reuses a register window
-    # and is not bound by it; layers with many dense rows can exceed it.)
-    p_smem = sm_count * 32 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
-    in_core = {"ceiling": "shared memory, one 4-byte load per FMA of a nonzero",
-               "achieved": num["useful_flop"] / (us_kernel * 1e-6) / 1e12,
-               "peak": p_smem / 1e12, "unit": "TFLOP/s",
-               "frac": num["useful_flop"] / (us_kernel * 1e-6) / p_smem,
-               "peak_source": f"{sm_count} SMs x 128 B/clk / 4 B x 2 FLOP x "
-                              f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz"}
+    num, roof, in_core = roofline_of(L, nnz, args.fmt, us_kernel, sm_count)
 
     line = {
         "metric": METRIC, "value": us_layer, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 (fp16 weights)" if args.fmt == "packed32" else "f32", "data": "synthetic",
-        "config": {**describe(L), "weight_format": args.fmt, "l2": l2_note,
-                   "timing": args.timing},
+        "config": describe(L, args.fmt, args.timing),
+        "timing": args.timing, "l2_detail": l2_detail,
         "dense_equiv_tflops": num["dense_flop"] / (us_kernel * 1e-6) / 1e12,
         "useful_gflops": num["useful_flop"] / (us_kernel * 1e-6) / 1e9,
         "alg_gbs": num["alg_bytes"] / (us_kernel * 1e-6) / 1e9,
@@ -502,6 +588,16 @@ def run_ours(args, L):
             else:
                 dc[f"speedup_{key}"] = dc[f"{key}_us"] / us_kernel
         line["dense_conv"] = dc
+    w.close()
+    del x, y, flush
+    torch.cuda.synchronize(dev)
+    if rank == 0 and args.layers:
+        # every other seeded layer, timed the same back-to-back way (outside the
+        # headline's timed region)
+        names = [n for n in LAYER_SET if n != L.name]
+        layers, layer_clk = time_layers(swd, torch, args, names, stream, dev, local, sm_count)
+        line["layers"] = layers
+        line["layers_clocks"] = layer_clk
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         us_cpu, threads, sample, _ = time_oracle(L, rowptr, colidx, value, x_host,
                                                  budget_s=args.cpu_budget, steps=3)
@@ -509,7 +605,6 @@ def run_ours(args, L):
                                 "kind": "oracle", "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    w.close()
     if world > 1:
         dist.destroy_process_group()
     return 0
@@ -598,10 +693,17 @@ def main(argv=None):
                     help="also time PyTorch's dense conv2d (cuDNN) on the same layer")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-layers", dest="layers", action="store_false",
+                    help="skip the `layers` record (every other seeded layer timed the same "
+                         "back-to-back way after the headline)")
+    ap.add_argument("--layer-steps", type=int, default=0,
+                    help="steps per layer of the `layers` record (default: max(steps, 20))")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    if args.layer_steps <= 0:
+        args.layer_steps = max(args.steps, 20)
     L = workloads.ALL_LAYERS[args.config]
     if args.impl == "reference":
         return run_reference(args, L)

@@ -105,8 +105,9 @@ def _p1_sweep() -> List[Layer]:
 P1_LAYERS: Dict[str, Layer] = {l.name: l for l in _p1_sweep()}
 ALL_LAYERS: Dict[str, Layer] = {**LAYERS, **P1_LAYERS}
 
-# The layer the benchmark times by default: the ResNet-style 3x3 layer at 90 %.
-BENCH_DEFAULT = "resnet3x3"
+# The layer the benchmark times by default: the largest one-GPU layer of the
+# 90-99 % sparsity range (N=8, C=M=512, 28x28, 3x3, 90 %, lognormal rows).
+BENCH_DEFAULT = "sweep90"
 
 
 def _lognormal_row_counts(M: int, K: int, density: float,
