@@ -182,6 +182,41 @@ int spconv_forward_host(int N, int C, int H, int W, int M, int R, int S, int str
                         int act, float *output_host, float *dev_input, float *dev_output,
                         void *stream);
 
+/* Bytes of device memory behind spconv_forward_host_noalloc's workspaces. */
+#define SPCONV_NOALLOC_MAX_BYTES (32u << 20)
+
+/*
+ * spconv_forward_host_noalloc -- spconv_forward_host without the two device
+ * workspace arguments, for callers that must not allocate device memory at
+ * the time they run a layer: a plugin inside a framework whose allocator owns
+ * the GPU's memory, a service whose memory is budgeted up front, or a caller
+ * on a latency-critical path that cannot take cudaMalloc's implicit
+ * synchronisation.  (No counterpart in the papers: this is an interface
+ * convenience.)  The call allocates nothing -- no cudaMalloc, cudaFree or
+ * allocating library routine; the packed weights come from an earlier
+ * spconv_pack, which does allocate, once, at set-up.
+ *
+ * The workspaces are one statically declared device array of
+ * SPCONV_NOALLOC_MAX_BYTES (32 MiB), which every GPU that loads this code
+ * holds until the process exits: the staged input (N*C*H*W floats) at its
+ * start and, 256-byte aligned after it, the staged output (N*M*E*F floats;
+ * used only when Y exceeds 1 MiB or the host buffers are not mapped).
+ *   Arguments, work enqueued, asynchrony and errors: as spconv_forward_host.
+ *   Also UNSUPPORTED when the two workspaces do not fit in the array
+ *   (rounding the input to 256 bytes), INVALID_ARG for a non-positive shape
+ *   argument, and CUDA when the array's address cannot be looked up.
+ *   Set-up: the first call on each device (with that device current) looks up
+ *   the array's device address with cudaGetSymbolAddress; make that first call
+ *   before any stream capture.
+ *   Sharing: every call on a device uses the same array, and it keeps the last
+ *   call's contents (each call overwrites all it reads).  Calls whose work
+ *   overlaps on the GPU -- on different streams, or from different threads --
+ *   race on the array: order them on one stream or by events.
+ */
+int spconv_forward_host_noalloc(int N, int C, int H, int W, int M, int R, int S, int stride,
+                                int pad, const float *input_host, const spconv_packed *packed,
+                                const float *bias, int act, float *output_host, void *stream);
+
 /* Frees the handle and its device buffers.  NULL-safe.  The caller must make
  * sure no forward that uses the handle is still running. */
 void spconv_packed_free(spconv_packed *p);

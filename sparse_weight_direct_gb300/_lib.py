@@ -24,7 +24,7 @@ SPCONV_ERR_DEVICE = -7
 
 # Every symbol include/spconv.h declares.
 EXPORTS = ("spconv_pack", "spconv_pack_ex", "spconv_forward", "spconv_forward_ex",
-           "spconv_forward_host", "spconv_packed_free",
+           "spconv_forward_host", "spconv_forward_host_noalloc", "spconv_packed_free",
            "spconv_status_string",
            "spconv_pack_host", "spconv_device_status", "spconv_selftest_wait",
            "spconv_packed_info_get", "spconv_launch_info_get", "spconv_packed_copy_array")
@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.spconv_forward_ex.restype = i
         L.spconv_forward_host.argtypes = [i] * 9 + [p, p, p, i, p, p, p, p]
         L.spconv_forward_host.restype = i
+        L.spconv_forward_host_noalloc.argtypes = [i] * 9 + [p, p, p, i, p, p]
+        L.spconv_forward_host_noalloc.restype = i
         L.spconv_packed_free.argtypes = [p]
         L.spconv_packed_free.restype = None
         L.spconv_status_string.argtypes = [i]
