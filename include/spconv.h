@@ -243,7 +243,9 @@ int spconv_pack_host(int C, int H, int W, int M, int R, int S, int stride, int p
  * writing its outputs; 2 = after such a timeout, the wait for the block's
  * copies still in flight ran out as well, so an asynchronous copy may have
  * landed in shared memory after the block left: treat the CUDA context as
- * suspect and reset it before further use).  Errors: INVALID_ARG (NULL or
+ * suspect and reset it before further use; 4 = only in the bounds-checked
+ * build libspconv_debug.so: an access failed its bounds check and was
+ * skipped, so the outputs are not valid).  Errors: INVALID_ARG (NULL or
  * host-only handle), CUDA.
  */
 int spconv_device_status(const spconv_packed *p, void *stream, int32_t *flags);

@@ -83,7 +83,9 @@ class PackedWeights:
         """Synchronise the stream and read/clear the device error flags
         (0 = clean; bit 0 = a pipeline wait of the forward kernel timed out;
         bit 1 = the wait for the block's copies in flight after that timeout
-        ran out too: the context is then suspect and should be reset)."""
+        ran out too: the context is then suspect and should be reset;
+        bit 2 = bounds-checked build only: an access failed its check and was
+        skipped)."""
         flags = ctypes.c_int32(0)
         rc = _lib.lib().spconv_device_status(self.handle, _stream_ptr(stream), ctypes.byref(flags))
         if rc not in (_lib.SPCONV_OK, _lib.SPCONV_ERR_DEVICE):

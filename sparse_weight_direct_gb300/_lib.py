@@ -11,7 +11,9 @@ import os
 import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libspconv.so")
+# SPCONV_LIBRARY selects another build of the same library (the bounds-checked
+# libspconv_debug.so); the default is the in-tree libspconv.so.
+LIB_PATH = os.environ.get("SPCONV_LIBRARY") or os.path.join(HERE, "libspconv.so")
 
 SPCONV_OK = 0
 SPCONV_ERR_INVALID_ARG = -1

@@ -4,6 +4,12 @@ The translation units (the kernel instances, one per output-channels-per-warp
 count, the launcher and the host library) compile in parallel and link against
 the shared CUDA runtime, so the library and PyTorch share one runtime and one
 primary context.
+
+build(debug=True) builds the bounds-checked variant, libspconv_debug.so (the
+same sources with -DSPCONV_DEBUG=1, objects in _build_debug/): every kernel
+access is checked against its extent first and a failed check sets bit 2 of
+the device error word instead of touching memory.  Point the Python binding
+at it with SPCONV_LIBRARY=<path>.
 """
 from __future__ import annotations
 
@@ -17,6 +23,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspconv.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libspconv_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["spconv_fwd.cu", "spconv_fwd_q1.cu", "spconv_fwd_q2.cu", "spconv_fwd_q4.cu",
            "spconv_fwd_q8.cu", "spconv_fwd_pairs.cu", "spconv_fwd_plane.cu", "spconv_fwd_cols.cu",
@@ -46,15 +54,18 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    bdir, lib_path = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     common = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-I", os.path.join(ROOT, "include"),
               "-Xcompiler", "-fPIC,-fvisibility=hidden,-O3,-Wall", *extra_flags]
+    if debug:
+        common.append("-DSPCONV_DEBUG=1")
     objs, procs = [], []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(bdir, src + ".o")
         objs.append(obj)
         if force or _stale(obj, [path, *HEADERS]):
             cmd = [nvcc, *common, "-c", path, "-o", obj]
@@ -68,17 +79,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             sys.stderr.write(out)
         if p.returncode:
             raise RuntimeError("nvcc failed: " + " ".join(cmd))
-    if force or procs or _stale(LIB, objs):
+    if force or procs or _stale(lib_path, objs):
         rpath = os.path.join(cuda_home(), "lib64")
-        cmd = [nvcc, "-shared", *ARCH, "-o", LIB + ".tmp", *objs, "-cudart", "shared",
+        cmd = [nvcc, "-shared", *ARCH, "-o", lib_path + ".tmp", *objs, "-cudart", "shared",
                "-Xlinker", "-rpath," + rpath]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link failed: " + " ".join(cmd))
-        os.replace(LIB + ".tmp", LIB)
-    return LIB
+        os.replace(lib_path + ".tmp", lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -171,6 +171,9 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
     p.pairs = (g.stride == 1 && g.W % 2 == 0 && g.row_pitch % 2 == 0 && g.plane % 2 == 0) ? 1 : 0;
     p.recv_off = (int)stages_bytes(g, split);
     p.plane_stage = g.plane_stage;
+    p.num_slots = g.num_slots;
+    p.smem_bytes = (int)smem;
+    p.blob_bytes = d.blob_bytes;
     CUtensorMap dummy;
     if (!tmap) {
         for (int i = 0; i < 16; ++i) dummy.opaque[i] = 0;

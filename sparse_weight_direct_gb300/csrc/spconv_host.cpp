@@ -897,6 +897,7 @@ int upload(spconv_packed *P, cudaStream_t stream) {
     P->d.slot_next = reinterpret_cast<const int *>(base + b_blobs + b_off + b_slot);
     P->d.group_flags = reinterpret_cast<const int *>(base + b_blobs + b_off + b_slot + b_next);
     P->d.err = reinterpret_cast<unsigned int *>(base + b_blobs + b_off + b_slot + b_next + b_gd);
+    P->d.blob_bytes = (int64_t)P->blobs.size();
     return SPCONV_OK;
 }
 

@@ -106,7 +106,9 @@ struct DeviceArrays {
     const int *slot_next;        // [num_slots]: next part (group-local slot) or -1
     const int *group_flags;      // [groups]: bit 0 dense-tap blobs, bit 1 split rows
     unsigned int *err;           // device error flags (bit 0: pipeline wait timed out;
-                                 // bit 1: the drain of in-flight copies timed out too)
+                                 // bit 1: the drain of in-flight copies timed out too;
+                                 // bit 2: a check of the bounds-checked build failed)
+    int64_t blob_bytes;          // bytes of the blobs array
 };
 
 // Kernel variants compiled for sm_103a.  Returns 0 if (S, stride, P, Q, LR)

@@ -79,7 +79,54 @@ struct KParams {
     int pairs;               // cp.async staging in 8-byte column pairs (stride 1, W even)
     int recv_off;            // byte offset of that receive buffer in shared memory
     int plane_stage;         // raw planes staged by one bulk copy (kModePlane instances)
+    int num_slots;           // entries of slot_oc / slot_next (bounds-checked build)
+    int smem_bytes;          // dynamic shared memory of the launch (bounds-checked build)
+    int64_t blob_bytes;      // bytes of the blobs array (bounds-checked build)
 };
+
+// ---------------------------------------------------------------- bounds-checked build
+//
+// Compiled with -DSPCONV_DEBUG=1 (libspconv_debug.so; the stand-in for a
+// memory checker), every read of a staged input tile, every weight-blob range,
+// shared-memory scratch index, distributed-shared-memory slot and global index
+// of the kernels is checked against its extent before the access.  An access
+// that would leave its extent is skipped (a read gives 0), and bit 2 of the
+// device error word is set; the kernel never traps.  The default build
+// compiles every check away.
+constexpr unsigned int kErrBounds = 4u;
+#ifdef SPCONV_DEBUG
+constexpr bool kDebug = true;
+#else
+constexpr bool kDebug = false;
+#endif
+
+// [lo, hi) of the staged input of the current stage, and the error word.
+struct Span {
+    const float *lo, *hi;
+    unsigned int *err;
+};
+
+// true if `in_range`; otherwise (bounds-checked build) records the failure.
+static __device__ __forceinline__ bool dbg_ok(bool in_range, unsigned int *err) {
+    if constexpr (kDebug) {
+        if (!in_range) {
+            atomicOr(err, kErrBounds);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Shared-memory read of a staged input word.
+static __device__ __forceinline__ float sld(const Span &sp, const float *ptr) {
+    if constexpr (kDebug) {
+        if (ptr < sp.lo || ptr >= sp.hi) {
+            atomicOr(sp.err, kErrBounds);
+            return 0.f;
+        }
+    }
+    return *ptr;
+}
 
 // ---------------------------------------------------------------- PTX helpers
 
@@ -196,7 +243,10 @@ static __device__ __forceinline__ void stage_input_cp_async(const KParams &p, fl
         const int phys = (st == 1) ? col + p.shift : (col % st) * p.phase_pitch + col / st;
         float *dst = buf + row * p.row_pitch + phys;
         for (int cl = 0; cl < cc; ++cl) {
-            cp_async_4(dst, src, ok);
+            if (dbg_ok(dst - buf + 1 <= p.in_stage_bytes / 4 &&
+                           (!ok || (src >= p.x && src < p.x + (size_t)p.N * p.C * hw)),
+                       p.err))
+                cp_async_4(dst, src, ok);
             dst += p.plane;
             src += src_step;
         }
@@ -243,7 +293,10 @@ static __device__ __forceinline__ void stage_input_cp_async_pairs(const KParams 
             const size_t step = ok ? hw : 0;
             float *d = dst + jj;
             for (int cl = 0; cl < cc; ++cl) {
-                cp_async_4(d, src, ok);
+                if (dbg_ok(d - buf + 1 <= p.in_stage_bytes / 4 &&
+                               (!ok || (src >= p.x && src < p.x + (size_t)p.N * p.C * hw)),
+                           p.err))
+                    cp_async_4(d, src, ok);
                 d += p.plane;
                 src += step;
             }
@@ -254,7 +307,11 @@ static __device__ __forceinline__ void stage_input_cp_async_pairs(const KParams 
             const size_t step = bytes ? hw : 0;
             float *d = dst + j;
             for (int cl = 0; cl < cc; ++cl) {
-                cp_async_8(d, src, bytes);
+                if (dbg_ok(d - buf + 2 <= p.in_stage_bytes / 4 &&
+                               (bytes == 0 ||
+                                (src >= p.x && src + bytes / 4 <= p.x + (size_t)p.N * p.C * hw)),
+                           p.err))
+                    cp_async_8(d, src, bytes);
                 d += p.plane;
                 src += step;
             }
@@ -270,6 +327,17 @@ static __device__ __forceinline__ void stage_input_cp_async_pairs(const KParams 
 
 // ---------------------------------------------------------------- compute
 
+// Reads of the per-slot arrays (bounds-checked build: an index past
+// num_slots reads as -1, "no channel / no next part").
+static __device__ __forceinline__ int slot_oc_at(const KParams &p, int i) {
+    if (!dbg_ok((unsigned)i < (unsigned)p.num_slots, p.err)) return -1;
+    return p.slot_oc[i];
+}
+static __device__ __forceinline__ int slot_next_at(const KParams &p, int i) {
+    if (!dbg_ok((unsigned)i < (unsigned)p.num_slots, p.err)) return -1;
+    return p.slot_next[i];
+}
+
 // Fused epilogue: bias, then the activation.
 static __device__ __forceinline__ float finish(const KParams &p, int m, float v) {
     if (p.bias) v += __ldg(p.bias + m);
@@ -283,32 +351,32 @@ constexpr bool kDenseTaps = ST_CT == 1 && (S_CT == 3 || S_CT == 5);
 
 template <int P, int ROW_STEP>
 static __device__ __forceinline__ void apply_entry(float (&acc)[P], const float *sb, float v, int off,
-                                            int row_step) {
+                                            int row_step, const Span &sp) {
     const float *s = sb + off;
 #pragma unroll
     for (int r = 0; r < P; ++r)
-        acc[r] = fmaf(v, s[r * (ROW_STEP ? ROW_STEP : row_step)], acc[r]);
+        acc[r] = fmaf(v, sld(sp, s + r * (ROW_STEP ? ROW_STEP : row_step)), acc[r]);
 }
 
 // UNROLL: iterations (two entries each) unrolled; more shared loads in flight
 // per lane, where the registers allow it.
 template <int P, int ROW_STEP, int UNROLL>
 static __device__ __forceinline__ void run_segment(float (&acc)[P], const float *sb, const float2 *ent,
-                                            int j, int j1, int row_step) {
+                                            int j, int j1, int row_step, const Span &sp) {
     if ((j & 1) && j < j1) {  // head: bring j to a 16-byte boundary
         const float2 e = ent[j];
-        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
+        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step, sp);
         ++j;
     }
 #pragma unroll UNROLL
     for (; j + 1 < j1; j += 2) {
         const float4 e = *reinterpret_cast<const float4 *>(ent + j);
-        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
-        apply_entry<P, ROW_STEP>(acc, sb, e.z, __float_as_int(e.w), row_step);
+        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step, sp);
+        apply_entry<P, ROW_STEP>(acc, sb, e.z, __float_as_int(e.w), row_step, sp);
     }
     if (j < j1) {  // tail
         const float2 e = ent[j];
-        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step);
+        apply_entry<P, ROW_STEP>(acc, sb, e.x, __float_as_int(e.y), row_step, sp);
     }
 }
 
@@ -326,7 +394,7 @@ static __device__ __forceinline__ void run_segment(float (&acc)[P], const float 
 template <int P, int RS>
 static __device__ __forceinline__ void apply_entry_plane(float (&acc)[P], const float *sb, float v,
                                                          uint32_t code, int row_step,
-                                                         uint32_t lanebits) {
+                                                         uint32_t lanebits, const Span &sp) {
     const float *s = sb + (code >> 4);
     const uint32_t hit = code & lanebits;
     const float wc = (hit & 3u) ? 0.f : v;
@@ -334,27 +402,29 @@ static __device__ __forceinline__ void apply_entry_plane(float (&acc)[P], const 
     const float wl = (hit & 8u) ? 0.f : wc;
 #pragma unroll
     for (int r = 0; r < P; ++r)
-        acc[r] = fmaf(r == 0 ? w0 : (r == P - 1 ? wl : wc), s[r * (RS ? RS : row_step)], acc[r]);
+        acc[r] = fmaf(r == 0 ? w0 : (r == P - 1 ? wl : wc), sld(sp, s + r * (RS ? RS : row_step)),
+                      acc[r]);
 }
 
 template <int P, int RS, int UNROLL>
 static __device__ __forceinline__ void run_segment_plane(float (&acc)[P], const float *sb,
                                                          const float2 *ent, int j, int j1,
-                                                         int row_step, uint32_t lanebits) {
+                                                         int row_step, uint32_t lanebits,
+                                                         const Span &sp) {
     if ((j & 1) && j < j1) {  // head: bring j to a 16-byte boundary
         const float2 e = ent[j];
-        apply_entry_plane<P, RS>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
+        apply_entry_plane<P, RS>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits, sp);
         ++j;
     }
 #pragma unroll UNROLL
     for (; j + 1 < j1; j += 2) {
         const float4 e = *reinterpret_cast<const float4 *>(ent + j);
-        apply_entry_plane<P, RS>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
-        apply_entry_plane<P, RS>(acc, sb, e.z, __float_as_uint(e.w), row_step, lanebits);
+        apply_entry_plane<P, RS>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits, sp);
+        apply_entry_plane<P, RS>(acc, sb, e.z, __float_as_uint(e.w), row_step, lanebits, sp);
     }
     if (j < j1) {  // tail
         const float2 e = ent[j];
-        apply_entry_plane<P, RS>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits);
+        apply_entry_plane<P, RS>(acc, sb, e.x, __float_as_uint(e.y), row_step, lanebits, sp);
     }
 }
 
@@ -362,11 +432,12 @@ static __device__ __forceinline__ void run_segment_plane(float (&acc)[P], const 
 // inputs are loaded once and feed both channels' accumulators.
 template <int P, int ROW_STEP>
 static __device__ __forceinline__ void apply_pair(float (&a)[P], float (&b)[P], const float *sb,
-                                                  float va, float vb, int off, int row_step) {
+                                                  float va, float vb, int off, int row_step,
+                                                  const Span &sp) {
     const float *s = sb + off;
 #pragma unroll
     for (int r = 0; r < P; ++r) {
-        const float x = s[r * (ROW_STEP ? ROW_STEP : row_step)];
+        const float x = sld(sp, s + r * (ROW_STEP ? ROW_STEP : row_step));
         a[r] = fmaf(va, x, a[r]);
         b[r] = fmaf(vb, x, b[r]);
     }
@@ -378,18 +449,20 @@ static __device__ __forceinline__ void apply_pair(float (&a)[P], float (&b)[P], 
 template <int P, int Q, int ROW_STEP>
 static __device__ __forceinline__ void run_pairs(float (&acc)[Q][P], const float *sb,
                                                  const uint32_t *hp, const float4 *ent4,
-                                                 int row_step) {
+                                                 int row_step, const Span &sp, int ent4_cap) {
 #pragma unroll
     for (int q1 = 0; q1 < Q; ++q1)
 #pragma unroll
         for (int q2 = q1 + 1; q2 < Q; ++q2) {
             const int k = q1 * Q - q1 * (q1 + 1) / 2 + (q2 - q1 - 1);
             const int j1 = (int)(hp[k + 1] >> 1);
+            int j = (int)(hp[k] >> 1);
+            if (!dbg_ok(0 <= j && j <= j1 && j1 <= ent4_cap, sp.err)) continue;
 #pragma unroll 2
-            for (int j = (int)(hp[k] >> 1); j < j1; ++j) {
+            for (; j < j1; ++j) {
                 const float4 e = ent4[j];
                 apply_pair<P, ROW_STEP>(acc[q1], acc[q2], sb, e.x, e.y, __float_as_int(e.z),
-                                        row_step);
+                                        row_step, sp);
             }
         }
 }
@@ -405,7 +478,8 @@ static __device__ __forceinline__ void run_pairs(float (&acc)[Q][P], const float
 template <int P, int Q, int K, int LR, int RP>
 static __device__ __forceinline__ void run_dense_chunk(float (&acc)[Q][P], const float *sb,
                                                 const uint32_t *dmask, const float4 *dw,
-                                                int warp, int chunk, int cc, int plane) {
+                                                int warp, int chunk, int cc, int plane,
+                                                const Span &sp, const void *blob_end) {
     constexpr int WR = LR * (P - 1) + K;  // window rows
     constexpr int KK4 = (K * K + 3) / 4;  // float4 per weight block
     for (int cl = 0; cl < cc; ++cl) {
@@ -416,11 +490,12 @@ static __device__ __forceinline__ void run_dense_chunk(float (&acc)[Q][P], const
 #pragma unroll
         for (int i = 0; i < WR; ++i)
 #pragma unroll
-            for (int j = 0; j < K; ++j) win[i][j] = s[i * RP + j];
+            for (int j = 0; j < K; ++j) win[i][j] = sld(sp, s + i * RP + j);
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
             if (!(mask & (1u << q))) continue;
             const float4 *wq = dw + ((size_t)(warp * chunk + cl) * Q + q) * KK4;
+            if (!dbg_ok((const void *)(wq + KK4) <= blob_end, sp.err)) continue;
             float w[KK4 * 4];
 #pragma unroll
             for (int t = 0; t < KK4; ++t) {
@@ -447,28 +522,28 @@ static __device__ __forceinline__ void run_dense_chunk(float (&acc)[Q][P], const
 // rebuilt from (channel, py, px) per entry.
 template <int P, int ROW_STEP, int ST_CT>
 static __device__ __forceinline__ void apply_word(float (&acc)[P], const float *sb, uint32_t w,
-                                           const KParams &p, int row_step) {
+                                           const KParams &p, int row_step, const Span &sp) {
     const float v = __half2float(__ushort_as_half((unsigned short)(w >> 16)));
     const int cl = (int)((w >> 8) & 0xffu), px = (int)((w >> 4) & 0xfu), py = (int)(w & 0xfu);
     const int st = ST_CT ? ST_CT : p.stride;
     const int col = (st == 1) ? px + p.shift : (px % st) * p.phase_pitch + px / st;
-    apply_entry<P, ROW_STEP>(acc, sb, v, cl * p.plane + py * p.row_pitch + col, row_step);
+    apply_entry<P, ROW_STEP>(acc, sb, v, cl * p.plane + py * p.row_pitch + col, row_step, sp);
 }
 
 template <int P, int ROW_STEP, int ST_CT>
 static __device__ __forceinline__ void run_segment_words(float (&acc)[P], const float *sb,
                                                   const uint32_t *ent, int j, int j1,
-                                                  const KParams &p, int row_step) {
+                                                  const KParams &p, int row_step, const Span &sp) {
     for (; (j & 3) && j < j1; ++j)  // head: bring j to a 16-byte boundary
-        apply_word<P, ROW_STEP, ST_CT>(acc, sb, ent[j], p, row_step);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, ent[j], p, row_step, sp);
     for (; j + 3 < j1; j += 4) {
         const uint4 e = *reinterpret_cast<const uint4 *>(ent + j);
-        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.x, p, row_step);
-        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.y, p, row_step);
-        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.z, p, row_step);
-        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.w, p, row_step);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.x, p, row_step, sp);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.y, p, row_step, sp);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.z, p, row_step, sp);
+        apply_word<P, ROW_STEP, ST_CT>(acc, sb, e.w, p, row_step, sp);
     }
-    for (; j < j1; ++j) apply_word<P, ROW_STEP, ST_CT>(acc, sb, ent[j], p, row_step);  // tail
+    for (; j < j1; ++j) apply_word<P, ROW_STEP, ST_CT>(acc, sb, ent[j], p, row_step, sp);  // tail
 }
 
 // P: output rows per lane; Q: output channels per warp; LR: lane rows (1, or 2
@@ -565,11 +640,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     // their latency overlaps the pipeline: the group's flags, the first
     // blobs' offsets (issuing thread) and the output channel (+ chain link)
     // of this warp's first output item.
-    const int gflags = p.group_flags[group];
+    const int gflags =
+        dbg_ok(group < p.groups, p.err) ? p.group_flags[group] : 0;
     const bool dense = (gflags & 1) != 0;
     const bool has_parts = (gflags & 2) != 0;
     uint32_t pre_off[3] = {0u, 0u, 0u};
-    if (threadIdx.x == 0 && nmine > 0 && p.blob_stride16 == 0) {
+    if (threadIdx.x == 0 && nmine > 0 && p.blob_stride16 == 0 &&
+        dbg_ok(group * p.num_chunks + k_end <= p.groups * p.num_chunks, p.err)) {
         const uint32_t *bo = p.blob_off + group * p.num_chunks + k_begin;
         pre_off[0] = bo[0];
         pre_off[1] = bo[1];
@@ -581,8 +658,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         split == 1 ? true : warp < ((kr + 1) * nslot / split - kr * nslot / split) * P;
     int pre_m = -1, pre_next = -1;
     if (item0_valid) {
-        pre_m = p.slot_oc[group * nslot + item0_slot];
-        pre_next = p.slot_next[group * nslot + item0_slot];
+        pre_m = slot_oc_at(p, group * nslot + item0_slot);
+        pre_next = slot_next_at(p, group * nslot + item0_slot);
     }
     // Push-mode cluster reduction: this block announces that it is running;
     // the matching wait comes before its first store into another block.
@@ -594,9 +671,18 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     // stages its share of the input with cp.async.
     // (weights: arm the stage's mbarrier for all its bytes and copy the blob;
     // input: copy the input tile, which completes on the same mbarrier.)
+    // (bounds-checked build: the staged input of a chunk fits its region; a
+    // copy that would not is skipped)
+    auto input_fits = [&](int c0) {
+        const size_t in_bytes =
+            PLANE ? kPlaneLead * sizeof(float) + (size_t)min(p.chunk, p.C - c0) * p.H * p.W * 4u
+                  : (p.use_tma ? (size_t)p.in_tma_bytes : 0u);
+        return !kDebug || in_bytes <= (size_t)p.in_stage_bytes;
+    };
     auto issue = [&](int k, int s, bool issuer, bool weights, bool input) {
         unsigned char *base = smem + (size_t)s * p.stage_bytes;
         const int c0 = k * p.chunk;
+        const bool in_fits = input_fits(c0);
         if (issuer && weights) {
             ++issued[s];  // one writer per stage at a time (the thread that frees it)
             uint32_t o0, blob_bytes;
@@ -610,17 +696,25 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                     i < 2 ? pre_off[i + 1] : p.blob_off[group * p.num_chunks + k + 1];
                 blob_bytes = (o1 - o0) * 16u;
             }
+            if (!dbg_ok(group * p.num_chunks + k < p.groups * p.num_chunks &&
+                            (int64_t)o0 * 16 + blob_bytes <= p.blob_bytes &&
+                            blob_bytes <= (uint32_t)(p.stage_bytes - p.in_stage_bytes),
+                        p.err))
+                blob_bytes = 0;  // (bounds-checked build) the copy is skipped
             asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
             const uint32_t in_bytes =
-                PLANE ? (uint32_t)(min(p.chunk, p.C - c0) * p.H * p.W) * 4u
-                      : (p.use_tma ? (uint32_t)p.in_tma_bytes : 0u);
+                !in_fits ? 0u
+                         : PLANE ? (uint32_t)(min(p.chunk, p.C - c0) * p.H * p.W) * 4u
+                                 : (p.use_tma ? (uint32_t)p.in_tma_bytes : 0u);
+            if (!in_fits) dbg_ok(false, p.err);
             mbar_expect_tx(&bar[s], blob_bytes + in_bytes);
-            bulk_load(base + p.in_stage_bytes, p.blobs + (size_t)o0 * 16u, blob_bytes, &bar[s]);
+            if (!kDebug || blob_bytes > 0)
+                bulk_load(base + p.in_stage_bytes, p.blobs + (size_t)o0 * 16u, blob_bytes, &bar[s]);
         }
         if constexpr (PLANE) {
             // the chunk's planes are contiguous in the input (and start on a
             // 16-byte boundary: H * W is a multiple of 4)
-            if (issuer && input) {
+            if (issuer && input && in_fits) {
                 asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
                 const size_t hw = (size_t)p.H * p.W;
                 bulk_load(base + kPlaneLead * sizeof(float), p.x + ((size_t)n * p.C + c0) * hw,
@@ -628,7 +722,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             }
             return;
         }
-        if (issuer && input && p.use_tma)
+        if (issuer && input && p.use_tma && in_fits)
             tma_load_4d(base, &tmap, ix0 - p.shift, iy0, c0, n, &bar[s]);
         if (input && !p.use_tma) {
             if (ST_CT == 1 && p.pairs)
@@ -685,39 +779,50 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                  (lx < p.W ? ly * p.W + lx : 2 * p.W + ly * (LC - p.W) + (lx - p.W));
         }
         const uint32_t *hdr = reinterpret_cast<const uint32_t *>(base + p.in_stage_bytes);
+        // this stage's staged input and the end of its weight blob
+        const Span sp{reinterpret_cast<const float *>(base),
+                      reinterpret_cast<const float *>(base + p.in_stage_bytes), p.err};
+        const unsigned char *blob_end = base + p.stage_bytes;
         if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4 && !PLANE && !COLS) {
             if (dense) {
                 const int k = k_begin + it;
                 run_dense_chunk<P, Q, S_CT, LR, row_pitch_s1(S_CT, LR)>(
                     acc, sb + p.shift, hdr, reinterpret_cast<const float4 *>(hdr + p.dense_mask_words),
-                    warp, p.chunk, min(p.chunk, p.C - k * p.chunk), p.plane);
+                    warp, p.chunk, min(p.chunk, p.C - k * p.chunk), p.plane, sp, blob_end);
             }
         }
         if (!dense && p.fmt == 0) {
             const float2 *ent = reinterpret_cast<const float2 *>(hdr + p.hdr_words);
+            const int ent_cap = (int)((blob_end - reinterpret_cast<const unsigned char *>(ent)) / 8);
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
                 const int j0 = (int)hdr[warp * Q + q];
                 const int j1 = (int)hdr[warp * Q + q + 1];
+                if (!dbg_ok(0 <= j0 && j0 <= j1 && j1 <= ent_cap, p.err)) continue;
                 if constexpr (PLANE) {
                     const uint32_t lanebits = (lx == 0 ? 1u : 0u) | (lx == p.W - 1 ? 2u : 0u) |
                                               (ly == 0 ? 4u : 0u) | (ly == LR - 1 ? 8u : 0u);
-                    run_segment_plane<P, PLANE_RS, 4>(acc[q], sb, ent, j0, j1, row_step, lanebits);
+                    run_segment_plane<P, PLANE_RS, 4>(acc[q], sb, ent, j0, j1, row_step, lanebits,
+                                                      sp);
                 } else {
                     // Q = 8 instances are at the register cap: no unrolling there
-                    run_segment<P, ROW_STEP, (Q >= 8 ? 1 : 4)>(acc[q], sb, ent, j0, j1, row_step);
+                    run_segment<P, ROW_STEP, (Q >= 8 ? 1 : 4)>(acc[q], sb, ent, j0, j1, row_step,
+                                                               sp);
                 }
             }
             if constexpr (PAIRS)
                 run_pairs<P, Q, ROW_STEP>(acc, sb, hdr + kWarps * Q + 1 + warp * (Q * (Q - 1) / 2),
-                                          reinterpret_cast<const float4 *>(ent), row_step);
+                                          reinterpret_cast<const float4 *>(ent), row_step, sp,
+                                          ent_cap / 2);
         } else if (!dense) {
             const uint32_t *ent = hdr + p.hdr_words;
+            const int ent_cap = (int)((blob_end - reinterpret_cast<const unsigned char *>(ent)) / 4);
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
                 const int j0 = (int)hdr[warp * Q + q];
                 const int j1 = (int)hdr[warp * Q + q + 1];
-                run_segment_words<P, ROW_STEP, ST_CT>(acc[q], sb, ent, j0, j1, p, row_step);
+                if (!dbg_ok(0 <= j0 && j0 <= j1 && j1 <= ent_cap, p.err)) continue;
+                run_segment_words<P, ROW_STEP, ST_CT>(acc[q], sb, ent, j0, j1, p, row_step, sp);
             }
         }
         if (p.use_tma || PLANE) {
@@ -765,6 +870,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     }
 
     const int slot0 = group * nslot + warp * Q;
+    // (bounds-checked build) end of the launch's dynamic shared memory
+    const unsigned char *smem_end = smem_raw + p.smem_bytes;
     // This lane's outputs r = 0 .. P-1: rows oy0 + LR * r of column ox, or
     // (column blocks) columns ox + r of row oy0.
     const int ox = COLS ? tx * (LC * P) + lx * P : tx * LC + lx;
@@ -783,6 +890,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             // 32 scattered ones.
             if (failed) return;
             float *tb = reinterpret_cast<float *>(smem) + (size_t)warp * Q * (P * 32);
+            if (!dbg_ok(reinterpret_cast<const unsigned char *>(tb + Q * P * 32) <= smem_end, p.err))
+                return;
 #pragma unroll
             for (int q = 0; q < Q; ++q)
 #pragma unroll
@@ -790,14 +899,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             __syncwarp();
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
-                const int m = q == 0 ? pre_m : p.slot_oc[slot0 + q];
+                const int m = q == 0 ? pre_m : slot_oc_at(p, slot0 + q);
                 if (m < 0) continue;
                 float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
 #pragma unroll
                 for (int i = 0; i < P; ++i) {
                     const int t = i * 32 + lane;
                     const int oy = ty * LR + t / (LC * P), oxt = tx * (LC * P) + t % (LC * P);
-                    if (oy < p.E && oxt < p.F)
+                    if (oy < p.E && oxt < p.F && dbg_ok(m < p.M, p.err))
                         yo[(size_t)oy * p.F + oxt] = finish(p, m, tb[q * (P * 32) + t]);
                 }
             }
@@ -808,12 +917,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (failed || !lane_out) return;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
-            const int m = q == 0 ? pre_m : p.slot_oc[slot0 + q];
+            const int m = q == 0 ? pre_m : slot_oc_at(p, slot0 + q);
             if (m < 0) continue;
             float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
 #pragma unroll
             for (int r = 0; r < P; ++r)
-                if (out_ok(r)) yo[out_at(r)] = finish(p, m, acc[q][r]);
+                if (out_ok(r) && dbg_ok(m < p.M, p.err)) yo[out_at(r)] = finish(p, m, acc[q][r]);
         }
         return;
     }
@@ -830,14 +939,19 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             // barrier after that because no other block reads it.
             float *recv = reinterpret_cast<float *>(smem + p.recv_off);  // [rank][own][P][32]
             const int own = (nslot + split - 1) / split;  // most slots a rank owns
+            // (bounds-checked build) every rank's buffer ends inside its shared memory
+            const bool recv_ok = dbg_ok(
+                reinterpret_cast<const unsigned char *>(recv + split * own * P * 32) <= smem_end,
+                p.err);
             cg::cluster_group cluster = cg::this_cluster();
             asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");  // all blocks started
-            if (!failed) {
+            if (!failed && recv_ok) {
 #pragma unroll
                 for (int q = 0; q < Q; ++q) {
                     const int sl = warp * Q + q;
                     int o = split - 1;  // owner: the last rank whose range starts at or before sl
                     while (o > 0 && o * nslot / split > sl) --o;
+                    if (!dbg_ok(sl - o * nslot / split < own, p.err)) continue;
                     float *dst = cluster.map_shared_rank(recv, o) +
                                  ((kr * own + (sl - o * nslot / split)) * P) * 32 + lane;
 #pragma unroll
@@ -846,12 +960,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             }
             asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
             asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-            if (failed || !lane_out) return;
+            if (failed || !lane_out || !recv_ok) return;
             const int s_begin = kr * nslot / split, s_end = (kr + 1) * nslot / split;
             const int items = (s_end - s_begin) * P;
             for (int item = warp; item < items; item += kWarps) {
                 const int li = item / P, r = item % P;
-                const int m = item == warp ? pre_m : p.slot_oc[group * nslot + s_begin + li];
+                const int m = item == warp ? pre_m : slot_oc_at(p, group * nslot + s_begin + li);
                 if (m < 0) continue;
                 float v[kMaxSplit];
 #pragma unroll
@@ -861,7 +975,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 #pragma unroll
                 for (int j = 0; j < kMaxSplit; ++j)
                     if (j < split) sum += v[j];
-                if (out_ok(r))
+                if (out_ok(r) && dbg_ok(m < p.M, p.err))
                     p.y[((size_t)n * p.M + m) * p.E * p.F + out_at(r)] = finish(p, m, sum);
             }
             return;
@@ -874,24 +988,29 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     // result is deterministic.  The stage buffers are free: every issued copy
     // has been consumed.
     float *part = reinterpret_cast<float *>(smem);  // [warp * Q + q][P][32]
+    if (!dbg_ok(reinterpret_cast<const unsigned char *>(part + kWarps * Q * P * 32) <= smem_end,
+                p.err))
+        failed = true;  // (bounds-checked build) no room: write nothing
 #pragma unroll
     for (int q = 0; q < Q; ++q)
 #pragma unroll
-        for (int r = 0; r < P; ++r) part[((warp * Q + q) * P + r) * 32 + lane] = acc[q][r];
+        for (int r = 0; r < P; ++r)
+            if (!kDebug || !failed) part[((warp * Q + q) * P + r) * 32 + lane] = acc[q][r];
     if (split == 1) {
         __syncthreads();
         if (failed || !lane_out) return;
         for (int q = 0; q < Q; ++q) {
             const int sl = warp * Q + q;
-            const int m = q == 0 ? pre_m : p.slot_oc[group * nslot + sl];
+            const int m = q == 0 ? pre_m : slot_oc_at(p, group * nslot + sl);
             if (m < 0) continue;
-            const int next0 = q == 0 ? pre_next : p.slot_next[group * nslot + sl];
+            const int next0 = q == 0 ? pre_next : slot_next_at(p, group * nslot + sl);
             float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
             for (int r = 0; r < P; ++r) {
                 float sum = part[(sl * P + r) * 32 + lane];
-                for (int c = next0; c >= 0; c = p.slot_next[group * nslot + c])
+                for (int c = next0; c >= 0 && dbg_ok(c < nslot, p.err);
+                     c = slot_next_at(p, group * nslot + c))
                     sum += part[(c * P + r) * 32 + lane];
-                if (out_ok(r)) yo[out_at(r)] = finish(p, m, sum);
+                if (out_ok(r) && dbg_ok(m < p.M, p.err)) yo[out_at(r)] = finish(p, m, sum);
             }
         }
         return;
@@ -907,11 +1026,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             for (int item = warp; item < items; item += kWarps) {
                 const int sl = s_begin + item / P, r = item % P;
                 const bool first = item == warp;
-                const int m = first ? pre_m : p.slot_oc[group * nslot + sl];
+                const int m = first ? pre_m : slot_oc_at(p, group * nslot + sl);
                 if (m < 0) continue;
                 float sum = 0.f;
-                for (int c = sl, next = first ? pre_next : p.slot_next[group * nslot + sl]; c >= 0;
-                     c = next, next = c >= 0 ? p.slot_next[group * nslot + c] : -1) {
+                for (int c = sl, next = first ? pre_next : slot_next_at(p, group * nslot + sl);
+                     c >= 0 && dbg_ok(c < nslot, p.err);
+                     c = next, next = c >= 0 ? slot_next_at(p, group * nslot + c) : -1) {
                     float v[kMaxSplit];
 #pragma unroll
                     for (int j = 0; j < kMaxSplit; ++j)
@@ -921,7 +1041,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                     for (int j = 0; j < kMaxSplit; ++j)
                         if (j < split) sum += v[j];
                 }
-                if (out_ok(r))
+                if (out_ok(r) && dbg_ok(m < p.M, p.err))
                     p.y[((size_t)n * p.M + m) * p.E * p.F + out_at(r)] = finish(p, m, sum);
             }
         }
@@ -930,15 +1050,16 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         // code; these instances carry the register-heavy dense-tap path)
         if (!failed && lane_out) {
             for (int sl = s_begin + warp; sl < s_end; sl += kWarps) {
-                const int m = p.slot_oc[group * nslot + sl];
+                const int m = slot_oc_at(p, group * nslot + sl);
                 if (m < 0) continue;
                 float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
                 for (int r = 0; r < P; ++r) {
                     float sum = 0.f;
-                    for (int c = sl; c >= 0; c = p.slot_next[group * nslot + c])
+                    for (int c = sl; c >= 0 && dbg_ok(c < nslot, p.err);
+                         c = slot_next_at(p, group * nslot + c))
                         for (int j = 0; j < split; ++j)
                             sum += cluster.map_shared_rank(part, j)[(c * P + r) * 32 + lane];
-                    if (out_ok(r)) yo[out_at(r)] = finish(p, m, sum);
+                    if (out_ok(r) && dbg_ok(m < p.M, p.err)) yo[out_at(r)] = finish(p, m, sum);
                 }
             }
         }

@@ -40,6 +40,7 @@ struct WsParams {
     int C, H, W, M, E, F, R, S, stride, pad;
     int tiles_x;  // spatial tiles along F (grid y = tiles_y * tiles_x)
     int piece;    // entries per pipeline stage (even)
+    int64_t ent_bytes;  // bytes of the entries array (bounds-checked build)
 };
 
 static __device__ __forceinline__ float ws_finish(const WsParams &p, int m, float v) {
@@ -51,8 +52,15 @@ static __device__ __forceinline__ float ws_finish(const WsParams &p, int m, floa
 // One entry applied to this thread's P outputs.  word = off << 8 | r << 4 | s
 // with off = c*H*W + r*W + s; base[i] = iy0_i*W + ix0 of output row i, so
 // base[i] + off indexes input (c, iy0_i + r, ix0 + s) of the image.
+// Read of input element i of the image (bounds-checked build: i inside the
+// image's C*H*W elements, else the read is skipped and gives 0).
+static __device__ __forceinline__ float ws_ld(const WsParams &p, const float *xn, int i) {
+    if (!dbg_ok((unsigned)i < (unsigned)(p.C * p.H * p.W), p.err)) return 0.f;
+    return __ldg(xn + i);
+}
+
 template <int P, bool CHECK>
-static __device__ __forceinline__ void ws_apply(float (&acc)[P], const float *xn,
+static __device__ __forceinline__ void ws_apply(const WsParams &p, float (&acc)[P], const float *xn,
                                                 const int (&base)[P], const uint32_t (&rmask)[P],
                                                 uint32_t cmask, float v, uint32_t word) {
     const int off = (int)(word >> 8);
@@ -61,28 +69,28 @@ static __device__ __forceinline__ void ws_apply(float (&acc)[P], const float *xn
         const uint32_t cv = (cmask >> s) & 1u;
 #pragma unroll
         for (int i = 0; i < P; ++i)
-            if ((rmask[i] >> r) & cv) acc[i] = fmaf(v, __ldg(xn + base[i] + off), acc[i]);
+            if ((rmask[i] >> r) & cv) acc[i] = fmaf(v, ws_ld(p, xn, base[i] + off), acc[i]);
     } else {
 #pragma unroll
-        for (int i = 0; i < P; ++i) acc[i] = fmaf(v, __ldg(xn + base[i] + off), acc[i]);
+        for (int i = 0; i < P; ++i) acc[i] = fmaf(v, ws_ld(p, xn, base[i] + off), acc[i]);
     }
 }
 
 // Entries [0, len) of a staged piece (16-byte aligned, two entries per load).
 template <int P, bool CHECK>
-static __device__ __forceinline__ void ws_run(float (&acc)[P], const float *xn,
+static __device__ __forceinline__ void ws_run(const WsParams &p, float (&acc)[P], const float *xn,
                                               const int (&base)[P], const uint32_t (&rmask)[P],
                                               uint32_t cmask, const float2 *e, int len) {
     int j = 0;
 #pragma unroll 2
     for (; j + 1 < len; j += 2) {
         const float4 q = *reinterpret_cast<const float4 *>(e + j);
-        ws_apply<P, CHECK>(acc, xn, base, rmask, cmask, q.x, __float_as_uint(q.y));
-        ws_apply<P, CHECK>(acc, xn, base, rmask, cmask, q.z, __float_as_uint(q.w));
+        ws_apply<P, CHECK>(p, acc, xn, base, rmask, cmask, q.x, __float_as_uint(q.y));
+        ws_apply<P, CHECK>(p, acc, xn, base, rmask, cmask, q.z, __float_as_uint(q.w));
     }
     if (j < len) {
         const float2 q = e[j];
-        ws_apply<P, CHECK>(acc, xn, base, rmask, cmask, q.x, __float_as_uint(q.y));
+        ws_apply<P, CHECK>(p, acc, xn, base, rmask, cmask, q.x, __float_as_uint(q.y));
     }
 }
 
@@ -98,7 +106,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     constexpr int ROWS = kWarps * LR;        // output rows covered by one step of i
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int ly = lane / LC, lx = lane % LC;
-    const int m = p.row_order[blockIdx.x];
+    const int m0 = dbg_ok(blockIdx.x < (unsigned)p.M, p.err) ? p.row_order[blockIdx.x] : 0;
+    const int m = dbg_ok((unsigned)m0 < (unsigned)p.M, p.err) ? m0 : 0;
     const int tx = blockIdx.y % p.tiles_x, ty = blockIdx.y / p.tiles_x;
     const int n = blockIdx.z;
     const uint32_t first = p.row_info[2 * m], count = p.row_info[2 * m + 1];
@@ -144,11 +153,17 @@ __global__ void __launch_bounds__(kWarps * 32)
     auto issue = [&](int k) {
         const uint32_t j0 = first + (uint32_t)k * (uint32_t)p.piece;
         const uint32_t len = min((uint32_t)p.piece, count - (uint32_t)k * (uint32_t)p.piece);
-        const uint32_t bytes = ((len + 1u) & ~1u) * 8u;
+        uint32_t bytes = ((len + 1u) & ~1u) * 8u;
+        // (bounds-checked build) the piece lies inside the entries and its stage
+        if (!dbg_ok((int64_t)j0 * 8 + bytes <= p.ent_bytes && bytes <= (uint32_t)p.piece * 8u &&
+                        (unsigned)m < (unsigned)p.M,
+                    p.err))
+            bytes = 0;
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         mbar_expect_tx(&bar[k & 1], bytes);
-        bulk_load(ws_smem + (size_t)(k & 1) * p.piece * 8, p.ent + (size_t)j0 * 8, bytes,
-                  &bar[k & 1]);
+        if (!kDebug || bytes > 0)
+            bulk_load(ws_smem + (size_t)(k & 1) * p.piece * 8, p.ent + (size_t)j0 * 8, bytes,
+                      &bar[k & 1]);
     };
     if (threadIdx.x == 0) {
         if (npieces > 0) issue(0);
@@ -167,9 +182,9 @@ __global__ void __launch_bounds__(kWarps * 32)
         const float2 *e = reinterpret_cast<const float2 *>(ws_smem + (size_t)(k & 1) * p.piece * 8);
         const int len = (int)min((uint32_t)p.piece, count - (uint32_t)k * (uint32_t)p.piece);
         if (interior)
-            ws_run<P, false>(acc, xn, base, rmask, cmask, e, len);
+            ws_run<P, false>(p, acc, xn, base, rmask, cmask, e, len);
         else
-            ws_run<P, true>(acc, xn, base, rmask, cmask, e, len);
+            ws_run<P, true>(p, acc, xn, base, rmask, cmask, e, len);
         __syncthreads();  // stage k & 1 is free again
         if (threadIdx.x == 0 && k + 2 < npieces) issue(k + 2);
     }
@@ -190,7 +205,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
     for (int i = 0; i < P; ++i) {
         const int oy = oy0 + i * ROWS;
-        if (oy < p.E) yo[(size_t)oy * p.F] = ws_finish(p, m, acc[i]);
+        if (oy < p.E && dbg_ok((unsigned)m < (unsigned)p.M, p.err))
+            yo[(size_t)oy * p.F] = ws_finish(p, m, acc[i]);
     }
 }
 
@@ -245,6 +261,7 @@ cudaError_t launch_forward_ws(const Geometry &g, int N, const float *x, float *y
     p.R = g.R; p.S = g.S; p.stride = g.stride; p.pad = g.pad;
     p.tiles_x = g.tiles_x;
     p.piece = g.chunk;
+    p.ent_bytes = d.blob_bytes;
     const dim3 grid((unsigned)g.M, (unsigned)(g.tiles_y * g.tiles_x), (unsigned)N);
     fn<<<grid, kWarps * 32, smem, stream>>>(p);
     return cudaGetLastError();

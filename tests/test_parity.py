@@ -28,6 +28,9 @@ def run_gpu(x, rowptr, colidx, value, C, H, W, M, R, S, stride, pad, stream=None
     out = torch.full((x.shape[0], M, E, F), prefill, device="cuda", dtype=torch.float32)
     swd.forward(xd, w, out=out, stream=stream)
     torch.cuda.synchronize()
+    # no kernel reported a failure (a timed-out wait, or a failed check of the
+    # bounds-checked build)
+    assert w.device_status(stream) == 0
     w.close()
     return out.cpu().numpy().astype(np.float64)
 
