@@ -196,7 +196,8 @@ def decode_layout(w):
 
 
 @pytest.mark.parametrize("fmt,name", [(f, n) for f in ("f32", "packed32") for n in (
-    "tiny", "tiny_int", "resnet3x3", "vgg3x3", "sweep90", "sweep99", "alex11x11", "conv5x5")])
+    "tiny", "tiny_int", "resnet3x3", "vgg3x3", "sweep50", "sweep80", "sweep90", "sweep99",
+    "alex11x11", "conv5x5")])
 def test_packed_layout_decodes_to_csr(name, fmt):
     L = workloads.LAYERS[name]
     rowptr, colidx, value = workloads.make_weights(L)
