@@ -310,6 +310,12 @@ typedef struct spconv_packed_info {
                               /* of tile_cols outputs, each lane holding       */
                               /* tile_rows consecutive outputs of one row      */
                               /* (entry offsets as for the padded tile)        */
+    int32_t tile_images;      /* 2: image-pair column blocks -- lanes 0..3 of  */
+                              /* a lane row on image 2n, lanes 4..7 on image   */
+                              /* 2n + 1; a stage holds both images' sub-tiles  */
+                              /* (same offsets), the second pair_off words     */
+                              /* after the first; else 1                       */
+    int32_t pair_off;
 } spconv_packed_info;
 
 /* For a SPCONV_FORMAT_WS handle: tile_rows, lane_rows, tile_cols, tiles_y and

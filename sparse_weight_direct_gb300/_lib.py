@@ -55,7 +55,7 @@ class PackedInfo(ctypes.Structure):
         (n, ctypes.c_int32) for n in
         ("hdr_words", "blob_stage_bytes", "in_stage_bytes", "lane_rows", "dense_groups",
          "dense_mask_words", "format", "batch_hint", "blob_stride", "tap_pairs",
-         "plane_stage", "col_blocks")]
+         "plane_stage", "col_blocks", "tile_images", "pair_off")]
 
 
 class LaunchInfo(ctypes.Structure):

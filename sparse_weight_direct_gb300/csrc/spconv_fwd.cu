@@ -32,7 +32,10 @@ __global__ void wait_selftest_kernel(unsigned int *flags, unsigned long long lim
 
 KernelFn pick(int S, int stride, int P, int Q, int LR, bool pairs = false, bool plane = false,
               bool cols = false, int W = 0) {
-    if (cols) return (S == 3 && stride == 1 && !pairs && !plane) ? pick_cols(P, Q, LR) : nullptr;
+    if (cols) {
+        if (S != 3 || stride != 1 || pairs || plane) return nullptr;
+        return LR == 4 ? pick_colpair(P, Q) : pick_cols(P, Q, LR);
+    }
     if (pairs) return pick_pairs(S, stride, P, Q, LR);
     if (plane) return (S == 3 && stride == 1 && LR == 2) ? pick_plane(P, Q, W) : nullptr;
     switch (Q) {
@@ -105,7 +108,9 @@ static size_t recv_bytes(const Geometry &g, int split) {
 
 void forward_grid(const Geometry &g, int N, int split, bool group_fast, unsigned *gx,
                   unsigned *gy) {
-    const int64_t tiles = (int64_t)N * g.tiles_y * g.tiles_x * split;
+    const int ti = g.tile_images > 1 ? g.tile_images : 1;
+    const int64_t tiles = (int64_t)((N + ti - 1) / ti) * g.tiles_y *
+                          g.tiles_x * split;
     *gx = (unsigned)(group_fast ? tiles * g.groups : tiles);
     *gy = group_fast ? 1u : (unsigned)g.groups;
 }
@@ -163,7 +168,8 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
     p.dense_mask_words = g.dense_mask_words;
     p.in_stage_bytes = (int)g.in_stage_bytes;
     p.stage_bytes = (int)stage_bytes(g);
-    p.in_tma_bytes = g.chunk * g.plane * (int)sizeof(float);
+    // (image pairs: one box spans both images' sub-tiles)
+    p.in_tma_bytes = g.chunk * g.plane * (int)sizeof(float) * (g.tile_images == 2 ? 2 : 1);
     p.use_tma = tmap ? 1 : 0;
     p.fmt = g.format;
     p.blob_stride16 = (uint32_t)g.blob_stride16;
@@ -171,6 +177,7 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
     p.pairs = (g.stride == 1 && g.W % 2 == 0 && g.row_pitch % 2 == 0 && g.plane % 2 == 0) ? 1 : 0;
     p.recv_off = (int)stages_bytes(g, split);
     p.plane_stage = g.plane_stage;
+    p.pair_off = g.tile_images == 2 ? g.pair_off : 0;
     p.num_slots = g.num_slots;
     p.smem_bytes = (int)smem;
     p.blob_bytes = d.blob_bytes;

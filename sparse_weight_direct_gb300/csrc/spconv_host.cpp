@@ -111,7 +111,7 @@ int validate_csr(int M, int64_t CRS, const int32_t *rowptr, const int32_t *colid
 
 // Tile shape and channel group size (everything but the chunking).
 int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, int stride,
-               int pad, int64_t nnz) {
+               int pad, int64_t nnz, double dense_share) {
     g.C = C; g.H = H; g.W = W; g.M = M; g.R = R; g.S = S; g.stride = stride; g.pad = pad;
     g.E = out_extent(H, R, stride, pad);
     g.F = out_extent(W, S, stride, pad);
@@ -146,6 +146,8 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     // staged row pitch is 4 mod 8 words, so the 32 lanes' first inputs
     // (ly * pitch + 7 lx) fall in distinct banks.
     g.col_blocks = 0;
+    g.tile_images = 1;
+    g.pair_off = 0;
     const bool tile_fmt = g.format == SPCONV_FORMAT_F32 || g.format == SPCONV_FORMAT_PACKED32;
     if (stride == 1 && R == 3 && S == 3 && tile_fmt && g.lane_rows == 1) {
         const int64_t area = (int64_t)g.tiles_y * g.tile_h * g.tiles_x * g.tile_w;
@@ -166,13 +168,50 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
             g.row_pitch = rp;
         }
     }
+    // Image-pair column blocks (3x3, stride 1, outputs 22..28 wide, batches of
+    // two or more): four lane rows of eight lanes, lanes 0..3 of a row on image
+    // 2n and 4..7 on image 2n + 1, each lane seven consecutive outputs -- a
+    // 4 x 28 tile of each of two images, so 28-wide outputs leave no lane idle
+    // (a column-per-lane tile leaves 4 of 32).  Same pitch rule as column
+    // blocks: the first image's 16 lanes start in 16 distinct banks, and the
+    // second image's sub-tile starts 16 words later (mod 32), in the other 16.
+    // The four-row tiles stage a fifth more input per channel, so chunks are
+    // smaller and per-chunk costs grow: measured on GB300 (the lognormal
+    // 512-channel 28 x 28 layers) they paid only where dense-tap rows hold most
+    // of the nonzeros (50 % sparse: 630 -> 584 us), and lost where sparse rows
+    // dominate (90 %: 244 -> 250, 95 %: 117 -> 123, 99 %: 38.6 -> 46.1 us).
+    // Taken when they cover at least 3 % fewer output positions and dense-tap
+    // rows hold at least three quarters of the nonzeros.
+    if (stride == 1 && R == 3 && S == 3 && tile_fmt && !g.col_blocks && g.lane_rows == 1 &&
+        g.F > 21 && g.F <= 28 && g.batch_hint >= 2 && dense_share >= 0.75) {
+        const int64_t nb = g.batch_hint;
+        const int64_t area = nb * g.tiles_y * g.tile_h * g.tiles_x * g.tile_w;
+        const int64_t area_p = (nb + 1) / 2 * 2 * ((g.E + 3) / 4) * 4 * 28;
+        if (area_p * 100 < area * 97) {
+            g.col_blocks = 1;
+            g.tile_images = 2;
+            g.lane_rows = 4;
+            g.tile_rows = 7;
+            g.tile_h = 4;
+            g.tile_w = 28;
+            g.tiles_y = (g.E + g.tile_h - 1) / g.tile_h;
+            g.tiles_x = (g.F + g.tile_w - 1) / g.tile_w;
+            g.in_rows = g.tile_h - 1 + R;
+            g.in_cols = g.tile_w - 1 + S;
+            int rp = (int)round_up((size_t)(g.shift + g.in_cols), 4);
+            if (rp % 8 == 0) rp += 4;
+            g.phase_pitch = rp;
+            g.row_pitch = rp;
+        }
+    }
     g.plane = g.in_rows * g.row_pitch;
     g.warps = spconv::kWarps;
     // output channels per warp: the largest Q in {4, 2, 1} whose one-image
     // grid, with the channels split over a full cluster, still gives ~1.5
     // blocks per SM (small layers trade per-warp reuse for parallelism)
     // blocks of one launch per channel group, at the planned batch size
-    const int64_t spatial = (int64_t)g.tiles_y * g.tiles_x * std::max(1, g.batch_hint);
+    const int64_t spatial = (int64_t)g.tiles_y * g.tiles_x *
+                            ((std::max(1, g.batch_hint) + g.tile_images - 1) / g.tile_images);
     auto groups_of = [&](int Q) {
         return (M + (int64_t)spconv::kWarps * Q - 1) / ((int64_t)spconv::kWarps * Q);
     };
@@ -237,7 +276,7 @@ int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx)
     const double crs = (double)g.C * g.R * g.S;
     auto nnz_of = [&](int m) { return (int64_t)rowptr[m + 1] - rowptr[m]; };
     std::vector<int> dense, sparse;
-    const bool can_dense = !g.plane_stage && !g.col_blocks &&
+    const bool can_dense = !g.plane_stage &&
                            spconv::dense_taps_supported(g.R, g.S, g.stride, g.lane_rows, g.slots);
     for (int m = 0; m < g.M; ++m)
         (can_dense && nnz_of(m) / crs >= kDenseRowMin ? dense : sparse).push_back(m);
@@ -392,8 +431,8 @@ size_t dense_blob_bytes(const spconv::Geometry &g, int chunk) {
 int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
     // gpre[(group) * (C + 1) + c]: entries of the group in channels [0, c)
     const int C = g.C;
-    const int64_t base_blocks =
-        (int64_t)g.tiles_y * g.tiles_x * g.groups * std::max(1, g.batch_hint);
+    const int64_t base_blocks = (int64_t)g.tiles_y * g.tiles_x * g.groups *
+                                ((std::max(1, g.batch_hint) + g.tile_images - 1) / g.tile_images);
     int want_split = base_blocks >= kSMs
                          ? 1
                          : (int)std::min<int64_t>(spconv::kMaxSplit,
@@ -416,11 +455,21 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
     // block per SM).
     const bool one_per_block =
         g.batch_hint > 0 && want_split > 1 && (int64_t)cap * want_split >= C;
+    // image pairs take only chunks with chunk * plane = 16 mod 32 words (see
+    // below): start from the first such chunk at or above the cap (a chunk
+    // past C reads zeros for the missing channels)
+    if (g.tile_images == 2)
+        while (cap < 256 && (size_t)cap * g.plane % 32 != 16) ++cap;
     for (int chunk = cap; chunk >= 1; --chunk) {
         const int nch = (C + chunk - 1) / chunk;
         const size_t hdr_bytes = (size_t)g.hdr_words * 4;
+        // (image pairs: the second image's sub-tile follows the first's, as one
+        // tensor copy writes them, so chunk * plane must be 16 mod 32 words for
+        // the two halves of a warp to load from disjoint banks)
+        if (g.tile_images == 2 && (size_t)chunk * g.plane % 32 != 16) continue;
+        const size_t pair_off = g.tile_images == 2 ? (size_t)chunk * g.plane : 0;
         const size_t in_stage = round_up(
-            ((size_t)chunk * g.plane +
+            (pair_off + (size_t)chunk * g.plane +
              (g.plane_stage ? spconv::kPlaneLead + spconv::kPlaneTail : 0)) * sizeof(float),
             128);
         size_t blob_max = g.dense_groups ? dense_blob_bytes(g, chunk) : 0;
@@ -441,6 +490,7 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
         if (total <= kSmemBudget || fits_split || (chunk == 1 && total <= 200 * 1024)) {
             g.chunk = chunk;
             g.num_chunks = nch;
+            g.pair_off = (int)pair_off;
             g.dense_mask_words = (int)round_up((size_t)g.warps * chunk, 4);
             g.in_stage_bytes = in_stage;
             g.blob_stage_bytes = round_up(blob_max, 128);
@@ -845,7 +895,15 @@ int make_handle(int C, int H, int W, int M, int R, int S, int stride, int pad,
         st = plan_ws(P->g, C, H, W, M, R, S, stride, pad, rowptr);
         if (!st) st = build_layout_ws(*P, rowptr, colidx, value);
     } else {
-        st = plan_tiles(P->g, C, H, W, M, R, S, stride, pad, nnz);
+        // share of the nonzeros in rows dense enough for the dense-tap path
+        int64_t dense_nnz = 0;
+        const double crs = (double)C * R * S;
+        for (int m = 0; m < M; ++m) {
+            const int64_t k = (int64_t)rowptr[m + 1] - rowptr[m];
+            if (k / crs >= kDenseRowMin) dense_nnz += k;
+        }
+        st = plan_tiles(P->g, C, H, W, M, R, S, stride, pad, nnz,
+                        nnz > 0 ? (double)dense_nnz / nnz : 0.0);
         if (!st) st = build_layout(*P, rowptr, colidx, value);
     }
     if (st) {
@@ -991,7 +1049,10 @@ const CUtensorMap *input_tmap(const spconv_packed *P, const float *x, int N, CUt
     cuuint64_t dims[4] = {(cuuint64_t)g.W, (cuuint64_t)g.H, (cuuint64_t)g.C, (cuuint64_t)N};
     cuuint64_t strides[3] = {(cuuint64_t)g.W * 4, (cuuint64_t)g.H * g.W * 4,
                              (cuuint64_t)g.C * g.H * g.W * 4};
-    cuuint32_t box[4] = {(cuuint32_t)g.row_pitch, (cuuint32_t)g.in_rows, (cuuint32_t)g.chunk, 1};
+    // (image pairs: the box spans two images, the second sub-tile right after
+    // the first -- chunk * plane words later, which the planner makes 16 mod 32)
+    cuuint32_t box[4] = {(cuuint32_t)g.row_pitch, (cuuint32_t)g.in_rows, (cuuint32_t)g.chunk,
+                         (cuuint32_t)(g.tile_images == 2 ? 2 : 1)};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(&tmp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1038,7 +1099,8 @@ bool choose_pdl(const spconv::Geometry &g, int N, int split, bool group_fast) {
 // else enough for about two blocks per SM
 // (measured best on the one-image ResNet-style layer).
 int choose_split(const spconv::Geometry &g, int N) {
-    const int64_t blocks = (int64_t)N * g.tiles_y * g.tiles_x * g.groups;
+    const int64_t blocks = (int64_t)((N + g.tile_images - 1) / g.tile_images) * g.tiles_y *
+                           g.tiles_x * g.groups;
     if (blocks >= kSMs) return 1;
     int s = (int)std::min<int64_t>(spconv::kMaxSplit, (2 * kSMs + blocks - 1) / blocks);
     return std::max(1, std::min(s, g.num_chunks));
@@ -1325,6 +1387,8 @@ __attribute__((visibility("default"))) int spconv_packed_info_get(const spconv_p
     info->tap_pairs = g.tap_pairs;
     info->plane_stage = g.plane_stage;
     info->col_blocks = g.col_blocks;
+    info->tile_images = g.tile_images;
+    info->pair_off = g.pair_off;
     return SPCONV_OK;
 }
 

@@ -91,6 +91,10 @@ struct Geometry {
     int col_blocks;   // 1: column blocks -- lane_rows lane rows of 32 / lane_rows
                       // lanes, each lane holding tile_rows consecutive outputs of
                       // its row (stride 1, widths a multiple of 28, not of 32)
+    int tile_images;  // images side by side in a tile: 2 for image-pair column
+                      // blocks (then N counts pairs in the grid), else 1
+    int pair_off;     // image pairs: words from a stage's first sub-tile to its
+                      // second (so the two halves of a warp hit disjoint banks)
     int dense_groups; // leading groups whose blobs are dense-tap (0 if none)
     int split_rows;   // 1 if any group has rows split into parts (bit 1 of its flags)
     int dense_mask_words;  // words of a dense blob's slot masks (warps * chunk, to 4)

@@ -79,6 +79,9 @@ struct KParams {
     int pairs;               // cp.async staging in 8-byte column pairs (stride 1, W even)
     int recv_off;            // byte offset of that receive buffer in shared memory
     int plane_stage;         // raw planes staged by one bulk copy (kModePlane instances)
+    int pair_off;            // image-pair column blocks: words from a stage's first
+                             // sub-tile (image 2n) to its second (image 2n + 1), else 0;
+                             // with TMA one box spans both images (in_tma_bytes)
     int num_slots;           // entries of slot_oc / slot_next (bounds-checked build)
     int smem_bytes;          // dynamic shared memory of the launch (bounds-checked build)
     int64_t blob_bytes;      // bytes of the blobs array (bounds-checked build)
@@ -516,6 +519,52 @@ static __device__ __forceinline__ void run_dense_chunk(float (&acc)[Q][P], const
     }
 }
 
+// Dense-tap accumulation for column blocks: a lane's P outputs run along a
+// row, so the channel's window is K rows x (P + K - 1) columns starting at the
+// lane's first output; tap (r, c) of output p reads window (r, p + c).  Blob
+// layout as for run_dense_chunk.
+template <int P, int Q, int K>
+static __device__ __forceinline__ void run_dense_chunk_cols(float (&acc)[Q][P], const float *sb,
+                                                            const uint32_t *dmask, const float4 *dw,
+                                                            int warp, int chunk, int cc, int plane,
+                                                            int rp, const Span &sp,
+                                                            const void *blob_end) {
+    constexpr int WC = P + K - 1;         // window columns
+    constexpr int KK4 = (K * K + 3) / 4;  // float4 per weight block
+    for (int cl = 0; cl < cc; ++cl) {
+        const uint32_t mask = dmask[warp * chunk + cl];
+        if (mask == 0) continue;
+        const float *s = sb + cl * plane;
+        float win[K][WC];
+#pragma unroll
+        for (int r = 0; r < K; ++r)
+#pragma unroll
+            for (int j = 0; j < WC; ++j) win[r][j] = sld(sp, s + r * rp + j);
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            if (!(mask & (1u << q))) continue;
+            const float4 *wq = dw + ((size_t)(warp * chunk + cl) * Q + q) * KK4;
+            if (!dbg_ok((const void *)(wq + KK4) <= blob_end, sp.err)) continue;
+            float w[KK4 * 4];
+#pragma unroll
+            for (int t = 0; t < KK4; ++t) {
+                const float4 v = wq[t];
+                w[4 * t] = v.x;
+                w[4 * t + 1] = v.y;
+                w[4 * t + 2] = v.z;
+                w[4 * t + 3] = v.w;
+            }
+#pragma unroll
+            for (int r = 0; r < K; ++r)
+#pragma unroll
+                for (int c = 0; c < K; ++c)
+#pragma unroll
+                    for (int pc = 0; pc < P; ++pc)
+                        acc[q][pc] = fmaf(w[r * K + c], win[r][pc + c], acc[q][pc]);
+        }
+    }
+}
+
 // The first page's packed weight word (Tuteja et al., Sec. 5.3, Fig. 4):
 // [31:16] FP16 value, [15:8] input channel (here: within the chunk), [7:4]
 // kernel column px, [3:0] kernel row py.  The offset into the staged tile is
@@ -555,6 +604,7 @@ static __device__ __forceinline__ void run_segment_words(float (&acc)[P], const 
 constexpr int kModePairs = 2;
 constexpr int kModePlane = 3;  // plane staging (see apply_entry_plane)
 constexpr int kModeCols = 4;   // column blocks: a lane's P outputs run along a row
+constexpr int kModeColsPair = 5;  // column blocks over two images side by side
 template <int P, int Q, int S_CT, int ST_CT, int LR, int MODE = 0, int PLANE_RS = 0>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     spconv_fwd_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap) {
@@ -563,8 +613,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     // Column blocks (stride 1): lane (ly, lx) holds outputs (ly, lx*P + r) of
     // an LR x (LC*P) tile, so widths that are multiples of LC*P but not of 32
     // leave no lane idle; a tap's P inputs are consecutive words.
-    constexpr bool COLS = MODE == kModeCols;
+    // Image-pair column blocks (outputs 22..28 wide): four lane rows of eight
+    // lanes; lanes 0..3 of a row cover image 2n, lanes 4..7 image 2n + 1,
+    // each lane seven consecutive outputs, so a 4 x 28 tile of each image
+    // leaves no lane idle (28-wide outputs waste 4 of 32 lanes otherwise).
+    // The stage holds the two images' sub-tiles pair_off words apart.
+    constexpr bool PAIR = MODE == kModeColsPair;
+    constexpr bool COLS = MODE == kModeCols || PAIR;
     static_assert(!COLS || ST_CT == 1, "column blocks: stride 1");
+    static_assert(!PAIR || (LR == 4 && P == 7), "image-pair column blocks: 4 x (2 x 28)");
     static_assert(!PLANE || (S_CT == 3 && ST_CT == 1 && LR == 2), "plane staging: 3x3, two lane rows");
     static_assert(PLANE || PLANE_RS == 0, "a fixed row step is a plane-staging instance");
     static_assert(!PAIRS || Q == 2 || Q == 4, "tap pairs: 2 or 4 output channels per warp");
@@ -605,7 +662,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int k_begin = kr * p.num_chunks / split;
     const int k_end = (kr + 1) * p.num_chunks / split;
     const int iy0 = ty * (COLS ? LR : LR * P) * st - p.pad;
-    const int ix0 = tx * (COLS ? LC * P : LC) * st - p.pad;
+    const int ix0 = tx * (PAIR ? (LC / 2) * P : COLS ? LC * P : LC) * st - p.pad;
+    // images of the block's tile (image pairs: n counts pairs) and of this lane
+    const int img0 = PAIR ? 2 * n : n;
+    const int img1 = img0 + 1;  // (image pairs) the second image, if < N
+    const int n_out = PAIR ? img0 + (lx >= LC / 2 ? 1 : 0) : n;
     const int nmine = k_end - k_begin;
     const int nslot = kWarps * Q;
 
@@ -722,15 +783,21 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             }
             return;
         }
+        // (image pairs: the box spans both images, the second landing pair_off
+        // words after the first -- one 128-byte aligned destination; an image
+        // past the batch reads as zeros)
         if (issuer && input && p.use_tma && in_fits)
-            tma_load_4d(base, &tmap, ix0 - p.shift, iy0, c0, n, &bar[s]);
+            tma_load_4d(base, &tmap, ix0 - p.shift, iy0, c0, img0, &bar[s]);
         if (input && !p.use_tma) {
-            if (ST_CT == 1 && p.pairs)
-                stage_input_cp_async_pairs(p, reinterpret_cast<float *>(base), n, c0,
-                                           min(p.chunk, p.C - c0), iy0, ix0);
-            else
-                stage_input_cp_async<ST_CT>(p, reinterpret_cast<float *>(base), n, c0,
-                                            min(p.chunk, p.C - c0), iy0, ix0);
+            for (int h = 0; h < (PAIR && img1 < p.N ? 2 : 1); ++h) {
+                float *dst = reinterpret_cast<float *>(base) + h * p.pair_off;
+                if (ST_CT == 1 && p.pairs)
+                    stage_input_cp_async_pairs(p, dst, img0 + h, c0, min(p.chunk, p.C - c0), iy0,
+                                               ix0);
+                else
+                    stage_input_cp_async<ST_CT>(p, dst, img0 + h, c0, min(p.chunk, p.C - c0),
+                                                iy0, ix0);
+            }
             cp_async_commit();
         }
     };
@@ -770,7 +837,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (failed) break;
         const unsigned char *base = smem + (size_t)s * p.stage_bytes;
         const float *sb = reinterpret_cast<const float *>(base) + ly * st * p.row_pitch +
-                          (COLS ? lx * P : lx);
+                          (PAIR ? (lx >= LC / 2 ? p.pair_off : 0) + (lx % (LC / 2)) * P
+                                : COLS ? lx * P : lx);
         if constexpr (PLANE) {
             // dense planes: lanes past the image's width read the spare banks
             // 2W .. 31 (finite values, outputs discarded), so the 32 reads of a
@@ -783,6 +851,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         const Span sp{reinterpret_cast<const float *>(base),
                       reinterpret_cast<const float *>(base + p.in_stage_bytes), p.err};
         const unsigned char *blob_end = base + p.stage_bytes;
+        if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4 && COLS) {
+            if (dense) {
+                const int k = k_begin + it;
+                run_dense_chunk_cols<P, Q, S_CT>(
+                    acc, sb + p.shift, hdr, reinterpret_cast<const float4 *>(hdr + p.dense_mask_words),
+                    warp, p.chunk, min(p.chunk, p.C - k * p.chunk), p.plane, p.row_pitch, sp,
+                    blob_end);
+            }
+        }
         if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4 && !PLANE && !COLS) {
             if (dense) {
                 const int k = k_begin + it;
@@ -874,9 +951,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const unsigned char *smem_end = smem_raw + p.smem_bytes;
     // This lane's outputs r = 0 .. P-1: rows oy0 + LR * r of column ox, or
     // (column blocks) columns ox + r of row oy0.
-    const int ox = COLS ? tx * (LC * P) + lx * P : tx * LC + lx;
+    const int ox = PAIR ? tx * ((LC / 2) * P) + (lx % (LC / 2)) * P
+                        : COLS ? tx * (LC * P) + lx * P : tx * LC + lx;
     const int oy0 = COLS ? ty * LR + ly : ty * (LR * P) + ly;
-    const bool lane_out = COLS ? oy0 < p.E : ox < p.F;  // the lane has outputs
+    const bool lane_out = (COLS ? oy0 < p.E : ox < p.F) && n_out < p.N;  // the lane has outputs
     auto out_ok = [&](int r) { return COLS ? ox + r < p.F : oy0 + LR * r < p.E; };
     auto out_at = [&](int r) {  // offset of output r within its (n, m) plane
         return COLS ? (size_t)oy0 * p.F + ox + r : (size_t)(oy0 + LR * r) * p.F + ox;
@@ -901,13 +979,20 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             for (int q = 0; q < Q; ++q) {
                 const int m = q == 0 ? pre_m : slot_oc_at(p, slot0 + q);
                 if (m < 0) continue;
-                float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
 #pragma unroll
                 for (int i = 0; i < P; ++i) {
+                    // tile position t: row t / (LC*P); with image pairs the row's
+                    // first half is image 2n, its second half image 2n + 1
                     const int t = i * 32 + lane;
-                    const int oy = ty * LR + t / (LC * P), oxt = tx * (LC * P) + t % (LC * P);
-                    if (oy < p.E && oxt < p.F && dbg_ok(m < p.M, p.err))
-                        yo[(size_t)oy * p.F + oxt] = finish(p, m, tb[q * (P * 32) + t]);
+                    const int oy = ty * LR + t / (LC * P);
+                    const int col = t % (LC * P);
+                    const int half = PAIR ? col / ((LC / 2) * P) : 0;
+                    const int oxt = PAIR ? tx * ((LC / 2) * P) + col % ((LC / 2) * P)
+                                         : tx * (LC * P) + col;
+                    const int img = img0 + half;
+                    if (oy < p.E && oxt < p.F && img < p.N && dbg_ok(m < p.M, p.err))
+                        p.y[(((size_t)img * p.M + m) * p.E + oy) * p.F + oxt] =
+                            finish(p, m, tb[q * (P * 32) + t]);
                 }
             }
             return;
@@ -919,7 +1004,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         for (int q = 0; q < Q; ++q) {
             const int m = q == 0 ? pre_m : slot_oc_at(p, slot0 + q);
             if (m < 0) continue;
-            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
+            float *yo = p.y + ((size_t)n_out * p.M + m) * p.E * p.F;
 #pragma unroll
             for (int r = 0; r < P; ++r)
                 if (out_ok(r) && dbg_ok(m < p.M, p.err)) yo[out_at(r)] = finish(p, m, acc[q][r]);
@@ -976,7 +1061,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                 for (int j = 0; j < kMaxSplit; ++j)
                     if (j < split) sum += v[j];
                 if (out_ok(r) && dbg_ok(m < p.M, p.err))
-                    p.y[((size_t)n * p.M + m) * p.E * p.F + out_at(r)] = finish(p, m, sum);
+                    p.y[((size_t)n_out * p.M + m) * p.E * p.F + out_at(r)] = finish(p, m, sum);
             }
             return;
         }
@@ -1004,7 +1089,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             const int m = q == 0 ? pre_m : slot_oc_at(p, group * nslot + sl);
             if (m < 0) continue;
             const int next0 = q == 0 ? pre_next : slot_next_at(p, group * nslot + sl);
-            float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
+            float *yo = p.y + ((size_t)n_out * p.M + m) * p.E * p.F;
             for (int r = 0; r < P; ++r) {
                 float sum = part[(sl * P + r) * 32 + lane];
                 for (int c = next0; c >= 0 && dbg_ok(c < nslot, p.err);
@@ -1042,7 +1127,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                         if (j < split) sum += v[j];
                 }
                 if (out_ok(r) && dbg_ok(m < p.M, p.err))
-                    p.y[((size_t)n * p.M + m) * p.E * p.F + out_at(r)] = finish(p, m, sum);
+                    p.y[((size_t)n_out * p.M + m) * p.E * p.F + out_at(r)] = finish(p, m, sum);
             }
         }
     } else {
@@ -1052,7 +1137,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             for (int sl = s_begin + warp; sl < s_end; sl += kWarps) {
                 const int m = slot_oc_at(p, group * nslot + sl);
                 if (m < 0) continue;
-                float *yo = p.y + ((size_t)n * p.M + m) * p.E * p.F;
+                float *yo = p.y + ((size_t)n_out * p.M + m) * p.E * p.F;
                 for (int r = 0; r < P; ++r) {
                     float sum = 0.f;
                     for (int c = sl; c >= 0 && dbg_ok(c < nslot, p.err);
@@ -1081,6 +1166,8 @@ KernelFn pick_pairs(int S, int stride, int P, int Q, int LR);
 // images (row step 28 words) have their own, with immediate load offsets.
 KernelFn pick_plane(int P, int Q, int W);
 KernelFn pick_cols(int P, int Q, int LR);
+// Image-pair column-block instances (3x3 stride 1, four lane rows of eight).
+KernelFn pick_colpair(int P, int Q);
 
 // Instantiates the kernels of one Q for the supported kernel widths, strides,
 // rows per lane and lane rows.

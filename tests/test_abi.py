@@ -225,9 +225,20 @@ def test_packed_layout_decodes_to_csr(name, fmt):
         # (ly * row_pitch + lx * tile_rows) fall in 32 distinct banks
         P, LR = info["tile_rows"], info["lane_rows"]
         tile_h = LR
-        assert info["tile_cols"] == (32 // LR) * P and L.stride == 1
-        banks = {(ly * info["row_pitch"] + lx * P) % 32 for ly in range(LR)
-                 for lx in range(32 // LR)}
+        if info["tile_images"] == 2:
+            # image pairs: lanes 0..3 of a row on the first image's sub-tile,
+            # lanes 4..7 on the second's, pair_off words later
+            assert LR == 4 and info["tile_cols"] == 4 * P and L.stride == 1
+            assert info["pair_off"] % 32 == 16
+            assert info["pair_off"] >= info["chunk"] * info["plane"]
+            assert info["in_stage_bytes"] >= 4 * (info["pair_off"] + info["chunk"] * info["plane"])
+            banks = {((lx // 4) * info["pair_off"] + ly * info["row_pitch"] + (lx % 4) * P) % 32
+                     for ly in range(LR) for lx in range(8)}
+        else:
+            assert info["tile_images"] == 1 and info["pair_off"] == 0
+            assert info["tile_cols"] == (32 // LR) * P and L.stride == 1
+            banks = {(ly * info["row_pitch"] + lx * P) % 32 for ly in range(LR)
+                     for lx in range(32 // LR)}
         assert len(banks) == 32
         assert info["row_pitch"] % 4 == 0 and info["row_pitch"] >= info["shift"] + info["in_cols"]
     else:
@@ -303,8 +314,16 @@ def test_launch_plans():
     assert info["col_blocks"] == 1  # the 32-bit words decode to the same offsets
     L, info, pl = plan("resnet3x3", 1, batch_hint=1, fmt="packed32")
     assert info["plane_stage"] == 0 and info["col_blocks"] == 0  # padded tile
-    L, info, pl = plan("sweep90", 8, batch_hint=8)  # 28 wide: column-per-lane tiles
+    # 28 wide, dense-tap rows holding most nonzeros: image-pair column blocks
+    L, info, pl = plan("sweep50", 8, batch_hint=8)
+    assert info["col_blocks"] == 1 and info["tile_images"] == 2 and info["lane_rows"] == 4
+    assert (info["tile_rows"], info["tile_cols"], info["tiles_y"], info["tiles_x"]) == (7, 28, 7, 1)
+    assert pl["grid_x"] * pl["grid_y"] == 4 * 7 * info["groups"]  # 4 image pairs x 7 row bands
+    assert info["dense_groups"] > 0
+    L, info, pl = plan("sweep90", 8, batch_hint=8)  # mostly sparse rows: column-per-lane tiles
     assert info["col_blocks"] == 0 and info["lane_rows"] == 1 and info["tile_cols"] == 32
+    L, info, pl = plan("sweep50", 1, batch_hint=1)  # one image: no image pairs
+    assert info["tile_images"] == 1
     L, info, pl = plan("sweep80", 8, batch_hint=8)  # dense-tap groups, several waves
     assert info["dense_groups"] > 0 and pl["grid_x"] * pl["grid_y"] > 2 * 152
     assert pl["pdl"] == 0
@@ -450,7 +469,11 @@ SHAPE_CASES = [
     (2, 12, 112, 112, 16, 1, 0.05, "cols"),
     (1, 40, 14, 10, 24, 1, 0.3, "plane"),
     (1, 64, 14, 14, 70, 1, 0.2, "plane"),
-    (2, 17, 28, 28, 33, 1, 0.15, "tile"),   # 28 x 28: same cover either way
+    (2, 17, 28, 28, 33, 1, 0.15, "tile"),   # 28 x 28, sparse rows: column-per-lane tiles
+    (2, 17, 28, 28, 33, 1, 0.4, "cols"),    # dense rows: image-pair column blocks
+    (1, 17, 28, 28, 33, 1, 0.4, "tile"),    # one image: column-per-lane tiles
+    (4, 5, 30, 25, 9, 0, 0.4, "cols"),      # 28 x 23 outputs, pad 0: image pairs
+    (4, 6, 20, 26, 11, 1, 0.45, "cols"),    # 20 x 26: the last 4 x 28 columns partly used
 ]
 
 

@@ -437,8 +437,51 @@ def test_column_blocks(case, integer, fmt):
     w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=3, S=3, stride=1, pad=pad,
                       batch_hint=N, fmt=fmt)
     assert w.info()["col_blocks"] == 1
-    assert not heavy or (w.array("group_flags") & 2).any()
+    # heavy rows: split into parts, or (dense enough) on the dense-tap path
+    assert not heavy or (w.array("group_flags") & 3).any()
     w.close()
     got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 3, 3, 1, pad, batch_hint=N, fmt=fmt)
     ref, mag = oracle.csr(x, rowptr, colidx, value, M, 3, 3, 1, pad)
     check(got, ref, mag, exact=integer, what=f"column blocks {case}")
+
+
+PAIR_IMG_CASES = [
+    # (N run, N planned, C, H, W, M, pad, sparse density, dense rows): 3x3 stride-1 layers
+    # 22..28 outputs wide planned for a batch, whose dense rows (density 0.6) hold most
+    # nonzeros, tiled in image-pair column blocks (lanes 0..3 of a row on image 2n, 4..7 on
+    # image 2n + 1, seven consecutive outputs each); dense-tap and sparse groups
+    (16, 16, 100, 28, 28, 256, 1, 0.05, 64),  # the sweep layers' 28 x 28: no cluster, chunks
+    (15, 16, 100, 28, 28, 256, 1, 0.05, 64),  # odd batch: the last pair's second half empty
+    (8, 8, 40, 28, 28, 72, 1, 0.05, 24),      # M not a multiple of 32
+    (3, 8, 24, 28, 28, 40, 1, 0.05, 16),      # odd batch, small grid
+    (1, 8, 24, 28, 28, 40, 1, 0.05, 16),      # one image on a pair plan
+    (4, 4, 20, 30, 25, 33, 0, 0.05, 16),      # 28 x 23 outputs, pad 0 (no alignment shift)
+    (6, 6, 16, 26, 28, 24, 1, 0.05, 16),      # 26 x 28: the last row band half used
+    (2, 2, 600, 28, 28, 16, 1, 0.05, 8),      # many chunks, channel-split clusters
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", PAIR_IMG_CASES, ids=[str(c) for c in PAIR_IMG_CASES])
+@pytest.mark.parametrize("integer", [False, True])
+def test_image_pair_column_blocks(case, integer):
+    N, hint, C, H, W, M, pad, d, ndense = case
+    rng = np.random.default_rng(abs(hash(case)) % (2 ** 32) + integer)
+    CRS = C * 9
+    rows = [np.nonzero(rng.random(CRS) < (0.6 if m < ndense else d))[0] for m in range(M)]
+    rowptr = np.concatenate([[0], np.cumsum([r.size for r in rows])]).astype(np.int32)
+    colidx = np.concatenate(rows).astype(np.int32)
+    if integer:
+        value = rng.choice(np.array([-3, -2, -1, 1, 2, 3], np.float32), size=colidx.size)
+    else:
+        value = rng.normal(0, 0.05, size=colidx.size).astype(np.float32)
+    x = workloads.random_input((N, C, H, W), rng, integer=integer)
+    w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=3, S=3, stride=1, pad=pad,
+                      batch_hint=hint)
+    info = w.info()
+    assert info["col_blocks"] == 1 and info["tile_images"] == 2 and info["lane_rows"] == 4
+    assert info["dense_groups"] > 0
+    w.close()
+    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 3, 3, 1, pad, batch_hint=hint)
+    ref, mag = oracle.csr(x, rowptr, colidx, value, M, 3, 3, 1, pad)
+    check(got, ref, mag, exact=integer, what=f"image pairs {case}")
