@@ -264,8 +264,8 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
 // Output channels whose rows are dense enough go to leading "dense" groups
 // (densest first, dealt round-robin over the warps).  The rest are sparse:
 // they are spread over the sparse groups longest row first onto the group with
-// the least work that has room; a row heavier than 1.5x a warp's fair share
-// is split into parts (its column-ordered nonzeros dealt round-robin, so every
+// the least work that has room; a row heavier than 1.1x (1.5x for short
+// warps) a warp's fair share is split into parts (its column-ordered nonzeros dealt round-robin, so every
 // part spans all chunks), and inside each group the parts are bound to warp
 // slots longest first onto the least-loaded warp with a free slot.  The parts
 // of one row stay in one group and are summed in the epilogue.  Sets groups,
@@ -287,6 +287,41 @@ int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx)
         sparse.insert(sparse.end(), dense.end() - tail, dense.end());
         dense.resize(dense.size() - tail);
     }
+    // Dense-tap groups or none.  A dense-tap block does all its rows' work
+    // over all channels, so with few dense groups it can outlast the whole
+    // rest of the launch; the same rows on the sparse path (split into parts)
+    // keep every block equally long but cost more shared-memory loads.
+    // Estimate both launches and keep the shorter.  Model, fitted to
+    // per-block timelines on GB300 (the lognormal 512-channel layers): sparse
+    // work moves P + 1/2 shared-memory wavefronts per entry and output tile at
+    // ~0.88 per clock per SM; a dense-tap warp takes ~2 ns per instruction,
+    // (window rows x K + 1) loads per channel plus (3 + K*K*P + 5) per row and
+    // channel; two blocks per SM.
+    if (!dense.empty()) {
+        int64_t dense_nnz = 0, all_nnz = 0;
+        for (int m : dense) dense_nnz += nnz_of(m);
+        for (int m = 0; m < g.M; ++m) all_nnz += nnz_of(m);
+        const int ti = std::max(1, g.tile_images);
+        const double tiles = (double)g.tiles_y * g.tiles_x *
+                             ((std::max(1, g.batch_hint) + ti - 1) / ti);
+        const double lsu = 0.88 * kSMs * 2.07e9;  // wavefronts per second
+        const double wf = g.tile_rows + 0.5;
+        const double t_sparse_all = (double)all_nnz * tiles * wf / lsu;
+        const int gd = (int)((dense.size() + per_group - 1) / per_group);
+        const double rows_per_warp = (double)dense.size() / ((double)gd * g.warps);
+        const double win = (double)(g.col_blocks ? g.R * (g.tile_rows + g.S - 1)
+                                                 : (g.lane_rows * (g.tile_rows - 1) + g.R) * g.S) +
+                           1.0;
+        const double t_dense_block =
+            (double)g.C * (win + rows_per_warp * (8.0 + (double)g.R * g.S * g.tile_rows)) * 2.0e-9;
+        const double t_with_dense =
+            std::max(t_dense_block, gd * tiles * t_dense_block / (2.0 * kSMs) +
+                                        (double)(all_nnz - dense_nnz) * tiles * wf / lsu);
+        if (t_sparse_all < t_with_dense) {
+            sparse.insert(sparse.end(), dense.begin(), dense.end());
+            dense.clear();
+        }
+    }
     std::stable_sort(sparse.begin(), sparse.end(), [&](int a, int b) { return nnz_of(a) > nnz_of(b); });
     const int gd = ((int)dense.size() + per_group - 1) / per_group;
 
@@ -303,9 +338,12 @@ int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx)
         const int64_t cap = std::max<int64_t>(1, (total + (int64_t)gs * g.warps - 1) / ((int64_t)gs * g.warps));
         int64_t nparts = 0;
         for (int m : sparse) {
-            // only rows well above the fair share are worth the extra slots
-            // (and only into parts of at least kMinPart entries)
-            parts[m] = nnz_of(m) * 2 > cap * 3
+            // rows well above the fair share are split (into parts of at least
+            // kMinPart entries): above 1.1x where warps are long (a warp's load
+            // sets its block's end; 90 % lognormal layer, 1.5x 229 us, 1.2x
+            // 214, 1.1x 213), above 1.5x where they are short (fair share
+            // under 512 entries: the parts' sums cost more than they save)
+            parts[m] = (cap >= 512 ? nnz_of(m) * 10 > cap * 11 : nnz_of(m) * 2 > cap * 3)
                            ? (int)std::min<int64_t>({(nnz_of(m) + cap - 1) / cap, g.warps,
                                                      std::max<int64_t>(1, nnz_of(m) / kMinPart)})
                            : 1;

@@ -119,16 +119,29 @@ def test_edge_shapes(case, integer):
     check(got, ref, mag, exact=integer, what=str(case))
 
 
+HEAVY = [  # (N, C, H, W, M), heavy-row density, every, group flag the plan must hold
+    ((8, 128, 28, 28, 256), 0.95, 3, 1),   # a third of the rows near-dense: dense-tap groups
+    ((4, 128, 56, 56, 128), 0.8, 2, 1),    # half the rows at 0.8: dense-tap groups
+    ((8, 128, 28, 28, 256), 0.95, 7, 2),   # too few for dense groups to pay: split rows
+    ((2, 24, 12, 12, 96), 0.6, 7, 2),
+    ((2, 24, 12, 12, 96), 0.6, 40, 2),
+    ((2, 24, 12, 12, 96), 0.95, 40, 2),
+]
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("integer", [False, True])
-@pytest.mark.parametrize("heavy_density,every,want_flag", [(0.6, 7, 1), (0.95, 7, 1),
-                                                           (0.6, 40, 2), (0.95, 40, 2)])
-def test_heavy_rows_split_and_dense(heavy_density, every, want_flag, integer):
-    """Very heavy rows among sparse ones.  Many of them (every 7th row) form
-    dense-tap groups; a few (every 40th) are too few for a dense group and are
-    split into parts in several warps, summed in the epilogue."""
+@pytest.mark.parametrize("shape,heavy_density,every,want_flag", HEAVY,
+                         ids=[f"{c[0]}-{c[1]}-{c[2]}" for c in HEAVY])
+def test_heavy_rows_split_and_dense(shape, heavy_density, every, want_flag, integer):
+    """Very heavy rows among sparse ones (0.05).  Where they carry most of a
+    large layer's work, the planner's estimate puts them in dense-tap groups
+    (flag 1); where they are few, or the layer is small, the all-sparse plan
+    is estimated faster and each heavy row is split into parts in several
+    warps, summed in the epilogue (flag 2)."""
     rng = np.random.default_rng(int(heavy_density * 100) + integer + every)
-    N, C, H, W, M, K = 2, 24, 12, 12, 96, 3
+    N, C, H, W, M = shape
+    K = 3
     CRS = C * K * K
     rows = []
     for m in range(M):
@@ -142,12 +155,13 @@ def test_heavy_rows_split_and_dense(heavy_density, every, want_flag, integer):
     else:
         value = rng.normal(0, 0.05, size=colidx.size).astype(np.float32)
     x = workloads.random_input((N, C, H, W), rng, integer=integer)
-    w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=K, S=K, stride=1, pad=1)
+    w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=K, S=K, stride=1, pad=1,
+                      batch_hint=N)
     assert (w.array("group_flags") & want_flag).any()
     w.close()
-    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, K, K, 1, 1)
+    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, K, K, 1, 1, batch_hint=N)
     ref, mag = oracle.csr(x, rowptr, colidx, value, M, K, K, 1, 1)
-    check(got, ref, mag, exact=integer, what=f"heavy {heavy_density}")
+    check(got, ref, mag, exact=integer, what=f"heavy {shape} {heavy_density} {every}")
 
 
 @pytest.mark.gpu
@@ -446,18 +460,20 @@ def test_column_blocks(case, integer, fmt):
 
 
 PAIR_IMG_CASES = [
-    # (N run, N planned, C, H, W, M, pad, sparse density, dense rows): 3x3 stride-1 layers
-    # 22..28 outputs wide planned for a batch, whose dense rows (density 0.6) hold most
-    # nonzeros, tiled in image-pair column blocks (lanes 0..3 of a row on image 2n, 4..7 on
-    # image 2n + 1, seven consecutive outputs each); dense-tap and sparse groups
-    (16, 16, 100, 28, 28, 256, 1, 0.05, 64),  # the sweep layers' 28 x 28: no cluster, chunks
-    (15, 16, 100, 28, 28, 256, 1, 0.05, 64),  # odd batch: the last pair's second half empty
-    (8, 8, 40, 28, 28, 72, 1, 0.05, 24),      # M not a multiple of 32
-    (3, 8, 24, 28, 28, 40, 1, 0.05, 16),      # odd batch, small grid
-    (1, 8, 24, 28, 28, 40, 1, 0.05, 16),      # one image on a pair plan
-    (4, 4, 20, 30, 25, 33, 0, 0.05, 16),      # 28 x 23 outputs, pad 0 (no alignment shift)
-    (6, 6, 16, 26, 28, 24, 1, 0.05, 16),      # 26 x 28: the last row band half used
-    (2, 2, 600, 28, 28, 16, 1, 0.05, 8),      # many chunks, channel-split clusters
+    # (N run, N planned, C, H, W, M, pad, sparse density, dense rows, dense groups planned):
+    # 3x3 stride-1 layers 22..28 outputs wide planned for a batch, whose dense rows
+    # (density 0.6) hold most nonzeros, tiled in image-pair column blocks (lanes 0..3 of a
+    # row on image 2n, 4..7 on image 2n + 1, seven consecutive outputs each).  On the two
+    # large layers the planner's estimate keeps dense-tap groups beside the sparse ones; on
+    # the small ones an all-sparse plan is estimated faster and the heavy rows are split.
+    (16, 16, 100, 28, 28, 256, 1, 0.05, 64, True),  # the sweep layers' 28 x 28: chunks
+    (15, 16, 100, 28, 28, 256, 1, 0.05, 64, True),  # odd batch: last pair's second half empty
+    (8, 8, 40, 28, 28, 72, 1, 0.05, 24, False),     # M not a multiple of 32
+    (3, 8, 24, 28, 28, 40, 1, 0.05, 16, False),     # odd batch, small grid
+    (1, 8, 24, 28, 28, 40, 1, 0.05, 16, False),     # one image on a pair plan
+    (4, 4, 20, 30, 25, 33, 0, 0.05, 16, False),     # 28 x 23 outputs, pad 0 (no shift)
+    (6, 6, 16, 26, 28, 24, 1, 0.05, 16, False),     # 26 x 28: the last row band half used
+    (2, 2, 600, 28, 28, 16, 1, 0.05, 8, False),     # many chunks, channel-split clusters
 ]
 
 
@@ -465,8 +481,8 @@ PAIR_IMG_CASES = [
 @pytest.mark.parametrize("case", PAIR_IMG_CASES, ids=[str(c) for c in PAIR_IMG_CASES])
 @pytest.mark.parametrize("integer", [False, True])
 def test_image_pair_column_blocks(case, integer):
-    N, hint, C, H, W, M, pad, d, ndense = case
-    rng = np.random.default_rng(abs(hash(case)) % (2 ** 32) + integer)
+    N, hint, C, H, W, M, pad, d, ndense, want_dense = case
+    rng = np.random.default_rng(abs(hash(case[:9])) % (2 ** 32) + integer)
     CRS = C * 9
     rows = [np.nonzero(rng.random(CRS) < (0.6 if m < ndense else d))[0] for m in range(M)]
     rowptr = np.concatenate([[0], np.cumsum([r.size for r in rows])]).astype(np.int32)
@@ -480,7 +496,7 @@ def test_image_pair_column_blocks(case, integer):
                       batch_hint=hint)
     info = w.info()
     assert info["col_blocks"] == 1 and info["tile_images"] == 2 and info["lane_rows"] == 4
-    assert info["dense_groups"] > 0
+    assert (info["dense_groups"] > 0) == want_dense
     w.close()
     got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 3, 3, 1, pad, batch_hint=hint)
     ref, mag = oracle.csr(x, rowptr, colidx, value, M, 3, 3, 1, pad)
