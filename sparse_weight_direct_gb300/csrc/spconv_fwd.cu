@@ -33,7 +33,9 @@ __global__ void wait_selftest_kernel(unsigned int *flags, unsigned long long lim
 KernelFn pick(int S, int stride, int P, int Q, int LR, bool pairs = false, bool plane = false,
               bool cols = false, int W = 0) {
     if (cols) {
-        if (S != 3 || stride != 1 || pairs || plane) return nullptr;
+        if (stride != 1 || plane) return nullptr;
+        if (LR == 4 && S == 5) return pick_colpair5(P, Q, pairs);
+        if (S != 3 || pairs) return nullptr;
         return LR == 4 ? pick_colpair(P, Q) : pick_cols(P, Q, LR);
     }
     if (pairs) return pick_pairs(S, stride, P, Q, LR);

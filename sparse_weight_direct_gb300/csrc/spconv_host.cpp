@@ -181,9 +181,12 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     // of the nonzeros (50 % sparse: 630 -> 584 us), and lost where sparse rows
     // dominate (90 %: 244 -> 250, 95 %: 117 -> 123, 99 %: 38.6 -> 46.1 us).
     // Taken when they cover at least 3 % fewer output positions and dense-tap
-    // rows hold at least three quarters of the nonzeros.
-    if (stride == 1 && R == 3 && S == 3 && tile_fmt && !g.col_blocks && g.lane_rows == 1 &&
-        g.F > 21 && g.F <= 28 && g.batch_hint >= 2 && dense_share >= 0.75) {
+    // rows hold at least three quarters of the nonzeros.  5x5 layers take them
+    // on the area alone: the 5x5 instances have no dense-tap path in this
+    // layout, and their sparse loop keeps its tap pairs.
+    const bool pair_kernel = (R == 3 && S == 3 && dense_share >= 0.75) || (R == 5 && S == 5);
+    if (stride == 1 && pair_kernel && tile_fmt && !g.col_blocks && g.lane_rows == 1 &&
+        g.F > 21 && g.F <= 28 && g.batch_hint >= 2) {
         const int64_t nb = g.batch_hint;
         const int64_t area = nb * g.tiles_y * g.tile_h * g.tiles_x * g.tile_w;
         const int64_t area_p = (nb + 1) / 2 * 2 * ((g.E + 3) / 4) * 4 * 28;
@@ -202,6 +205,12 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
             if (rp % 8 == 0) rp += 4;
             g.phase_pitch = rp;
             g.row_pitch = rp;
+            // A tensor copy puts the second image's sub-tile chunk x plane
+            // words after the first, which must be 16 mod 32 words: with 8
+            // staged rows (5x5) every plane is a multiple of 32, so stage a
+            // ninth row (read as zeros or ignored) when the rows are
+            // 16-byte aligned.  cp.async staging pads the gap instead.
+            if ((size_t)g.in_rows * rp % 32 == 0 && (W * sizeof(float)) % 16 == 0) ++g.in_rows;
         }
     }
     g.plane = g.in_rows * g.row_pitch;
@@ -493,19 +502,23 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
     // block per SM).
     const bool one_per_block =
         g.batch_hint > 0 && want_split > 1 && (int64_t)cap * want_split >= C;
-    // image pairs take only chunks with chunk * plane = 16 mod 32 words (see
-    // below): start from the first such chunk at or above the cap (a chunk
-    // past C reads zeros for the missing channels)
-    if (g.tile_images == 2)
+    // Image pairs: the second image's sub-tile starts pair_off words after the
+    // first, 16 mod 32 so that the two halves of a warp load from disjoint
+    // banks.  A tensor copy writes it right after the first (pair_off = chunk
+    // x plane), so with rows a tensor map can address only chunks with chunk x
+    // plane = 16 mod 32 qualify: start from the first such chunk at or above
+    // the cap (a chunk past C reads zeros for the missing channels).  cp.async
+    // staging places the second sub-tile itself: any chunk, the gap padded.
+    const bool tma_pairs = g.tile_images == 2 && (g.W * sizeof(float)) % 16 == 0;
+    if (tma_pairs)
         while (cap < 256 && (size_t)cap * g.plane % 32 != 16) ++cap;
     for (int chunk = cap; chunk >= 1; --chunk) {
         const int nch = (C + chunk - 1) / chunk;
         const size_t hdr_bytes = (size_t)g.hdr_words * 4;
-        // (image pairs: the second image's sub-tile follows the first's, as one
-        // tensor copy writes them, so chunk * plane must be 16 mod 32 words for
-        // the two halves of a warp to load from disjoint banks)
-        if (g.tile_images == 2 && (size_t)chunk * g.plane % 32 != 16) continue;
-        const size_t pair_off = g.tile_images == 2 ? (size_t)chunk * g.plane : 0;
+        if (tma_pairs && (size_t)chunk * g.plane % 32 != 16) continue;
+        const size_t pair_off =
+            g.tile_images == 2 ? (size_t)chunk * g.plane + (48 - (size_t)chunk * g.plane % 32) % 32
+                               : 0;
         const size_t in_stage = round_up(
             (pair_off + (size_t)chunk * g.plane +
              (g.plane_stage ? spconv::kPlaneLead + spconv::kPlaneTail : 0)) * sizeof(float),
@@ -557,9 +570,9 @@ int pair_index(int Q, int q1, int q2) { return q1 * Q - q1 * (q1 + 1) / 2 + (q2 
 void choose_tap_pairs(spconv::Geometry &g, const std::vector<int32_t> &group_flags,
                       const std::vector<std::vector<int64_t>> &order, const int32_t *colidx) {
     g.tap_pairs = 0;
-    if (g.format != SPCONV_FORMAT_F32 || g.plane_stage || g.col_blocks ||
+    if (g.format != SPCONV_FORMAT_F32 || g.plane_stage || (g.col_blocks && g.tile_images != 2) ||
         spconv::forward_variant_supported(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows,
-                                          true) != 0)
+                                          true, false, g.col_blocks != 0) != 0)
         return;
     int64_t pairs = 0, total = 0;
     std::vector<int32_t> cols;

@@ -605,10 +605,11 @@ constexpr int kModePairs = 2;
 constexpr int kModePlane = 3;  // plane staging (see apply_entry_plane)
 constexpr int kModeCols = 4;   // column blocks: a lane's P outputs run along a row
 constexpr int kModeColsPair = 5;  // column blocks over two images side by side
+constexpr int kModeColsPairTaps = 6;  // kModeColsPair with tap-pair segments
 template <int P, int Q, int S_CT, int ST_CT, int LR, int MODE = 0, int PLANE_RS = 0>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     spconv_fwd_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tmap) {
-    constexpr bool PAIRS = MODE == kModePairs;
+    constexpr bool PAIRS = MODE == kModePairs || MODE == kModeColsPairTaps;
     constexpr bool PLANE = MODE == kModePlane;
     // Column blocks (stride 1): lane (ly, lx) holds outputs (ly, lx*P + r) of
     // an LR x (LC*P) tile, so widths that are multiples of LC*P but not of 32
@@ -618,7 +619,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     // each lane seven consecutive outputs, so a 4 x 28 tile of each image
     // leaves no lane idle (28-wide outputs waste 4 of 32 lanes otherwise).
     // The stage holds the two images' sub-tiles pair_off words apart.
-    constexpr bool PAIR = MODE == kModeColsPair;
+    constexpr bool PAIR = MODE == kModeColsPair || MODE == kModeColsPairTaps;
     constexpr bool COLS = MODE == kModeCols || PAIR;
     static_assert(!COLS || ST_CT == 1, "column blocks: stride 1");
     static_assert(!PAIR || (LR == 4 && P == 7), "image-pair column blocks: 4 x (2 x 28)");
@@ -851,7 +852,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         const Span sp{reinterpret_cast<const float *>(base),
                       reinterpret_cast<const float *>(base + p.in_stage_bytes), p.err};
         const unsigned char *blob_end = base + p.stage_bytes;
-        if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4 && COLS) {
+        if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4 && COLS && S_CT == 3) {
             if (dense) {
                 const int k = k_begin + it;
                 run_dense_chunk_cols<P, Q, S_CT>(
@@ -1166,8 +1167,10 @@ KernelFn pick_pairs(int S, int stride, int P, int Q, int LR);
 // images (row step 28 words) have their own, with immediate load offsets.
 KernelFn pick_plane(int P, int Q, int W);
 KernelFn pick_cols(int P, int Q, int LR);
-// Image-pair column-block instances (3x3 stride 1, four lane rows of eight).
+// Image-pair column-block instances (3x3 stride 1, four lane rows of eight),
+// and those of 5x5 layers, with or without tap-pair segments.
 KernelFn pick_colpair(int P, int Q);
+KernelFn pick_colpair5(int P, int Q, bool pairs);
 
 // Instantiates the kernels of one Q for the supported kernel widths, strides,
 // rows per lane and lane rows.

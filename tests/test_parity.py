@@ -501,3 +501,43 @@ def test_image_pair_column_blocks(case, integer):
     got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 3, 3, 1, pad, batch_hint=hint)
     ref, mag = oracle.csr(x, rowptr, colidx, value, M, 3, 3, 1, pad)
     check(got, ref, mag, exact=integer, what=f"image pairs {case}")
+
+
+PAIR5_CASES = [
+    # (N run, N planned, C, H, W, M, pad, density, tap pairs, Q): 5x5 stride-1 layers 22..28
+    # outputs wide in image-pair column blocks.  Rows that a tensor map can address (W a
+    # multiple of 4) are staged by one tensor copy with a ninth staged row; the others by
+    # cp.async with the gap between the two images' sub-tiles padded to 16 mod 32 words.
+    (16, 16, 96, 27, 27, 256, 2, 0.2, 1, 4),  # the 5x5 layer's shape: tap pairs, 7 chunks
+    (9, 10, 48, 27, 27, 128, 2, 0.2, 1, 4),   # odd batch, tap pairs
+    (8, 8, 8, 28, 28, 300, 2, 0.25, 1, 4),    # tensor copies, tap pairs, chunk past C
+    (4, 4, 24, 28, 28, 64, 2, 0.2, 0, 2),     # tensor copies, two channels per warp
+    (3, 4, 16, 24, 24, 40, 2, 0.05, 0, 2),    # odd batch, tensor copies, 24 x 24
+    (2, 2, 40, 26, 26, 33, 1, 0.3, 0, 1),     # pad 1: 24 x 24 outputs, M not a multiple of 8
+    (5, 6, 12, 22, 22, 16, 2, 0.3, 0, 1),     # 22 x 22: each lane row's last lanes idle
+    (1, 4, 24, 27, 27, 64, 2, 0.2, 0, 2),     # one image on a pair plan
+    (16, 16, 64, 27, 27, 512, 2, 0.01, 0, 8), # eight channels per warp
+    (2, 2, 300, 28, 28, 24, 2, 0.1, 0, 1),    # many chunks, channel-split clusters
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", PAIR5_CASES, ids=[str(c) for c in PAIR5_CASES])
+@pytest.mark.parametrize("integer", [False, True])
+def test_image_pair_5x5(case, integer):
+    N, hint, C, H, W, M, pad, d, want_pairs, want_q = case
+    rng = np.random.default_rng(abs(hash(case[:8])) % (2 ** 32))
+    rowptr, colidx, value = workloads.random_csr(M, C * 25, d, rng, integer=integer)
+    x = workloads.random_input((N, C, H, W), rng, integer=integer)
+    w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=5, S=5, stride=1, pad=pad,
+                      batch_hint=hint)
+    info = w.info()
+    assert info["tile_images"] == 2 and info["lane_rows"] == 4 and info["col_blocks"] == 1
+    assert info["tap_pairs"] == want_pairs and info["slots_per_warp"] == want_q
+    assert info["pair_off"] % 32 == 16
+    if (W * 4) % 16 == 0:  # one tensor copy: the second sub-tile right after the first
+        assert info["pair_off"] == info["chunk"] * info["plane"]
+    w.close()
+    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 5, 5, 1, pad, batch_hint=hint)
+    ref, mag = oracle.csr(x, rowptr, colidx, value, M, 5, 5, 1, pad)
+    check(got, ref, mag, exact=integer, what=f"5x5 image pairs {case}")
