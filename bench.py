@@ -674,6 +674,92 @@ def time_dense_conv(L, rowptr, colidx, value, x, y, flush, stream, steps, graph)
     return out
 
 
+def run_timeline(args, L):
+    """Per-block timeline of the forward kernel: needs the trace build
+    (python sparse_weight_direct_gb300/build.py --trace, then
+    SPCONV_LIBRARY=sparse_weight_direct_gb300/libspconv_trace.so).  Warm-up
+    launches, then `steps` launches (at most 20), each after a 256 MiB L2 flush
+    and timed alone; prints one JSON line summarising the launch with the
+    median span: block durations by group kind, when each block's first stage
+    was ready, how many blocks ran at once over time, and the blocks per SM.
+    Not a benchmark line (the records cost a few stores per block)."""
+    import numpy as np
+    import torch
+    import sparse_weight_direct_gb300 as swd
+    from sparse_weight_direct_gb300 import _lib
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    rowptr, colidx, value = workloads.make_weights(L)
+    stream = torch.cuda.Stream(device=dev)
+    w = swd.pack(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
+                 stride=L.stride, pad=L.pad, stream=stream, fmt=args.fmt, batch_hint=L.N)
+    launch = w.launch_info(L.N)
+    nb = launch["grid_x"] * launch["grid_y"]
+    x = torch.from_numpy(workloads.make_input(L)).to(dev)
+    y = torch.empty((L.N, L.M, L.E, L.F), device=dev, dtype=torch.float32)
+    flush = torch.empty(64 << 20, device=dev, dtype=torch.float32)
+    buf = np.zeros(min(nb, 65536) * 4, dtype=np.uint64)
+    lib = _lib.lib()
+    runs = []
+    for i in range(args.warmup + min(args.steps, 20)):
+        flush.zero_()
+        torch.cuda.synchronize()
+        swd.forward(x, w, out=y, stream=stream)
+        torch.cuda.synchronize()
+        rc = lib.spconv_trace_read(buf.ctypes.data, buf.nbytes)
+        if rc == _lib.SPCONV_ERR_UNSUPPORTED:
+            print(json.dumps({"timeline": L.name, "error": "not the trace build: run "
+                              "`python sparse_weight_direct_gb300/build.py --trace` and set "
+                              "SPCONV_LIBRARY=sparse_weight_direct_gb300/libspconv_trace.so"}))
+            return 1
+        _lib.check(rc, "spconv_trace_read")
+        if i >= args.warmup:
+            runs.append(buf.reshape(-1, 4).astype(np.int64).copy())
+    assert w.device_status(stream) == 0
+    w.close()
+    spans = [(r[:, 2].max() - r[:, 0].min()) / 1e3 for r in runs]
+    rec = runs[int(np.argsort(spans)[len(spans) // 2])]
+    t0 = rec[:, 0].min()
+    start, end = (rec[:, 0] - t0) / 1e3, (rec[:, 2] - t0) / 1e3
+    ready = (rec[:, 1] - rec[:, 0]) / 1e3
+    dur = end - start
+    sm = rec[:, 3] & 0xFFFF
+    flags = (rec[:, 3] >> 32) & 0xFF
+    span = float(end.max())
+    step = max(span / 20.0, 1e-3)
+    ticks = np.arange(0.0, span, step)
+    running = [int(((start <= t) & (end > t)).sum()) for t in ticks]
+    peak = max(running) if running else 0
+    half = next((float(t) for t, n in zip(ticks[1:], running[1:]) if n < peak / 2), span)
+
+    def stats(a):
+        return [round(float(a.min()), 2), round(float(np.median(a)), 2), round(float(a.max()), 2)]
+
+    kinds = {}
+    for name, m in (("dense", (flags & 1) != 0), ("split", (flags & 3) == 2),
+                    ("sparse", (flags & 3) == 0)):
+        if m.any():
+            kinds[name] = {"blocks": int(m.sum()), "us_min_med_max": stats(dur[m]),
+                           "end_max_us": round(float(end[m].max()), 2)}
+    per_sm = np.bincount(sm, minlength=int(sm.max()) + 1)
+    per_sm = per_sm[per_sm > 0]
+    print(json.dumps({
+        "timeline": L.name, "launches": len(runs), "blocks": int(nb),
+        "grid": [launch["grid_x"], launch["grid_y"]], "cluster": launch["cluster"],
+        "span_us": round(span, 2), "span_us_all_launches": [round(float(v), 2) for v in spans],
+        "block_us_min_med_max": stats(dur), "by_kind": kinds,
+        "first_stage_ready_us_med_max": [round(float(np.median(ready)), 2),
+                                         round(float(ready.max()), 2)],
+        "peak_running_blocks": peak,
+        "ideal_span_us": round(float(dur.sum()) / max(peak, 1), 2),
+        "below_half_peak_from_us": round(half, 2),
+        "running_blocks_every_us": round(step, 2), "running_blocks": running,
+        "blocks_per_sm_min_max": [int(per_sm.min()), int(per_sm.max())],
+        "sms_used": int(per_sm.size)}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -700,6 +786,9 @@ def main(argv=None):
                     help="steps per layer of the `layers` record (default: max(steps, 20))")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline leg")
+    ap.add_argument("--timeline", action="store_true",
+                    help="per-block timeline of the forward kernel (trace build only; "
+                         "see run_timeline)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.layer_steps <= 0:
@@ -707,6 +796,8 @@ def main(argv=None):
     L = workloads.ALL_LAYERS[args.config]
     if args.impl == "reference":
         return run_reference(args, L)
+    if args.timeline:
+        return run_timeline(args, L)
     return run_ours(args, L)
 
 

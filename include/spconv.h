@@ -262,6 +262,20 @@ int spconv_device_status(const spconv_packed *p, void *stream, int32_t *flags);
  */
 int spconv_selftest_wait(int complete, void *stream, int32_t *flags);
 
+/*
+ * spconv_trace_read -- the per-block timeline of the last spconv_forward /
+ * spconv_forward_ex launch on the current device, recorded only by the trace
+ * build libspconv_trace.so (the same sources compiled with -DSPCONV_TRACE=1);
+ * no counterpart in the pages, a diagnostic of this library.  Copies up to
+ * `bytes` to host_dst: 4 x uint64 per block in launch order (linear block
+ * index y * grid_x + x, the first 65536 blocks): start, first stage ready,
+ * end of the chunk pipeline (global-timer ns; 0 = not reached), and
+ * smid | group << 16 | group flags << 32.  Synchronises the device.  Errors:
+ * INVALID_ARG (NULL or negative size), UNSUPPORTED (not the trace build),
+ * CUDA.
+ */
+int spconv_trace_read(void *host_dst, int64_t bytes);
+
 /* Geometry and sizes of a packed handle (all counts are plain integers). */
 typedef struct spconv_packed_info {
     int32_t C, H, W, M, R, S, stride, pad, E, F;

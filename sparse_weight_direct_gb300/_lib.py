@@ -12,7 +12,8 @@ import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 # SPCONV_LIBRARY selects another build of the same library (the bounds-checked
-# libspconv_debug.so); the default is the in-tree libspconv.so.
+# libspconv_debug.so, the trace build libspconv_trace.so); the default is the
+# in-tree libspconv.so.
 LIB_PATH = os.environ.get("SPCONV_LIBRARY") or os.path.join(HERE, "libspconv.so")
 
 SPCONV_OK = 0
@@ -29,7 +30,8 @@ EXPORTS = ("spconv_pack", "spconv_pack_ex", "spconv_forward", "spconv_forward_ex
            "spconv_forward_host", "spconv_forward_host_noalloc", "spconv_packed_free",
            "spconv_status_string",
            "spconv_pack_host", "spconv_device_status", "spconv_selftest_wait",
-           "spconv_packed_info_get", "spconv_launch_info_get", "spconv_packed_copy_array")
+           "spconv_packed_info_get", "spconv_launch_info_get", "spconv_packed_copy_array",
+           "spconv_trace_read")
 
 _lock = threading.Lock()
 _lib = None
@@ -106,6 +108,8 @@ def lib() -> ctypes.CDLL:
         L.spconv_device_status.restype = i
         L.spconv_selftest_wait.argtypes = [i, p, ctypes.POINTER(ctypes.c_int32)]
         L.spconv_selftest_wait.restype = i
+        L.spconv_trace_read.argtypes = [p, ctypes.c_int64]
+        L.spconv_trace_read.restype = i
         _lib = L
         return L
 

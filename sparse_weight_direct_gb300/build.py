@@ -10,6 +10,10 @@ same sources with -DSPCONV_DEBUG=1, objects in _build_debug/): every kernel
 access is checked against its extent first and a failed check sets bit 2 of
 the device error word instead of touching memory.  Point the Python binding
 at it with SPCONV_LIBRARY=<path>.
+
+build(trace=True) builds libspconv_trace.so (-DSPCONV_TRACE=1, objects in
+_build_trace/): every forward block records its start, first-stage-ready and
+pipeline-end times, read back with spconv_trace_read (bench.py --timeline).
 """
 from __future__ import annotations
 
@@ -25,6 +29,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspconv.so")
 BUILD_DEBUG = os.path.join(HERE, "_build_debug")
 LIB_DEBUG = os.path.join(HERE, "libspconv_debug.so")
+BUILD_TRACE = os.path.join(HERE, "_build_trace")
+LIB_TRACE = os.path.join(HERE, "libspconv_trace.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["spconv_fwd.cu", "spconv_fwd_q1.cu", "spconv_fwd_q2.cu", "spconv_fwd_q4.cu",
            "spconv_fwd_q8.cu", "spconv_fwd_pairs.cu", "spconv_fwd_plane.cu", "spconv_fwd_cols.cu",
@@ -55,14 +61,20 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
-    bdir, lib_path = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False,
+          trace: bool = False) -> str:
+    if debug and trace:
+        raise ValueError("the bounds-checked and trace builds are separate libraries")
+    bdir, lib_path = ((BUILD_DEBUG, LIB_DEBUG) if debug else
+                      (BUILD_TRACE, LIB_TRACE) if trace else (BUILD, LIB))
     os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     common = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-I", os.path.join(ROOT, "include"),
               "-Xcompiler", "-fPIC,-fvisibility=hidden,-O3,-Wall", *extra_flags]
     if debug:
         common.append("-DSPCONV_DEBUG=1")
+    if trace:
+        common.append("-DSPCONV_TRACE=1")
     objs, procs = [], []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
@@ -94,4 +106,4 @@ def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: boo
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                debug="--debug" in sys.argv))
+                debug="--debug" in sys.argv, trace="--trace" in sys.argv))

@@ -76,6 +76,45 @@ cudaError_t raise_smem_limit(const void *fn) {
 
 using namespace kern;
 
+#ifdef SPCONV_TRACE
+// Trace build: one record buffer per device, allocated on first use.
+static unsigned long long *trace_buffer() {
+    constexpr int kMaxDev = 64;
+    static std::mutex lock;
+    static unsigned long long *bufs[kMaxDev] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+    std::lock_guard<std::mutex> lk(lock);
+    if (!bufs[dev]) {
+        void *ptr = nullptr;
+        if (cudaMalloc(&ptr, (size_t)kTraceBlocks * 4 * sizeof(unsigned long long)) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        bufs[dev] = static_cast<unsigned long long *>(ptr);
+    }
+    return bufs[dev];
+}
+#endif
+
+int trace_read(void *dst, int64_t bytes) {
+#ifdef SPCONV_TRACE
+    unsigned long long *b = trace_buffer();
+    if (!b) return -5;
+    const size_t cap = (size_t)kTraceBlocks * 4 * sizeof(unsigned long long);
+    const size_t n = bytes < 0 ? 0 : ((size_t)bytes < cap ? (size_t)bytes : cap);
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpy(dst, b, n, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return -5;
+    }
+    return 0;
+#else
+    (void)dst;
+    (void)bytes;
+    return -3;
+#endif
+}
+
 cudaError_t launch_wait_selftest(unsigned int *flags, int arrive, cudaStream_t stream) {
     wait_selftest_kernel<<<1, 32, 0, stream>>>(flags, 20000000ull /* 20 ms */, arrive);
     return cudaGetLastError();
@@ -183,6 +222,11 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
     p.num_slots = g.num_slots;
     p.smem_bytes = (int)smem;
     p.blob_bytes = d.blob_bytes;
+    p.trace = nullptr;
+#ifdef SPCONV_TRACE
+    p.trace = trace_buffer();
+    if (p.trace) cudaMemsetAsync(p.trace, 0, (size_t)kTraceBlocks * 4 * sizeof(unsigned long long), stream);
+#endif
     CUtensorMap dummy;
     if (!tmap) {
         for (int i = 0; i < 16; ++i) dummy.opaque[i] = 0;

@@ -1345,6 +1345,11 @@ __attribute__((visibility("default"))) int spconv_device_status(const spconv_pac
     return word ? SPCONV_ERR_DEVICE : SPCONV_OK;
 }
 
+__attribute__((visibility("default"))) int spconv_trace_read(void *host_dst, int64_t bytes) {
+    if (!host_dst || bytes < 0) return SPCONV_ERR_INVALID_ARG;
+    return spconv::trace_read(host_dst, bytes);
+}
+
 __attribute__((visibility("default"))) int spconv_selftest_wait(int complete, void *stream,
                                                                 int32_t *flags) {
     if (!flags) return SPCONV_ERR_INVALID_ARG;

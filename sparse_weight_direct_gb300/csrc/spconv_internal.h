@@ -132,6 +132,12 @@ constexpr int kPlaneTail = 48;
 // start on 16-byte boundaries (H W a multiple of 4).
 bool plane_stage_supported(int H, int W, int R, int S, int stride, int pad, int P, int LR, int Q);
 
+// Trace build (-DSPCONV_TRACE=1): copies up to `bytes` of the current
+// device's per-block records of the last forward launch to host memory
+// (synchronises the device).  0 on success, -3 in other builds, -5 on a CUDA
+// error.
+int trace_read(void *dst, int64_t bytes);
+
 // Whether a layer shape can use the dense-tap path (output channels with dense
 // rows get their K x K blocks applied from a register window).
 bool dense_taps_supported(int R, int S, int stride, int LR, int Q);

@@ -85,6 +85,7 @@ struct KParams {
     int num_slots;           // entries of slot_oc / slot_next (bounds-checked build)
     int smem_bytes;          // dynamic shared memory of the launch (bounds-checked build)
     int64_t blob_bytes;      // bytes of the blobs array (bounds-checked build)
+    unsigned long long *trace;  // trace build: kTraceBlocks records of 4 words, else nullptr
 };
 
 // ---------------------------------------------------------------- bounds-checked build
@@ -102,6 +103,21 @@ constexpr bool kDebug = true;
 #else
 constexpr bool kDebug = false;
 #endif
+
+// ---------------------------------------------------------------- trace build
+//
+// Compiled with -DSPCONV_TRACE=1 (libspconv_trace.so), every block of the
+// forward kernel records four words in p.trace[block * 4 ..]: its start, the
+// moment its first stage became ready (thread 0), the end of its pipeline
+// (all warps out of the chunk loop), each a global-timer value in ns, and
+// smid | group << 16 | group flags << 32.  The default build compiles the
+// records away.
+#ifdef SPCONV_TRACE
+constexpr bool kTrace = true;
+#else
+constexpr bool kTrace = false;
+#endif
+constexpr int kTraceBlocks = 65536;  // records kept per launch
 
 // [lo, hi) of the staged input of the current stage, and the error word.
 struct Span {
@@ -670,6 +686,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     const int n_out = PAIR ? img0 + (lx >= LC / 2 ? 1 : 0) : n;
     const int nmine = k_end - k_begin;
     const int nslot = kWarps * Q;
+    const unsigned int tr_block = blockIdx.y * gridDim.x + blockIdx.x;
+    const bool tr_on = kTrace && p.trace != nullptr && tr_block < (unsigned)kTraceBlocks;
+    unsigned long long tr_start = 0;
+    if (tr_on && threadIdx.x == 0) tr_start = global_ns();
 
     // Barrier set-up first: its release fence would otherwise wait for the
     // global loads below (a whole memory round trip before the first copy).
@@ -836,6 +856,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             failed = __syncthreads_or(!ok) != 0;  // cp.async data of all threads
         }
         if (failed) break;
+        if (tr_on && it == 0 && threadIdx.x == 0) p.trace[(size_t)tr_block * 4 + 1] = global_ns();
         const unsigned char *base = smem + (size_t)s * p.stage_bytes;
         const float *sb = reinterpret_cast<const float *>(base) + ly * st * p.row_pitch +
                           (PAIR ? (lx >= LC / 2 ? p.pair_off : 0) + (lx % (LC / 2)) * P
@@ -935,6 +956,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     // drain that runs out too is recorded apart (bit 1): a copy may then still
     // be writing into shared memory that the SM's next block will own.
     failed = __syncthreads_or(failed) != 0;
+    if (tr_on && threadIdx.x == 0) {
+        unsigned int smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        p.trace[(size_t)tr_block * 4 + 0] = tr_start;
+        p.trace[(size_t)tr_block * 4 + 2] = global_ns();
+        p.trace[(size_t)tr_block * 4 + 3] = (unsigned long long)smid |
+                                            ((unsigned long long)group << 16) |
+                                            ((unsigned long long)(gflags & 0xff) << 32);
+    }
     if (failed) {
         if (!p.use_tma && !PLANE) cp_async_wait_all();
         if (threadIdx.x == 0) {
