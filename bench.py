@@ -720,6 +720,8 @@ def run_timeline(args, L):
     w.close()
     spans = [(r[:, 2].max() - r[:, 0].min()) / 1e3 for r in runs]
     rec = runs[int(np.argsort(spans)[len(spans) // 2])]
+    if args.timeline_out:  # the raw records of that launch (uint64, blocks x 4)
+        np.save(args.timeline_out, rec.astype(np.uint64))
     t0 = rec[:, 0].min()
     start, end = (rec[:, 0] - t0) / 1e3, (rec[:, 2] - t0) / 1e3
     ready = (rec[:, 1] - rec[:, 0]) / 1e3
@@ -789,6 +791,9 @@ def main(argv=None):
     ap.add_argument("--timeline", action="store_true",
                     help="per-block timeline of the forward kernel (trace build only; "
                          "see run_timeline)")
+    ap.add_argument("--timeline-out", default="",
+                    help="with --timeline: also save the median launch's raw records "
+                         "(.npy, blocks x 4 uint64)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     if args.layer_steps <= 0:

@@ -642,10 +642,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     static_assert(!PLANE || (S_CT == 3 && ST_CT == 1 && LR == 2), "plane staging: 3x3, two lane rows");
     static_assert(PLANE || PLANE_RS == 0, "a fixed row step is a plane-staging instance");
     static_assert(!PAIRS || Q == 2 || Q == 4, "tap pairs: 2 or 4 output channels per warp");
+    static_assert(Q <= 8, "at most eight output channels per warp (the slot table in shared memory)");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar[2];
     __shared__ int stage_done[2];  // warps that have released a stage (TMA path)
     __shared__ int issued[2];      // copy phases issued into each stage
+    // One-block tiles: the group's slot table (output channel and next part
+    // of each slot) for the write-back, so that its lookups cost no global
+    // round trips (one per slot and per link of a split row otherwise).
+    __shared__ int oc_sh[kWarps * 8], next_sh[kWarps * 8];
     // stage buffers start on a 128-byte boundary (TMA destination)
     unsigned char *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     constexpr int LC = kLanes / LR;  // lanes per lane row = output columns of a tile
@@ -743,6 +748,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         pre_m = slot_oc_at(p, group * nslot + item0_slot);
         pre_next = slot_next_at(p, group * nslot + item0_slot);
     }
+    // (the last warp copies the slot table while the first stage is in
+    // flight; the barrier after the pipeline publishes it)
+    if (split == 1 && warp == kWarps - 1)
+        for (int i = lane; i < nslot; i += 32) {
+            oc_sh[i] = slot_oc_at(p, group * nslot + i);
+            next_sh[i] = slot_next_at(p, group * nslot + i);
+        }
     // Push-mode cluster reduction: this block announces that it is running;
     // the matching wait comes before its first store into another block.
     const bool push = split > 1 && p.push;
@@ -977,7 +989,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         __syncthreads();
     }
 
-    const int slot0 = group * nslot + warp * Q;
     // (bounds-checked build) end of the launch's dynamic shared memory
     const unsigned char *smem_end = smem_raw + p.smem_bytes;
     // This lane's outputs r = 0 .. P-1: rows oy0 + LR * r of column ox, or
@@ -1008,7 +1019,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
             __syncwarp();
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
-                const int m = q == 0 ? pre_m : slot_oc_at(p, slot0 + q);
+                const int m = oc_sh[warp * Q + q];
                 if (m < 0) continue;
 #pragma unroll
                 for (int i = 0; i < P; ++i) {
@@ -1033,7 +1044,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (failed || !lane_out) return;
 #pragma unroll
         for (int q = 0; q < Q; ++q) {
-            const int m = q == 0 ? pre_m : slot_oc_at(p, slot0 + q);
+            const int m = oc_sh[warp * Q + q];
             if (m < 0) continue;
             float *yo = p.y + ((size_t)n_out * p.M + m) * p.E * p.F;
 #pragma unroll
@@ -1117,14 +1128,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (failed || !lane_out) return;
         for (int q = 0; q < Q; ++q) {
             const int sl = warp * Q + q;
-            const int m = q == 0 ? pre_m : slot_oc_at(p, group * nslot + sl);
+            const int m = oc_sh[sl];
             if (m < 0) continue;
-            const int next0 = q == 0 ? pre_next : slot_next_at(p, group * nslot + sl);
+            const int next0 = next_sh[sl];
             float *yo = p.y + ((size_t)n_out * p.M + m) * p.E * p.F;
             for (int r = 0; r < P; ++r) {
                 float sum = part[(sl * P + r) * 32 + lane];
-                for (int c = next0; c >= 0 && dbg_ok(c < nslot, p.err);
-                     c = slot_next_at(p, group * nslot + c))
+                for (int c = next0; c >= 0 && dbg_ok(c < nslot, p.err); c = next_sh[c])
                     sum += part[(c * P + r) * 32 + lane];
                 if (out_ok(r) && dbg_ok(m < p.M, p.err)) yo[out_at(r)] = finish(p, m, sum);
             }
