@@ -64,7 +64,8 @@ KERNEL_SOURCES = {
         "spconv_kernel.cuh", "spconv_fwd.cu", "spconv_fwd_q1.cu", "spconv_fwd_q2.cu",
         "spconv_fwd_q4.cu", "spconv_fwd_q8.cu", "spconv_fwd_pairs.cu",
         "spconv_fwd_plane.cu", "spconv_fwd_cols.cu", "spconv_fwd_colpair.cu",
-        "spconv_fwd_colpair5.cu", "spconv_host.cpp", "spconv_internal.h")],
+        "spconv_fwd_colpair5.cu", "spconv_fwd_tight.cu", "spconv_host.cpp",
+        "spconv_internal.h")],
     "spconv_ws_kernel": [os.path.join(_CSRC, f) for f in (
         "spconv_kernel.cuh", "spconv_ws.cu", "spconv_host.cpp", "spconv_internal.h")],
 }

@@ -34,7 +34,7 @@ LIB_TRACE = os.path.join(HERE, "libspconv_trace.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["spconv_fwd.cu", "spconv_fwd_q1.cu", "spconv_fwd_q2.cu", "spconv_fwd_q4.cu",
            "spconv_fwd_q8.cu", "spconv_fwd_pairs.cu", "spconv_fwd_plane.cu", "spconv_fwd_cols.cu",
-           "spconv_fwd_colpair.cu", "spconv_fwd_colpair5.cu",
+           "spconv_fwd_colpair.cu", "spconv_fwd_colpair5.cu", "spconv_fwd_tight.cu",
            "spconv_ws.cu", "spconv_io.cu", "spconv_noalloc.cu", "spconv_host.cpp"]
 HEADERS = [os.path.join(CSRC, "spconv_internal.h"), os.path.join(CSRC, "spconv_kernel.cuh"),
            os.path.join(ROOT, "include", "spconv.h")]

@@ -31,7 +31,10 @@ __global__ void wait_selftest_kernel(unsigned int *flags, unsigned long long lim
 }
 
 KernelFn pick(int S, int stride, int P, int Q, int LR, bool pairs = false, bool plane = false,
-              bool cols = false, int W = 0) {
+              bool cols = false, int W = 0, bool tight = false) {
+    if (tight)
+        return (S == 3 && stride == 1 && LR == 1 && !pairs && !plane && !cols) ? pick_tight(P, Q)
+                                                                                : nullptr;
     if (cols) {
         if (stride != 1 || plane) return nullptr;
         if (LR == 4 && S == 5) return pick_colpair5(P, Q, pairs);
@@ -125,8 +128,8 @@ bool dense_taps_supported(int R, int S, int stride, int LR, int Q) {
 }
 
 int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool pairs, bool plane,
-                              bool cols) {
-    return pick(S, stride, P, Q, LR, pairs, plane, cols) ? 0 : -1;
+                              bool cols, bool tight) {
+    return pick(S, stride, P, Q, LR, pairs, plane, cols, 0, tight) ? 0 : -1;
 }
 
 bool plane_stage_supported(int H, int W, int R, int S, int stride, int pad, int P, int LR, int Q) {
@@ -181,9 +184,11 @@ cudaError_t launch_forward(const Geometry &g, int N, int split, bool group_fast,
                            const float *x, float *y, const float *bias, int act,
                            const DeviceArrays &d, const CUtensorMap *tmap, cudaStream_t stream) {
     KernelFn fn = pick(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows, g.tap_pairs != 0,
-                       g.plane_stage != 0, g.col_blocks != 0, g.W);
+                       g.plane_stage != 0, g.col_blocks != 0, g.W, g.tight != 0);
     if (!fn || split < 1 || split > kMaxSplit || split > g.num_chunks)
         return cudaErrorInvalidConfiguration;
+    // tight-pitch tiles have no cp.async path: their tensor map is required
+    if (g.tight && !tmap) return cudaErrorInvalidConfiguration;
     const size_t smem = forward_smem_bytes(g, split);
     if (smem > 48 * 1024) {
         cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(fn));

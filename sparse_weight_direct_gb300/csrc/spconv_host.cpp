@@ -146,6 +146,7 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     // staged row pitch is 4 mod 8 words, so the 32 lanes' first inputs
     // (ly * pitch + 7 lx) fall in distinct banks.
     g.col_blocks = 0;
+    g.tight = 0;
     g.tile_images = 1;
     g.pair_off = 0;
     const bool tile_fmt = g.format == SPCONV_FORMAT_F32 || g.format == SPCONV_FORMAT_PACKED32;
@@ -250,6 +251,25 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
     if (spconv::forward_variant_supported(S, stride, g.tile_rows, g.slots, g.lane_rows, false, false,
                                           g.col_blocks != 0) != 0)
         return SPCONV_ERR_UNSUPPORTED;
+    // Tight pitch (3x3, pad 1, one lane row, the whole width in one tile
+    // column, rows a tensor copy can address, 16-byte-aligned widths up to
+    // 31): the copy starts at column 0 with a 32-word pitch; the columns past
+    // the image arrive as zeros and stand in for the right halo, and the left
+    // halo of row r is the last (zero) column of row r - 1 (a lead of zeroed
+    // words before the tile covers the first row).  9 x 32 words per channel
+    // against 9 x 40 for the padded tile: the chunks hold a quarter more
+    // channels.
+    if (stride == 1 && R == 3 && S == 3 && pad == 1 && tile_fmt && !g.col_blocks &&
+        g.lane_rows == 1 && g.tiles_x == 1 && W % 4 == 0 && W <= 31 &&
+        spconv::forward_variant_supported(S, stride, g.tile_rows, g.slots, g.lane_rows, false,
+                                          false, false, true) == 0) {
+        g.tight = 1;
+        g.shift = -1;
+        g.in_cols = 32;
+        g.phase_pitch = 32;
+        g.row_pitch = 32;
+        g.plane = g.in_rows * g.row_pitch;
+    }
     // Whole-image tiles of images whose rows TMA cannot address: one bulk copy
     // of the chunk's raw planes (dense, pitch W) instead of per-element
     // cp.async into a padded tile; the kernel applies the padding to the
@@ -521,7 +541,8 @@ int plan_chunks(spconv::Geometry &g, const std::vector<int64_t> &gpre) {
                                : 0;
         const size_t in_stage = round_up(
             (pair_off + (size_t)chunk * g.plane +
-             (g.plane_stage ? spconv::kPlaneLead + spconv::kPlaneTail : 0)) * sizeof(float),
+             (g.plane_stage ? spconv::kPlaneLead + spconv::kPlaneTail : 0) +
+             (g.tight ? spconv::kTightLeadWords + spconv::kTightTailWords : 0)) * sizeof(float),
             128);
         size_t blob_max = g.dense_groups ? dense_blob_bytes(g, chunk) : 0;
         for (int grp = g.dense_groups; grp < g.groups; ++grp) {
@@ -572,7 +593,7 @@ void choose_tap_pairs(spconv::Geometry &g, const std::vector<int32_t> &group_fla
     g.tap_pairs = 0;
     if (g.format != SPCONV_FORMAT_F32 || g.plane_stage || (g.col_blocks && g.tile_images != 2) ||
         spconv::forward_variant_supported(g.S, g.stride, g.tile_rows, g.slots, g.lane_rows,
-                                          true, false, g.col_blocks != 0) != 0)
+                                          true, false, g.col_blocks != 0, g.tight != 0) != 0)
         return;
     int64_t pairs = 0, total = 0;
     std::vector<int32_t> cols;

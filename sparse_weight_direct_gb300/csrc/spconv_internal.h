@@ -91,6 +91,8 @@ struct Geometry {
     int col_blocks;   // 1: column blocks -- lane_rows lane rows of 32 / lane_rows
                       // lanes, each lane holding tile_rows consecutive outputs of
                       // its row (stride 1, widths a multiple of 28, not of 32)
+    int tight;        // 1: tight-pitch tiles (a 32-word pitch from column 0, shift -1,
+                      // kTightLead zeroed words before each stage's tile)
     int tile_images;  // images side by side in a tile: 2 for image-pair column
                       // blocks (then N counts pairs in the grid), else 1
     int pair_off;     // image pairs: words from a stage's first sub-tile to its
@@ -119,7 +121,14 @@ struct DeviceArrays {
 // has an instance (pairs: with tap-pair segments; plane: with plane staging;
 // cols: with column blocks), else -1.
 int forward_variant_supported(int S, int stride, int P, int Q, int LR, bool pairs = false,
-                              bool plane = false, bool cols = false);
+                              bool plane = false, bool cols = false, bool tight = false);
+
+// Tight-pitch tiles: zeroed words before each stage's tile (kTightLead in the
+// kernel; the copy's destination stays 128-byte aligned), and words after it
+// (the right tap of the last lanes -- past the image, outputs discarded --
+// reaches one word beyond the last row of the last channel).
+constexpr int kTightLeadWords = 32;
+constexpr int kTightTailWords = 32;
 
 // Plane staging: zeroed words before and after the raw planes of a stage, so
 // that taps reaching past the first or last plane read finite values.

@@ -611,6 +611,15 @@ static __device__ __forceinline__ void run_segment_words(float (&acc)[P], const 
     for (; j < j1; ++j) apply_word<P, ROW_STEP, ST_CT>(acc, sb, ent[j], p, row_step, sp);  // tail
 }
 
+// Tight-pitch tiles (3x3, pad 1, one lane row, images up to 31 wide in one
+// tile column): the tensor copy starts at column 0 with a 32-word pitch, so
+// the columns past the image arrive as the copy's zero fill and a tap left of
+// column 0 reads the previous row's last column -- a zero -- instead of a
+// staged halo column: 9 x 32 words per channel against the padded tile's
+// 9 x 40, so the chunks hold a quarter more channels.  The stage keeps
+// kTightLead zeroed words before the tile for the first row's left tap.
+constexpr int kTightLead = kTightLeadWords;  // 128 bytes: the copy's destination stays aligned
+
 // P: output rows per lane; Q: output channels per warp; LR: lane rows (1, or 2
 // interleaved half-warps of 16 lanes for outputs at most 16 wide); S_CT/ST_CT:
 // kernel width and stride when known at compile time (0 = read from p); MODE:
@@ -640,7 +649,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     static_assert(!COLS || ST_CT == 1, "column blocks: stride 1");
     static_assert(!PAIR || (LR == 4 && P == 7), "image-pair column blocks: 4 x (2 x 28)");
     static_assert(!PLANE || (S_CT == 3 && ST_CT == 1 && LR == 2), "plane staging: 3x3, two lane rows");
-    static_assert(PLANE || PLANE_RS == 0, "a fixed row step is a plane-staging instance");
+    // (MODE 0 with PLANE_RS: the tight-pitch tiles, PLANE_RS their row pitch)
+    constexpr bool TIGHT = MODE == 0 && PLANE_RS != 0;
+    constexpr int LEAD = TIGHT ? kTightLead : 0;
+    static_assert(PLANE || TIGHT || PLANE_RS == 0, "a fixed row step is a plane-staging instance");
+    static_assert(!TIGHT || (S_CT == 3 && ST_CT == 1 && LR == 1), "tight pitch: 3x3, one lane row");
     static_assert(!PAIRS || Q == 2 || Q == 4, "tap pairs: 2 or 4 output channels per warp");
     static_assert(Q <= 8, "at most eight output channels per warp (the slot table in shared memory)");
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -656,6 +669,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     constexpr int LC = kLanes / LR;  // lanes per lane row = output columns of a tile
     constexpr int ROW_STEP =
         COLS ? 1
+             : TIGHT ? PLANE_RS
              : (S_CT && !PLANE) ? LR * (ST_CT == 1 ? row_pitch_s1(S_CT, LR)
                                                    : ST_CT * ST_CT * phase_pitch_for(S_CT, ST_CT))
                                 : 0;
@@ -707,6 +721,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         issued[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    }
+    if constexpr (TIGHT) {
+        // the lead words of the block's stages (read by the first row's left
+        // taps; a block of one chunk has one stage)
+        for (int i = threadIdx.x; i < (nmine > 1 ? 2 : 1) * LEAD; i += blockDim.x)
+            reinterpret_cast<float *>(smem + (size_t)(i / LEAD) * p.stage_bytes)[i % LEAD] = 0.f;
     }
     if constexpr (PLANE) {
         // stage input regions start zeroed: the margins (and a last, partial
@@ -770,7 +790,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     auto input_fits = [&](int c0) {
         const size_t in_bytes =
             PLANE ? kPlaneLead * sizeof(float) + (size_t)min(p.chunk, p.C - c0) * p.H * p.W * 4u
-                  : (p.use_tma ? (size_t)p.in_tma_bytes : 0u);
+                  : (p.use_tma ? (size_t)p.in_tma_bytes + LEAD * sizeof(float) : 0u);
         return !kDebug || in_bytes <= (size_t)p.in_stage_bytes;
     };
     auto issue = [&](int k, int s, bool issuer, bool weights, bool input) {
@@ -820,7 +840,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         // words after the first -- one 128-byte aligned destination; an image
         // past the batch reads as zeros)
         if (issuer && input && p.use_tma && in_fits)
-            tma_load_4d(base, &tmap, ix0 - p.shift, iy0, c0, img0, &bar[s]);
+            tma_load_4d(base + LEAD * sizeof(float), &tmap, ix0 - p.shift, iy0, c0, img0, &bar[s]);
         if (input && !p.use_tma) {
             for (int h = 0; h < (PAIR && img1 < p.N ? 2 : 1); ++h) {
                 float *dst = reinterpret_cast<float *>(base) + h * p.pair_off;
@@ -870,7 +890,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (failed) break;
         if (tr_on && it == 0 && threadIdx.x == 0) p.trace[(size_t)tr_block * 4 + 1] = global_ns();
         const unsigned char *base = smem + (size_t)s * p.stage_bytes;
-        const float *sb = reinterpret_cast<const float *>(base) + ly * st * p.row_pitch +
+        const float *sb = reinterpret_cast<const float *>(base) + LEAD + ly * st * p.row_pitch +
                           (PAIR ? (lx >= LC / 2 ? p.pair_off : 0) + (lx % (LC / 2)) * P
                                 : COLS ? lx * P : lx);
         if constexpr (PLANE) {
@@ -897,7 +917,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if constexpr (kDenseTaps<S_CT, ST_CT> && Q <= 4 && !PLANE && !COLS) {
             if (dense) {
                 const int k = k_begin + it;
-                run_dense_chunk<P, Q, S_CT, LR, row_pitch_s1(S_CT, LR)>(
+                run_dense_chunk<P, Q, S_CT, LR, (TIGHT ? PLANE_RS : row_pitch_s1(S_CT, LR))>(
                     acc, sb + p.shift, hdr, reinterpret_cast<const float4 *>(hdr + p.dense_mask_words),
                     warp, p.chunk, min(p.chunk, p.C - k * p.chunk), p.plane, sp, blob_end);
             }
@@ -1211,6 +1231,8 @@ KernelFn pick_cols(int P, int Q, int LR);
 // and those of 5x5 layers, with or without tap-pair segments.
 KernelFn pick_colpair(int P, int Q);
 KernelFn pick_colpair5(int P, int Q, bool pairs);
+// Tight-pitch instances (3x3 stride 1 pad 1, one lane row, a 32-word pitch).
+KernelFn pick_tight(int P, int Q);
 
 // Instantiates the kernels of one Q for the supported kernel widths, strides,
 // rows per lane and lane rows.

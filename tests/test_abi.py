@@ -146,10 +146,11 @@ def decode_layout(w):
                             assert m >= 0 or pe.size == 0
                             for e in pe:
                                 off = int(e["off"])
-                                cl, rem = divmod(off, info["plane"])
+                                cl, rem = divmod(off - (info["shift"] if st == 1 else 0),
+                                                 info["plane"])
                                 r, qq = divmod(rem, info["row_pitch"])
                                 if st == 1:
-                                    s = qq - info["shift"]
+                                    s = qq
                                 else:
                                     phase, qq2 = divmod(qq, info["phase_pitch"])
                                     s = qq2 * st + phase
@@ -177,9 +178,10 @@ def decode_layout(w):
                         r, s = divmod(rem, info["W"])
                         assert flags == (s == 0) | (s == 2) << 1 | (r == 0) << 2 | (r == 2) << 3
                     elif st == 1:
-                        cl, rem = divmod(off, info["plane"])
-                        r, q = divmod(rem, info["row_pitch"])
-                        s = q - info["shift"]
+                        # (the shift is -1 on tight-pitch plans: decode from the
+                        # tap's distance to the channel's first staged word)
+                        cl, rem = divmod(off - info["shift"], info["plane"])
+                        r, s = divmod(rem, info["row_pitch"])
                     else:
                         cl, rem = divmod(off, info["plane"])
                         r, q = divmod(rem, info["row_pitch"])
@@ -246,6 +248,9 @@ def test_packed_layout_decodes_to_csr(name, fmt):
         assert info["tile_cols"] * info["lane_rows"] == 32
     if info["plane_stage"]:  # whole raw planes, the padding applied to the weights
         assert info["in_rows"] == L.H == tile_h and info["in_cols"] == L.W <= info["tile_cols"]
+    elif info["shift"] == -1:  # tight pitch: 32 columns from column 0, the halo implicit
+        assert info["in_rows"] == (tile_h - 1) * L.stride + L.R
+        assert info["in_cols"] == info["row_pitch"] == 32 and L.W <= 31 and info["tiles_x"] == 1
     else:
         assert info["in_rows"] == (tile_h - 1) * L.stride + L.R
         assert info["in_cols"] == (info["tile_cols"] - 1) * L.stride + L.S

@@ -541,3 +541,52 @@ def test_image_pair_5x5(case, integer):
     got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 5, 5, 1, pad, batch_hint=hint)
     ref, mag = oracle.csr(x, rowptr, colidx, value, M, 5, 5, 1, pad)
     check(got, ref, mag, exact=integer, what=f"5x5 image pairs {case}")
+
+
+TIGHT_CASES = [
+    # (N run, N planned, C, H, W, M, density, heavy every, heavy density, Q, chunks, cluster):
+    # 3x3 pad-1 layers up to 31 wide in one column-per-lane tile column, staged from column 0
+    # at a 32-word pitch (the copy's zero fill stands in for the halo columns; the first
+    # row's left tap reads the zeroed lead)
+    (8, 8, 64, 28, 28, 96, 0.1, 0, 0.0, 4, 1, 1),        # one chunk
+    (6, 8, 300, 28, 28, 64, 0.03, 0, 0.0, 4, 5, 5),      # partial last chunk, cluster split
+    (3, 3, 77, 35, 20, 40, 0.15, 0, 0.0, 4, 1, None),    # 20 wide: eight columns of zeros
+    (16, 16, 64, 28, 28, 512, 0.01, 0, 0.0, 8, 1, 1),    # eight channels per warp
+    (2, 0, 48, 28, 28, 24, 0.2, 0, 0.0, 1, 1, None),     # batch unknown at pack time
+    (4, 4, 64, 28, 28, 64, 0.05, 16, 0.9, 4, 1, None),   # heavy rows split over warps
+    (1, 1, 300, 28, 28, 16, 0.1, 0, 0.0, 1, 8, 8),       # one image: 8-block cluster (push)
+    (1, 1, 300, 28, 28, 32, 0.05, 8, 0.8, 1, 8, 8),      # cluster + split rows (pull)
+    (8, 8, 256, 28, 28, 512, 0.15, 5, 0.7, 4, 13, 1),    # dense-tap groups (window at pitch 32)
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", TIGHT_CASES, ids=[str(c[:9]) for c in TIGHT_CASES])
+@pytest.mark.parametrize("integer", [False, True])
+@pytest.mark.parametrize("fmt", ["f32", "packed32"])
+def test_tight_pitch(case, integer, fmt):
+    N, hint, C, H, W, M, d, every, hd, want_q, want_nch, want_cluster = case
+    rng = np.random.default_rng(abs(hash(case[:9])) % (2 ** 32) + integer)
+    rows = [np.nonzero(rng.random(C * 9) < (hd if every and m % every == 0 else d))[0]
+            for m in range(M)]
+    rowptr = np.concatenate([[0], np.cumsum([r.size for r in rows])]).astype(np.int32)
+    colidx = np.concatenate(rows).astype(np.int32)
+    if integer:
+        value = rng.choice(np.array([-3, -2, -1, 1, 2, 3], np.float32), size=colidx.size)
+    else:
+        value = rng.normal(0, 0.05, size=colidx.size).astype(np.float32)
+    if fmt == "packed32":  # the 32-bit word holds FP16 values
+        value = value.astype(np.float16).astype(np.float32)
+    x = workloads.random_input((N, C, H, W), rng, integer=integer)
+    w = swd.pack_host(rowptr, colidx, value, C=C, H=H, W=W, M=M, R=3, S=3, stride=1, pad=1,
+                      batch_hint=hint, fmt=fmt)
+    info = w.info()
+    assert info["shift"] == -1 and info["row_pitch"] == 32 and info["col_blocks"] == 0
+    if fmt == "f32":
+        assert info["slots_per_warp"] == want_q and info["num_chunks"] == want_nch
+        if want_cluster is not None:
+            assert w.launch_info(N)["cluster"] == want_cluster
+    w.close()
+    got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 3, 3, 1, 1, batch_hint=hint, fmt=fmt)
+    ref, mag = oracle.csr(x, rowptr, colidx, value, M, 3, 3, 1, 1)
+    check(got, ref, mag, exact=integer, what=f"tight pitch {fmt} {case[:9]}")
