@@ -323,7 +323,10 @@ def test_launch_plans():
     L, info, pl = plan("sweep50", 8, batch_hint=8)
     assert info["col_blocks"] == 1 and info["tile_images"] == 2 and info["lane_rows"] == 4
     assert (info["tile_rows"], info["tile_cols"], info["tiles_y"], info["tiles_x"]) == (7, 28, 7, 1)
-    assert pl["grid_x"] * pl["grid_y"] == 4 * 7 * info["groups"]  # 4 image pairs x 7 row bands
+    # 4 image pairs x 7 row bands; most groups dense-tap: every tile's chunks split over a
+    # two-block cluster, halving the long dense-tap blocks
+    assert pl["grid_x"] * pl["grid_y"] == 4 * 7 * info["groups"] * 2 and pl["cluster"] == 2
+    assert 2 * info["dense_groups"] >= info["groups"]
     assert info["dense_groups"] > 0
     L, info, pl = plan("sweep90", 8, batch_hint=8)  # mostly sparse rows: column-per-lane tiles
     assert info["col_blocks"] == 0 and info["lane_rows"] == 1 and info["tile_cols"] == 32

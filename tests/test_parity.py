@@ -590,3 +590,20 @@ def test_tight_pitch(case, integer, fmt):
     got = run_gpu(x, rowptr, colidx, value, C, H, W, M, 3, 3, 1, 1, batch_hint=hint, fmt=fmt)
     ref, mag = oracle.csr(x, rowptr, colidx, value, M, 3, 3, 1, 1)
     check(got, ref, mag, exact=integer, what=f"tight pitch {fmt} {case[:9]}")
+
+
+@pytest.mark.gpu
+def test_dense_dominated_split_bit_exact():
+    """The 50 % lognormal layer at its batch: most groups are dense-tap, so every
+    tile's chunks are split over a two-block cluster and the dense-tap
+    partial sums meet in the cluster reduction.  Integer weights and inputs:
+    bit-exact against the oracle."""
+    import dataclasses
+    L = dataclasses.replace(workloads.LAYERS["sweep50"], integer=True, name="sweep50_int")
+    rowptr, colidx, value = workloads.make_weights(L)
+    w = swd.pack_host(rowptr, colidx, value, C=L.C, H=L.H, W=L.W, M=L.M, R=L.R, S=L.S,
+                      stride=L.stride, pad=L.pad, batch_hint=L.N)
+    info, launch = w.info(), w.launch_info(L.N)
+    assert launch["cluster"] == 2 and 2 * info["dense_groups"] >= info["groups"]
+    w.close()
+    layer_case(L)
