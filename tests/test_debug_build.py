@@ -10,10 +10,10 @@ The GPU test builds that library and runs, in a child process bound to it
 write-back paths at their edges -- edge shapes, heavy and dense rows, empty
 rows, both cluster reductions, tap pairs, plane staging, column blocks (one
 image and image pairs, 3x3 and 5x5), tight-pitch tiles, the 32-bit word
-format and the weight-stationary kernel.  Every GPU helper of
-those suites asserts that the device error word is clear after each forward,
-so a single failed check fails the run; outputs are compared with the oracle
-as usual (a skipped access would also show there)."""
+format, the weight-stationary kernel and the seeded random layers.  Every
+GPU helper of those suites asserts that the device error word is clear after
+each forward, so a single failed check fails the run; outputs are compared
+with the oracle as usual (a skipped access would also show there)."""
 import os
 import subprocess
 import sys
@@ -35,6 +35,7 @@ SUITES = [
     "tests/test_parity.py::test_tight_pitch",
     "tests/test_parity.py::test_packed32_format",
     "tests/test_ws.py",
+    "tests/test_random_shapes.py",
 ]
 
 
