@@ -294,11 +294,12 @@ int plan_tiles(spconv::Geometry &g, int C, int H, int W, int M, int R, int S, in
 // (densest first, dealt round-robin over the warps).  The rest are sparse:
 // they are spread over the sparse groups longest row first onto the group with
 // the least work that has room; a row heavier than 1.1x (1.5x for short
-// warps) a warp's fair share is split into parts (its column-ordered nonzeros dealt round-robin, so every
-// part spans all chunks), and inside each group the parts are bound to warp
-// slots longest first onto the least-loaded warp with a free slot.  The parts
-// of one row stay in one group and are summed in the epilogue.  Sets groups,
-// num_slots, slot_oc, slot_next, group_flags and the per-slot entry lists.
+// warps) a warp's fair share is split into parts (its column-ordered nonzeros
+// dealt round-robin, so every part spans all chunks), and inside each group
+// the parts are bound to warp slots longest first onto the least-loaded warp
+// with a free slot.  The parts of one row stay in one group and are summed in
+// the epilogue.  Sets groups, num_slots, slot_oc, slot_next, group_flags and
+// the per-slot entry lists.
 int bin_channels(spconv_packed &P, const int32_t *rowptr, const int32_t *colidx) {
     spconv::Geometry &g = P.g;
     const int per_group = g.warps * g.slots;
